@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in the CPU oracle and check that the pins catch each one.
+
+Each mutant rewrites one expression of one oracle function (a dropped term, a wrong
+index or sign, an off-by-one, a swapped operand), installs it in place of the
+original for the duration of the test, and runs every pin. At least one pin must
+fail. Nothing here touches a GPU.
+"""
+import inspect
+import textwrap
+
+import pytest
+
+import oracle.paged_kv_oracle as O
+from tests import pins
+
+MUTANTS = [
+    ("slot_of", "* BLOCK_SIZE + pos % BLOCK_SIZE", "* (BLOCK_SIZE - 1) + pos % BLOCK_SIZE"),
+    ("slot_of", "+ pos % BLOCK_SIZE", "+ (pos + 1) % BLOCK_SIZE"),
+    ("slot_of", "block_table_row[pos // BLOCK_SIZE]", "block_table_row[-1 - pos // BLOCK_SIZE]"),
+    ("query_positions", "pos[start + i] = L - n + i", "pos[start + i] = L - n + i - 1"),
+    ("query_positions", "pos[start + i] = L - n + i", "pos[start + i] = n - 1 - i"),
+    ("kv_head_of", "return h // (H_q // H_kv)", "return h % H_kv"),
+    ("causal_softmax_attention", "<= np.asarray(positions)", "< np.asarray(positions)"),
+    ("causal_softmax_attention", "S = (Q @ K.T) * scale", "S = (Q @ K.T)"),
+    ("causal_softmax_attention", "S = (Q @ K.T) * scale", "S = (Q @ K.T) / scale"),
+    ("causal_softmax_attention", "P = E / E.sum(axis=1, keepdims=True)", "P = E"),
+    ("causal_softmax_attention", "return P @ V, P", "return P @ K, P"),
+    ("causal_softmax_attention", "np.exp(S - m)", "np.exp(m - S)"),
+    ("paged_attention", "Vb = decode_bits(gather_context(v_pool", "Vb = decode_bits(gather_context(k_pool"),
+    ("paged_attention", "qf[rs, h, :]", "qf[rs, kv, :]"),
+    ("gather_context", "flat[slot_of(block_table_row, j)]", "flat[slot_of(block_table_row, L - 1 - j)]"),
+    ("reshape_and_cache", "vp[s] = v[t]", "vp[s] = k[t]"),
+    ("reshape_and_cache", "if s < 0:", "if s <= 0:"),
+    ("decode_bits", "<< 16", "<< 15"),
+]
+
+
+def _mutated(name, old, new):
+    src = textwrap.dedent(inspect.getsource(getattr(O, name)))
+    assert src.count(old) == 1, (name, old)
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    return ns[name]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[f"{m[0]}:{m[2]}" for m in MUTANTS])
+def test_mutant_is_caught(monkeypatch, name, old, new):
+    monkeypatch.setattr(O, name, _mutated(name, old, new))
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(O)
+        except Exception as e:  # an assertion or a crash both count as caught
+            failed.append((pin.__name__, type(e).__name__))
+    assert failed, f"no pin caught the mutant {name}: {old!r} -> {new!r}"
