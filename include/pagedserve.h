@@ -1,0 +1,182 @@
+/*
+ * pagedserve.h -- C ABI of the GB300 (sm_103a) paged KV attention library.
+ *
+ * One attention step over a paged KV cache for a packed ragged batch:
+ *   1. ps_slot_mapping       -- the pool slot of every packed token;
+ *   2. ps_reshape_and_cache  -- scatter each token's K/V row into the pool at its slot;
+ *   3. ps_paged_attention    -- causal grouped-query attention of every packed query row
+ *                               over its sequence's context, read through block tables.
+ *
+ * Sources (three web pages on paged KV serving):
+ *   - PageServe, section 01 "Scheduler loop": one packed [1, T] forward per step with
+ *     explicit position ids and a slot mapping per token; the forward writes K/V into the
+ *     pool and reads context via block tables; a token's slot is
+ *     block_table[pos // 16] * 16 + pos % 16; every step computes the tokens that do not
+ *     yet have K/V ("num_computed_tokens").
+ *   - PageServe, section 03 "Paged KV cache" and development-history phases 6-8: fixed
+ *     16-token blocks in one pre-allocated pool [layers, blocks, 16, H, D]; per-sequence
+ *     block tables; a custom attention backend that scatters new K/V and attends through
+ *     the table.
+ *   - tinyserve, "How it works": K/V slabs [layers, blocks x 16, H_kv, D] (the same memory
+ *     order); shared prefix blocks referenced from several tables; one fused pass over a
+ *     flattened ragged batch mixing prefill chunks and decodes; k+1 speculative-verify
+ *     tokens scored at once under a stepped causal mask; grouped-query attention
+ *     ("Highlights" table, forward-pass row).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller, unless the argument says
+ *     otherwise. The library allocates no device memory and keeps no pointer after return.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and returns PS_OK once its kernels are enqueued, or a negative ps_status.
+ *     Host-side argument errors are detected before anything is enqueued.
+ *   - Tensors are dense and row-major with the shapes given. 16-bit values are IEEE fp16
+ *     or bfloat16 as `dtype` says. Tensor pointers must be 16-byte aligned.
+ *   - Block size is 16 tokens. head_dim D is 64 or 128. H_q is a multiple of H_kv; query
+ *     head h reads KV head h / (H_q / H_kv).
+ *   - Device-side index errors (a block id outside the pool, a slot past the pool, a
+ *     sequence with more query tokens than context) never trap: the kernel records the
+ *     first such error in the library's device error word (ps_get_device_error) and
+ *     skips the access; the affected outputs are left unwritten.
+ */
+#ifndef PAGEDSERVE_H
+#define PAGEDSERVE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PS_BLOCK_SIZE 16
+
+typedef enum { PS_F16 = 0, PS_BF16 = 1 } ps_dtype;
+
+typedef enum {
+  PS_OK = 0,
+  PS_ERR_ARG = -1,          /* a size, count or required pointer is invalid            */
+  PS_ERR_UNSUPPORTED = -2,  /* dtype, head_dim or head counts not supported            */
+  PS_ERR_ALIGN = -3,        /* a tensor pointer is not 16-byte aligned                 */
+  PS_ERR_WORKSPACE = -4,    /* workspace missing, misaligned or too small              */
+  PS_ERR_CUDA = -5          /* a CUDA call or kernel launch failed                     */
+} ps_status;
+
+/* Device error codes reported by ps_get_device_error. */
+typedef enum {
+  PS_DEV_OK = 0,
+  PS_DEV_BAD_BLOCK_ID = 1,   /* a block-table entry outside [0, num_blocks)            */
+  PS_DEV_BAD_SLOT = 2,       /* a slot_mapping entry >= num_blocks * 16                */
+  PS_DEV_BAD_SEQUENCE = 3,   /* query count > context, or context beyond the table     */
+  PS_DEV_WAIT_TIMEOUT = 4,   /* a kernel's bounded wait ran out (the kernel returned)  */
+  PS_DEV_PLAN_OVERFLOW = 5   /* the work plan did not fit the workspace                */
+} ps_device_error;
+
+/*
+ * ps_slot_mapping -- slot of every packed query token (PageServe section 01).
+ *
+ *   block_tables     int32 [B, max_blocks_per_seq]: physical block ids of each sequence;
+ *                    entries past a sequence's context are never read.
+ *   seq_lens         int32 [B]: context length of each sequence AFTER this step's tokens.
+ *   query_start_loc  int32 [B + 1]: packed offsets, [0] = 0, [B] = T, non-decreasing.
+ *                    Sequence b owns packed tokens [query_start_loc[b], query_start_loc[b+1]).
+ *   slot_mapping     int32 [T], written: for token i of the n_b tokens of sequence b,
+ *                    pos = seq_lens[b] - n_b + i and
+ *                    slot = block_tables[b][pos / 16] * 16 + pos % 16;
+ *                    -1 (and a device error) where the entry would be invalid.
+ *   num_blocks       pool size in blocks, for the bounds check.
+ * B = 0 requires T = 0. Returns PS_ERR_ARG for negative sizes or null pointers with T > 0.
+ */
+int ps_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* seq_lens, const int32_t* query_start_loc, int B, int T,
+                    int num_blocks, int32_t* slot_mapping, void* stream);
+
+/*
+ * ps_reshape_and_cache -- KV scatter (PageServe section 01 "Execute"; section 03).
+ *
+ *   k, v          [T, H_kv, D] of dtype: the new tokens' keys and values.
+ *   slot_mapping  int32 [T]: destination slot of each token; a negative slot skips the
+ *                 token; a slot >= num_blocks * 16 is skipped and recorded as
+ *                 PS_DEV_BAD_SLOT.
+ *   k_pool, v_pool [num_blocks, 16, H_kv, D] of dtype, updated in place:
+ *                 pool[slot / 16, slot % 16, :, :] = k[t] (bit-exact copy).
+ * Two tokens mapped to one slot leave one of the two rows (which one is unspecified).
+ */
+int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping,
+                         void* k_pool, void* v_pool, int T, int H_kv, int D, int num_blocks,
+                         int dtype, void* stream);
+
+/*
+ * ps_paged_attention_workspace_size -- bytes of device workspace ps_paged_attention wants
+ * for a batch of at most T packed tokens, B sequences and contexts of at most
+ * max_seq_len tokens. A smaller workspace (at least the size returned for
+ * max_seq_len = 0) still works; the attention then splits long contexts into fewer parts.
+ */
+size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
+                                         int max_seq_len);
+
+/*
+ * ps_paged_attention -- causal paged attention over a packed ragged batch.
+ *
+ * For packed row r = query_start_loc[b] + i of sequence b (n_b rows, context
+ * L_b = seq_lens[b], position p = L_b - n_b + i) and query head h, with G = H_q / H_kv:
+ *     out[r, h, :] = sum_{j <= p} softmax_j(scale * q[r, h, :] . K_b[j]) V_b[j]
+ * where K_b[j] = k_pool[block_tables[b][j / 16], j % 16, h / G, :] (V likewise).
+ * One-token decodes, k+1-token speculative-verify rows and prefill chunks mix freely
+ * (PageServe section 01; tinyserve "How it works").
+ *
+ *   q              [T, H_q, D] of dtype.
+ *   k_pool, v_pool [num_blocks, 16, H_kv, D] of dtype (already holding this step's K/V).
+ *   block_tables, seq_lens, query_start_loc  as for ps_slot_mapping; 0 <= n_b <= L_b.
+ *   scale          softmax scale (normally 1 / sqrt(D)).
+ *   out            [T, H_q, D] of dtype, written for every packed row.
+ *   workspace      device scratch of workspace_bytes bytes, 256-byte aligned, owned by the
+ *                  caller; contents on entry are ignored and on return are undefined.
+ *                  Calls that share a workspace must not overlap on the device.
+ * Accumulation is fp32; the output is rounded to dtype.
+ */
+int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, const int32_t* query_start_loc, int B, int T,
+                       int H_q, int H_kv, int D, int num_blocks, float scale, void* out,
+                       void* workspace, size_t workspace_bytes, int dtype, void* stream);
+
+/*
+ * ps_attention_step -- the whole step in one call: ps_slot_mapping, ps_reshape_and_cache,
+ * then ps_paged_attention, on one stream. k, v are the step's new tokens [T, H_kv, D];
+ * slot_mapping is caller-provided device scratch of T int32 (written). Other arguments as
+ * above.
+ */
+int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens, const int32_t* query_start_loc, int B, int T,
+                      int H_q, int H_kv, int D, int num_blocks, float scale, void* out,
+                      int32_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                      int dtype, void* stream);
+
+/*
+ * ps_get_device_error -- read (and clear) the device error word of the current device.
+ * Synchronises with the device. *code receives a ps_device_error value. Returns PS_OK or
+ * PS_ERR_CUDA / PS_ERR_ARG.
+ */
+int ps_get_device_error(int* code);
+
+/* Human-readable name of a ps_status value. The string is static. */
+const char* ps_status_string(int status);
+
+/*
+ * Kernel timing hook for benchmarks. ps_profile_begin(n) starts recording CUDA events
+ * around the next n launches of each kernel kind (host memory only; events are created
+ * here, not in the timed calls). ps_profile_end() waits for the recorded events and
+ * stops recording. ps_profile_read(kind, &ms, &launches) then gives the summed device
+ * time and the launch count of one kind: 0 slot mapping, 1 KV scatter, 2 planner,
+ * 3 split attention, 4 split combine.
+ */
+int ps_profile_begin(int max_launches_per_kind);
+int ps_profile_end(void);
+int ps_profile_read(int kind, float* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDSERVE_H */

@@ -1,0 +1,182 @@
+"""Python binding of the C ABI: argument marshalling from torch tensors, nothing else.
+
+Every function checks that its tensors live on the current CUDA device, are
+contiguous and have the expected dtypes and shapes, passes their addresses and the
+current stream to the matching ``ps_*`` entry point of include/pagedserve.h, and
+raises :class:`PagedServeError` on a non-zero status. All arithmetic happens in the
+library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+BLOCK_SIZE = 16
+
+# kernel kinds of the timing hook
+PROFILE_KINDS = {"slot_mapping": 0, "reshape_and_cache": 1, "plan": 2, "split_attention": 3,
+                 "combine": 4}
+
+
+class PagedServeError(RuntimeError):
+    pass
+
+
+def lib():
+    return _lib.load()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        msg = lib().ps_status_string(rc).decode()
+        raise PagedServeError(f"{what} failed: {msg} ({rc})")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise PagedServeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PagedServeError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise PagedServeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise PagedServeError(f"{name} must have {ndim} dimensions, has {t.dim()}")
+    return t.data_ptr()
+
+
+def _batch(block_tables, seq_lens, query_start_loc):
+    bt = _dev(block_tables, "block_tables", torch.int32, 2)
+    sl = _dev(seq_lens, "seq_lens", torch.int32, 1)
+    qs = _dev(query_start_loc, "query_start_loc", torch.int32, 1)
+    B = seq_lens.shape[0]
+    if block_tables.shape[0] != B or query_start_loc.shape[0] != B + 1:
+        raise PagedServeError("block_tables / query_start_loc do not match seq_lens")
+    return bt, sl, qs, B, block_tables.shape[1]
+
+
+def slot_mapping(block_tables, seq_lens, query_start_loc, T: int, num_blocks: int, out=None,
+                 stream=None) -> torch.Tensor:
+    """int32 [T]: pool slot of every packed query token (ps_slot_mapping)."""
+    bt, sl, qs, B, maxblk = _batch(block_tables, seq_lens, query_start_loc)
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=seq_lens.device)
+    o = _dev(out, "slot_mapping", torch.int32, 1)
+    _check(lib().ps_slot_mapping(bt, maxblk, sl, qs, B, T, num_blocks, o, _stream(stream)),
+           "ps_slot_mapping")
+    return out
+
+
+def reshape_and_cache(k, v, slot_mapping_t, k_pool, v_pool, stream=None) -> None:
+    """Write k/v [T, H_kv, D] into the pools [NB, 16, H_kv, D] at the slots (in place)."""
+    dt = tuple(DTYPE_CODE)
+    kp = _dev(k, "k", dt, 3)
+    vp = _dev(v, "v", k.dtype, 3)
+    sp = _dev(slot_mapping_t, "slot_mapping", torch.int32, 1)
+    kpp = _dev(k_pool, "k_pool", k.dtype, 4)
+    vpp = _dev(v_pool, "v_pool", k.dtype, 4)
+    T, H_kv, D = k.shape
+    if v.shape != k.shape or slot_mapping_t.shape[0] != T or k_pool.shape != v_pool.shape \
+            or tuple(k_pool.shape[1:]) != (BLOCK_SIZE, H_kv, D):
+        raise PagedServeError("reshape_and_cache: inconsistent shapes")
+    _check(lib().ps_reshape_and_cache(kp, vp, sp, kpp, vpp, T, H_kv, D, k_pool.shape[0],
+                                      DTYPE_CODE[k.dtype], _stream(stream)),
+           "ps_reshape_and_cache")
+
+
+def workspace_size(T: int, B: int, H_q: int, H_kv: int, D: int, max_seq_len: int) -> int:
+    return int(lib().ps_paged_attention_workspace_size(T, B, H_q, H_kv, D, max_seq_len))
+
+
+def alloc_workspace(T, B, H_q, H_kv, D, max_seq_len, device=None) -> torch.Tensor:
+    n = max(workspace_size(T, B, H_q, H_kv, D, max_seq_len), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, scale: float,
+                    out=None, workspace=None, max_seq_len: int | None = None,
+                    stream=None) -> torch.Tensor:
+    """Causal paged attention of every packed query row (ps_paged_attention)."""
+    qp = _dev(q, "q", tuple(DTYPE_CODE), 3)
+    kpp = _dev(k_pool, "k_pool", q.dtype, 4)
+    vpp = _dev(v_pool, "v_pool", q.dtype, 4)
+    bt, sl, qs, B, maxblk = _batch(block_tables, seq_lens, query_start_loc)
+    T, H_q, D = q.shape
+    NB, bs, H_kv, Dk = k_pool.shape
+    if bs != BLOCK_SIZE or Dk != D or v_pool.shape != k_pool.shape:
+        raise PagedServeError("paged_attention: inconsistent pool shape")
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev(out, "out", q.dtype, 3)
+    if tuple(out.shape) != tuple(q.shape):
+        raise PagedServeError("out must have q's shape")
+    if workspace is None:
+        msl = max_seq_len if max_seq_len is not None else maxblk * BLOCK_SIZE
+        workspace = alloc_workspace(T, B, H_q, H_kv, D, msl, device=q.device)
+    wp = _dev(workspace, "workspace", torch.uint8, 1)
+    _check(lib().ps_paged_attention(qp, kpp, vpp, bt, maxblk, sl, qs, B, T, H_q, H_kv, D, NB,
+                                    float(scale), op, wp, workspace.numel(),
+                                    DTYPE_CODE[q.dtype], _stream(stream)),
+           "ps_paged_attention")
+    return out
+
+
+def attention_step(q, k, v, k_pool, v_pool, block_tables, seq_lens, query_start_loc,
+                   scale: float, out=None, workspace=None, slot_buf=None,
+                   max_seq_len: int | None = None, stream=None) -> torch.Tensor:
+    """Slot mapping, KV scatter and paged attention of one step (ps_attention_step)."""
+    qp = _dev(q, "q", tuple(DTYPE_CODE), 3)
+    kp = _dev(k, "k", q.dtype, 3)
+    vp = _dev(v, "v", q.dtype, 3)
+    kpp = _dev(k_pool, "k_pool", q.dtype, 4)
+    vpp = _dev(v_pool, "v_pool", q.dtype, 4)
+    bt, sl, qs, B, maxblk = _batch(block_tables, seq_lens, query_start_loc)
+    T, H_q, D = q.shape
+    NB, _, H_kv, _ = k_pool.shape
+    if k.shape != (T, H_kv, D) or v.shape != k.shape:
+        raise PagedServeError("attention_step: k/v shape")
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev(out, "out", q.dtype, 3)
+    if slot_buf is None:
+        slot_buf = torch.empty(T, dtype=torch.int32, device=q.device)
+    sp = _dev(slot_buf, "slot_buf", torch.int32, 1)
+    if workspace is None:
+        msl = max_seq_len if max_seq_len is not None else maxblk * BLOCK_SIZE
+        workspace = alloc_workspace(T, B, H_q, H_kv, D, msl, device=q.device)
+    wp = _dev(workspace, "workspace", torch.uint8, 1)
+    _check(lib().ps_attention_step(qp, kp, vp, kpp, vpp, bt, maxblk, sl, qs, B, T, H_q, H_kv, D,
+                                   NB, float(scale), op, sp, wp, workspace.numel(),
+                                   DTYPE_CODE[q.dtype], _stream(stream)),
+           "ps_attention_step")
+    return out
+
+
+def device_error() -> int:
+    """Read and clear the device error word (synchronises)."""
+    code = ctypes.c_int(0)
+    _check(lib().ps_get_device_error(ctypes.addressof(code)), "ps_get_device_error")
+    return code.value
+
+
+def profile_begin(max_launches_per_kind: int) -> None:
+    _check(lib().ps_profile_begin(max_launches_per_kind), "ps_profile_begin")
+
+
+def profile_end() -> dict:
+    _check(lib().ps_profile_end(), "ps_profile_end")
+    res = {}
+    for name, kind in PROFILE_KINDS.items():
+        ms, n = ctypes.c_float(0), ctypes.c_int(0)
+        _check(lib().ps_profile_read(kind, ctypes.addressof(ms), ctypes.addressof(n)),
+               "ps_profile_read")
+        res[name] = (ms.value, n.value)
+    return res

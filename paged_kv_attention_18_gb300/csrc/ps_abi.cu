@@ -1,0 +1,388 @@
+// C ABI of the paged KV attention library: argument validation, workspace layout,
+// TMA descriptors, kernel launches and the benchmark timing hook.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pagedserve.h"
+#include "ps_common.cuh"
+#include "ps_launch.h"
+
+namespace {
+
+__device__ int g_device_error;  // the library's device error word (one per device)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  int num_sms = 0;
+  int* err = nullptr;  // device address of g_device_error
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.init) {
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PS_ERR_CUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return PS_ERR_CUDA;
+    s.err = static_cast<int*>(addr);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return PS_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.init = true;
+  }
+  *out = &s;
+  return PS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------------
+struct Layout {
+  size_t hdr, items, seq_off, tok_ns, tok_base, fixed_end;
+  int cap_items;
+};
+
+Layout fixed_layout(int T, int B, int H_q, int H_kv) {
+  Layout l;
+  const int64_t G = H_q / H_kv;
+  const int64_t groups = (static_cast<int64_t>(T) * G + 15) / 16;
+  const int64_t split_seqs = B < T ? B : T;
+  int64_t cap = static_cast<int64_t>(H_kv) *
+                (groups + B + split_seqs * ps::kSplitGroupLimit * (ps::kMaxSplits - 1));
+  if (cap < 1) cap = 1;
+  l.cap_items = static_cast<int>(cap);
+  l.hdr = 0;
+  l.items = 256;
+  l.seq_off = align_up(l.items + static_cast<size_t>(cap) * sizeof(ps::WorkItem), 256);
+  l.tok_ns = align_up(l.seq_off + static_cast<size_t>(B + 1) * 4, 256);
+  l.tok_base = align_up(l.tok_ns + static_cast<size_t>(T) * 4, 256);
+  l.fixed_end = align_up(l.tok_base + static_cast<size_t>(T) * 4, 256);
+  return l;
+}
+
+size_t partial_bytes(int64_t cap_part, int D) {
+  return align_up(static_cast<size_t>(cap_part) * 4, 256) + static_cast<size_t>(cap_part) * D * 4;
+}
+
+// ---------------------------------------------------------------------------------
+// timing hook
+// ---------------------------------------------------------------------------------
+constexpr int kKinds = 5;
+struct Profile {
+  bool on = false;
+  int cap = 0;
+  std::vector<cudaEvent_t> ev[kKinds];  // pairs: start, stop
+  int used[kKinds] = {0, 0, 0, 0, 0};
+  float ms[kKinds] = {0, 0, 0, 0, 0};
+  int done[kKinds] = {0, 0, 0, 0, 0};
+};
+Profile g_prof;
+std::mutex g_prof_mu;
+
+struct Timed {
+  cudaEvent_t stop = nullptr;
+  cudaStream_t stream;
+  Timed(int kind, cudaStream_t s) : stream(s) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof.on || g_prof.used[kind] >= g_prof.cap) return;
+    const int i = g_prof.used[kind]++;
+    cudaEventRecord(g_prof.ev[kind][2 * i], s);
+    stop = g_prof.ev[kind][2 * i + 1];
+  }
+  ~Timed() {
+    if (stop) cudaEventRecord(stop, stream);
+  }
+};
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PS_OK : PS_ERR_CUDA; }
+
+int make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, int D, bool bf16) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H_kv) * D,
+                              static_cast<cuuint64_t>(num_blocks) * PS_BLOCK_SIZE};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H_kv) * D * 2};
+  const cuuint32_t box[2] = {64, PS_BLOCK_SIZE};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(
+      map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+      const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PS_OK : PS_ERR_CUDA;
+}
+
+int check_shapes(int H_q, int H_kv, int D, int dtype) {
+  if (H_q <= 0 || H_kv <= 0) return PS_ERR_ARG;
+  if (dtype != PS_F16 && dtype != PS_BF16) return PS_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PS_ERR_UNSUPPORTED;
+  if (H_q % H_kv != 0) return PS_ERR_UNSUPPORTED;
+  return PS_OK;
+}
+
+int check_batch(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                const int32_t* qsl, int B, int T, int num_blocks) {
+  if (B < 0 || T < 0 || max_blocks < 0 || num_blocks <= 0) return PS_ERR_ARG;
+  if (B == 0 && T != 0) return PS_ERR_ARG;
+  if (static_cast<int64_t>(num_blocks) * PS_BLOCK_SIZE > INT32_MAX) return PS_ERR_ARG;
+  if (B > 0 && (!seq_lens || !qsl || !block_tables || max_blocks == 0)) return PS_ERR_ARG;
+  return PS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ps_status_string(int status) {
+  switch (status) {
+    case PS_OK: return "PS_OK";
+    case PS_ERR_ARG: return "PS_ERR_ARG: invalid size, count or pointer";
+    case PS_ERR_UNSUPPORTED: return "PS_ERR_UNSUPPORTED: dtype, head_dim or head counts";
+    case PS_ERR_ALIGN: return "PS_ERR_ALIGN: tensor pointer not 16-byte aligned";
+    case PS_ERR_WORKSPACE: return "PS_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PS_ERR_CUDA: return "PS_ERR_CUDA: CUDA call or kernel launch failed";
+    default: return "unknown ps_status";
+  }
+}
+
+int ps_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    const int32_t* query_start_loc, int B, int T, int num_blocks,
+                    int32_t* slot_mapping, void* stream) {
+  int rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
+                       num_blocks);
+  if (rc) return rc;
+  if (T > 0 && !slot_mapping) return PS_ERR_ARG;
+  if (T == 0) return PS_OK;
+  DeviceState* ds;
+  if ((rc = current_device_state(&ds))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timed tm(0, s);
+  return cuda_status(ps::launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens,
+                                             query_start_loc, B, T, num_blocks, slot_mapping,
+                                             ds->err, s));
+}
+
+int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, void* k_pool,
+                         void* v_pool, int T, int H_kv, int D, int num_blocks, int dtype,
+                         void* stream) {
+  int rc = check_shapes(H_kv, H_kv, D, dtype);
+  if (rc) return rc;
+  if (T < 0 || num_blocks <= 0) return PS_ERR_ARG;
+  if (static_cast<int64_t>(num_blocks) * PS_BLOCK_SIZE > INT32_MAX) return PS_ERR_ARG;
+  if (T == 0) return PS_OK;
+  if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PS_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PS_ERR_ALIGN;
+  DeviceState* ds;
+  if ((rc = current_device_state(&ds))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timed tm(1, s);
+  return cuda_status(ps::launch_reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, T, H_kv, D,
+                                                  num_blocks, ds->err, ds->num_sms, s));
+}
+
+size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
+                                         int max_seq_len) {
+  if (T < 0 || B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || (D != 64 && D != 128))
+    return 0;
+  const Layout l = fixed_layout(T, B, H_q, H_kv);
+  int64_t splits = (static_cast<int64_t>(max_seq_len) + ps::kBlockSize * ps::kMinSplitPages - 1) /
+                   (ps::kBlockSize * ps::kMinSplitPages);
+  if (splits > ps::kMaxSplits) splits = ps::kMaxSplits;
+  if (splits < 2) splits = 0;  // nothing to split
+  const int64_t cap_part = static_cast<int64_t>(T) * H_q * splits;
+  return l.fixed_end + partial_bytes(cap_part, D);
+}
+
+namespace {
+// Host-side checks of ps_paged_attention's arguments (T > 0 assumed checked by caller).
+int check_attention(const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    const int32_t* query_start_loc, int B, int T, int H_q, int H_kv, int D,
+                    int num_blocks, const void* out, const void* workspace,
+                    size_t workspace_bytes, int dtype) {
+  int rc = check_shapes(H_q, H_kv, D, dtype);
+  if (rc) return rc;
+  if ((rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
+                        num_blocks)))
+    return rc;
+  if (T == 0) return PS_OK;
+  if (!q || !k_pool || !v_pool || !out) return PS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PS_ERR_ALIGN;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
+  if (workspace_bytes < fixed_layout(T, B, H_q, H_kv).fixed_end) return PS_ERR_WORKSPACE;
+  return PS_OK;
+}
+}  // namespace
+
+int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int B, int T, int H_q, int H_kv, int D,
+                       int num_blocks, float scale, void* out, void* workspace,
+                       size_t workspace_bytes, int dtype, void* stream) {
+  int rc = check_attention(q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
+                           query_start_loc, B, T, H_q, H_kv, D, num_blocks, out, workspace,
+                           workspace_bytes, dtype);
+  if (rc) return rc;
+  if (T == 0) return PS_OK;
+  const Layout l = fixed_layout(T, B, H_q, H_kv);
+  // the rest of the workspace holds split partials
+  int64_t cap_part = static_cast<int64_t>((workspace_bytes - l.fixed_end) / ((D + 1) * 4));
+  while (cap_part > 0 && partial_bytes(cap_part, D) > workspace_bytes - l.fixed_end) --cap_part;
+  if (cap_part > INT32_MAX) cap_part = INT32_MAX;
+
+  DeviceState* ds;
+  if ((rc = current_device_state(&ds))) return rc;
+  const bool bf16 = dtype == PS_BF16;
+  CUtensorMap kmap, vmap;
+  if ((rc = make_pool_map(&kmap, k_pool, num_blocks, H_kv, D, bf16))) return rc;
+  if ((rc = make_pool_map(&vmap, v_pool, num_blocks, H_kv, D, bf16))) return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ps::AttnParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.max_blocks = max_blocks_per_seq;
+  p.B = B;
+  p.T = T;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.D = D;
+  p.G = H_q / H_kv;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.hdr = reinterpret_cast<int*>(ws + l.hdr);
+  p.items = reinterpret_cast<ps::WorkItem*>(ws + l.items);
+  p.seq_off = reinterpret_cast<int*>(ws + l.seq_off);
+  p.tok_ns = reinterpret_cast<int*>(ws + l.tok_ns);
+  p.tok_base = reinterpret_cast<int*>(ws + l.tok_base);
+  p.part_lse = reinterpret_cast<float*>(ws + l.fixed_end);
+  p.part_o = reinterpret_cast<float*>(ws + l.fixed_end + align_up(static_cast<size_t>(cap_part) * 4, 256));
+  p.cap_items = l.cap_items;
+  p.cap_part = static_cast<int>(cap_part);
+  p.err = ds->err;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int concurrency = ps::attention_ctas(D, ds->num_sms) * ps::attention_warps(D);
+  {
+    Timed tm(2, s);
+    if (ps::launch_plan(p, concurrency, s) != cudaSuccess) return PS_ERR_CUDA;
+  }
+  {
+    Timed tm(3, s);
+    if (ps::launch_split_attention(p, bf16, kmap, vmap, ds->num_sms, s) != cudaSuccess)
+      return PS_ERR_CUDA;
+  }
+  {
+    Timed tm(4, s);
+    if (ps::launch_combine(p, bf16, s) != cudaSuccess) return PS_ERR_CUDA;
+  }
+  return PS_OK;
+}
+
+int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                      const int32_t* query_start_loc, int B, int T, int H_q, int H_kv, int D,
+                      int num_blocks, float scale, void* out, int32_t* slot_mapping,
+                      void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  // validate everything before enqueuing anything
+  int rc = check_attention(q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
+                           query_start_loc, B, T, H_q, H_kv, D, num_blocks, out, workspace,
+                           workspace_bytes, dtype);
+  if (rc) return rc;
+  if (T == 0) return PS_OK;
+  if (!k || !v || !slot_mapping) return PS_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v)) return PS_ERR_ALIGN;
+  rc = ps_slot_mapping(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
+                           num_blocks, slot_mapping, stream);
+  if (rc) return rc;
+  rc = ps_reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, T, H_kv, D, num_blocks, dtype,
+                            stream);
+  if (rc) return rc;
+  return ps_paged_attention(q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
+                            query_start_loc, B, T, H_q, H_kv, D, num_blocks, scale, out,
+                            workspace, workspace_bytes, dtype, stream);
+}
+
+int ps_get_device_error(int* code) {
+  if (!code) return PS_ERR_ARG;
+  DeviceState* ds;
+  int rc = current_device_state(&ds);
+  if (rc) return rc;
+  int v = 0;
+  if (cudaMemcpy(&v, ds->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PS_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(ds->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PS_ERR_CUDA;
+  *code = v;
+  return PS_OK;
+}
+
+int ps_profile_begin(int max_launches_per_kind) {
+  if (max_launches_per_kind <= 0) return PS_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (int k = 0; k < kKinds; ++k) {
+    for (cudaEvent_t e : g_prof.ev[k]) cudaEventDestroy(e);
+    g_prof.ev[k].assign(2 * max_launches_per_kind, nullptr);
+    for (auto& e : g_prof.ev[k])
+      if (cudaEventCreate(&e) != cudaSuccess) return PS_ERR_CUDA;
+    g_prof.used[k] = 0;
+    g_prof.ms[k] = 0.f;
+    g_prof.done[k] = 0;
+  }
+  g_prof.cap = max_launches_per_kind;
+  g_prof.on = true;
+  return PS_OK;
+}
+
+int ps_profile_end(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof.on = false;
+  for (int k = 0; k < kKinds; ++k) {
+    float total = 0.f;
+    for (int i = 0; i < g_prof.used[k]; ++i) {
+      if (cudaEventSynchronize(g_prof.ev[k][2 * i + 1]) != cudaSuccess) return PS_ERR_CUDA;
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, g_prof.ev[k][2 * i], g_prof.ev[k][2 * i + 1]) != cudaSuccess)
+        return PS_ERR_CUDA;
+      total += ms;
+    }
+    g_prof.ms[k] = total;
+    g_prof.done[k] = g_prof.used[k];
+  }
+  return PS_OK;
+}
+
+int ps_profile_read(int kind, float* total_ms, int* launches) {
+  if (kind < 0 || kind >= kKinds || !total_ms || !launches) return PS_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  *total_ms = g_prof.ms[kind];
+  *launches = g_prof.done[kind];
+  return PS_OK;
+}
+
+}  // extern "C"

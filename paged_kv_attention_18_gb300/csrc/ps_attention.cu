@@ -1,0 +1,632 @@
+// Paged attention over a packed ragged batch: planner, split kernel, split-combine.
+//
+// What is computed (PageServe section 01 "Execute": the backend reads each sequence's
+// context through its block table; tinyserve "How it works": one fused pass over a
+// flattened ragged batch, the stepped causal mask for k+1 verify tokens, grouped-query
+// attention): for every packed query row r of sequence b at position
+// p = L_b - n_b + i and every query head h,
+//     out[r, h] = softmax_j<=p( q[r, h] . K_b[j, h / G] * scale ) . V_b[j, h / G]
+// with K_b[j] read from the pool row block_table[b][j / 16] * 16 + j % 16.
+//
+// Design (GB300): a one-CTA planner turns the batch into work items on the device
+// (16 packed rows = query tokens x GQA heads of one KV head, over one split of the
+// context); a persistent split kernel lets every warp fetch items from an atomic
+// counter and stream the item's K/V pages through its own ring of TMA-filled shared
+// memory stages (128-byte swizzled, one mbarrier per stage), computing QK^T and PV with
+// mma.sync and an online softmax in registers; a combine kernel merges the splits of
+// rows whose context was split, by log-sum-exp weights.
+#include "ps_common.cuh"
+#include "ps_launch.h"
+
+namespace ps {
+
+// ----------------------------------------------------------------------------------
+// planner
+// ----------------------------------------------------------------------------------
+struct SeqInfo {
+  int n, L, valid, groups, pages, tok0;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
+  SeqInfo s;
+  s.tok0 = p.qsl[b];
+  s.n = p.qsl[b + 1] - s.tok0;
+  s.L = p.seq_lens[b];
+  s.pages = (s.L + kBlockSize - 1) / kBlockSize;
+  s.valid = s.n >= 0 && s.n <= s.L && s.pages <= p.max_blocks;
+  const int rows = s.valid ? s.n * p.G : 0;
+  s.groups = (rows + 15) / 16;
+  return s;
+}
+
+__device__ __forceinline__ int seq_splits(const SeqInfo& s, int pps) {
+  if (s.groups == 0) return 0;
+  if (s.groups > kSplitGroupLimit) return 1;
+  int ns = (s.pages + pps - 1) / pps;
+  ns = ns < 1 ? 1 : ns;
+  ns = ns > kMaxSplits ? kMaxSplits : ns;
+  return ns > s.pages ? s.pages : ns;
+}
+
+// largest b in [0, n) with arr[b] <= x (arr non-decreasing, arr[0] <= x)
+__device__ __forceinline__ int last_le(const int* arr, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (arr[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Exclusive scan over the block (blockDim.x a multiple of 32, at most 1024).
+__device__ int block_exscan(int v, int* sh, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = wid ? sh[wid - 1] : 0;
+  total = sh[nw - 1];
+  __syncthreads();
+  return prefix + x - v;
+}
+
+__device__ long long block_sum_ll(long long v, long long* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[wid] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int i = 0; i < nw; ++i) t += sh[i];
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency) {
+  __shared__ int sh[32];
+  __shared__ long long shl[32];
+  const int tid = threadIdx.x, nth = blockDim.x;
+
+  // cost of the batch in pages read (every row group reads up to the whole context)
+  long long w = 0;
+  for (int b = tid; b < p.B; b += nth) {
+    const SeqInfo s = seq_info(p, b);
+    if (!s.valid) {
+      record_error(p.err, kDevBadSequence);
+      continue;
+    }
+    w += static_cast<long long>(s.groups) * s.pages;
+  }
+  const long long W = block_sum_ll(w, shl) * p.H_kv;
+  const long long target = static_cast<long long>(concurrency) * 4;
+  long long pps_ll = (W + target - 1) / (target > 0 ? target : 1);
+  int pps = static_cast<int>(pps_ll < kMinSplitPages ? kMinSplitPages
+                             : (pps_ll > (1 << 24) ? (1 << 24) : pps_ll));
+
+  int n_items = 0, n_part = 0;
+  for (int attempt = 0; attempt < 32; ++attempt) {
+    // items of every sequence
+    int running = 0;
+    for (int base = 0; base < p.B; base += nth) {
+      const int b = base + tid;
+      int cnt = 0;
+      if (b < p.B) {
+        const SeqInfo s = seq_info(p, b);
+        cnt = s.groups * seq_splits(s, pps) * p.H_kv;
+      }
+      int total;
+      const int ex = block_exscan(cnt, sh, total);
+      if (b < p.B) p.seq_off[b] = running + ex;
+      running += total;
+    }
+    // partial entries of every token whose rows are split
+    int prun = 0;
+    for (int base = 0; base < p.T; base += nth) {
+      const int t = base + tid;
+      int cnt = 0, ns_t = 0;
+      if (t < p.T) {
+        const int b = last_le(p.qsl, p.B, t);
+        const SeqInfo s = seq_info(p, b);
+        if (s.valid && s.groups > 0) {
+          const int ns = seq_splits(s, pps);
+          const int pos = s.L - s.n + (t - s.tok0);
+          const int page = pos / kBlockSize;
+          for (int k = 0; k < ns; ++k)
+            if ((k * s.pages) / ns <= page) ns_t = k + 1;
+          cnt = ns_t > 1 ? ns_t * p.H_q : 0;
+        }
+      }
+      int total;
+      const int ex = block_exscan(cnt, sh, total);
+      if (t < p.T) {
+        p.tok_ns[t] = ns_t;
+        p.tok_base[t] = prun + ex;
+      }
+      prun += total;
+    }
+    n_items = running;
+    n_part = prun;
+    if (n_items <= p.cap_items && n_part <= p.cap_part) break;
+    if (pps >= (1 << 24)) {  // cannot shrink further: leave nothing to do
+      record_error(p.err, kDevPlanOverflow);
+      n_items = 0;
+      break;
+    }
+    pps *= 2;
+  }
+  if (tid == 0) p.seq_off[p.B] = n_items;
+  __syncthreads();
+
+  // emit the items, group index fastest so rows sharing pages run back to back
+  for (int i = tid; i < n_items; i += nth) {
+    const int b = last_le(p.seq_off, p.B, i);
+    const SeqInfo s = seq_info(p, b);
+    const int ns = seq_splits(s, pps);
+    const int local = i - p.seq_off[b];
+    const int j = local % s.groups;
+    const int rest = local / s.groups;
+    const int kv = rest % p.H_kv;
+    const int sp = rest / p.H_kv;
+    const int rows = s.n * p.G;
+    WorkItem it;
+    it.seq = b;
+    it.kv = kv;
+    it.row0 = 16 * j;
+    it.nrows = min(16, rows - 16 * j);
+    const int i_last = (it.row0 + it.nrows - 1) / p.G;
+    const int page_last = (s.L - s.n + i_last) / kBlockSize;
+    it.page_begin = (sp * s.pages) / ns;
+    it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
+    it.split = sp;
+    it.nsplit = ns;
+    it.ctx_len = s.L;
+    it.n_query = s.n;
+    it.tok0 = s.tok0;
+    it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
+    const int4* src = reinterpret_cast<const int4*>(&it);
+    int4* dst = reinterpret_cast<int4*>(p.items + i);
+    dst[0] = src[0];
+    dst[1] = src[1];
+    dst[2] = src[2];
+    dst[3] = src[3];
+  }
+  if (tid == 0) {
+    p.hdr[0] = n_items;
+    p.hdr[1] = 0;
+    p.hdr[2] = pps;
+    p.hdr[3] = n_part;
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// split kernel: one warp = one work item at a time
+// ----------------------------------------------------------------------------------
+template <int D>
+struct SplitCfg;
+template <>
+struct SplitCfg<128> {
+  static constexpr int kWarps = 4, kStages = 4;
+};
+template <>
+struct SplitCfg<64> {
+  static constexpr int kWarps = 4, kStages = 8;
+};
+
+template <int D>
+constexpr int split_smem_bytes() {
+  return 1024 /*alignment slack*/ +
+         SplitCfg<D>::kWarps * SplitCfg<D>::kStages * (2 * kBlockSize * D * 2) +
+         SplitCfg<D>::kWarps * SplitCfg<D>::kStages * 8 +
+         SplitCfg<D>::kWarps * (SplitCfg<D>::kStages + 2) * 64;
+}
+
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
+    split_attention_kernel(const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+  constexpr int W = SplitCfg<D>::kWarps;
+  constexpr int S = SplitCfg<D>::kStages;
+  constexpr int kRing = S + 2;
+  constexpr int kPage = kBlockSize * D * 2;  // bytes of one page of K (or V), one head
+  constexpr int kStage = 2 * kPage;
+  constexpr int kBoxes = D / 64;             // 64-element (128-byte) boxes per row
+  constexpr int kKSteps = D / 16;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* tiles = smem + warp * S * kStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + W * S * kStage) + warp * S;
+  WorkItem* ring =
+      reinterpret_cast<WorkItem*>(smem + W * S * kStage + W * S * 8) + warp * kRing;
+  const uint32_t tiles_addr = smem_u32(tiles);
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  __syncwarp();
+
+  const int n_items = *reinterpret_cast<volatile int*>(p.hdr);
+  const uint64_t policy = l2_policy_evict_first();
+
+  // ---------------- issue side (runs ahead of compute by up to S pages) -------------
+  int iss_page = 0, iss_end = 0, iss_seq = 0, iss_kv = 0;
+  int bt_base = 0, bt_reg = -1;
+  bool no_more = false;
+  uint32_t g_issue = 0, ring_tail = 0;
+
+  auto load_bt = [&](int first) {
+    bt_base = first;
+    const int pg = first + lane;
+    bt_reg = pg < iss_end
+                 ? __ldg(p.block_tables + static_cast<int64_t>(iss_seq) * p.max_blocks + pg)
+                 : -1;
+  };
+
+  // Issue the next page of work into stage g_issue % S; false when nothing is left.
+  auto issue_one = [&]() -> bool {
+    while (iss_page >= iss_end) {
+      if (no_more) return false;
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.hdr + 1, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx >= n_items) {
+        no_more = true;
+        return false;
+      }
+      const int* src = reinterpret_cast<const int*>(p.items + idx);
+      const int v = lane < 16 ? __ldg(src + lane) : 0;
+      const int pb = __shfl_sync(0xffffffffu, v, 4), pe = __shfl_sync(0xffffffffu, v, 5);
+      if (pe <= pb) continue;  // no key of this split is visible to these rows
+      WorkItem* slot = ring + (ring_tail % kRing);
+      if (lane < 16) reinterpret_cast<int*>(slot)[lane] = v;
+      ++ring_tail;
+      iss_seq = __shfl_sync(0xffffffffu, v, 0);
+      iss_kv = __shfl_sync(0xffffffffu, v, 1);
+      iss_page = pb;
+      iss_end = pe;
+      load_bt(pb);
+    }
+    if (iss_page - bt_base >= 32) load_bt(iss_page);
+    const int blk = __shfl_sync(0xffffffffu, bt_reg, iss_page - bt_base);
+    if (lane == 0) {
+      int row = blk * kBlockSize;
+      if (blk < 0 || blk >= p.num_blocks) {
+        record_error(p.err, kDevBadBlockId);
+        row = p.num_blocks * kBlockSize;  // past the tensor: the copy reads zeros
+      }
+      const uint32_t st = g_issue % S;
+      uint8_t* dst = tiles + st * kStage;
+      mbar_arrive_expect_tx(&full[st], kStage);
+#pragma unroll
+      for (int x = 0; x < kBoxes; ++x) {
+        tma_load_2d_hint(dst + x * (kBlockSize * 128), &kmap, &full[st], iss_kv * D + x * 64,
+                         row, policy);
+        tma_load_2d_hint(dst + kPage + x * (kBlockSize * 128), &vmap, &full[st],
+                         iss_kv * D + x * 64, row, policy);
+      }
+    }
+    ++iss_page;
+    ++g_issue;
+    return true;
+  };
+
+  // ---------------- compute side ---------------------------------------------------
+  const int g = lane >> 2, t4 = lane & 3;
+  uint32_t g_comp = 0, ring_head = 0;
+  int comp_left = 0, comp_page = 0;
+  bool have_item = false;
+  WorkItem cur;
+  // per-thread rows g and g + 8 of the item
+  int row_tok[2], row_h[2], row_pos[2];
+  float m_run[2], l_run[2];
+  float o[D / 8][4];
+  uint32_t qa[kKSteps][4];
+  const float scale_log2 = p.scale_log2;
+  const uint16_t* qptr = static_cast<const uint16_t*>(p.q);
+
+  auto start_item = [&]() {
+    __syncwarp();  // the ring slot was written by lanes 0..15
+    cur = ring[ring_head % kRing];
+    ++ring_head;
+    comp_page = cur.page_begin;
+    comp_left = cur.page_end - cur.page_begin;
+    have_item = true;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int rr = g + 8 * r;
+      if (rr < cur.nrows) {
+        const int R = cur.row0 + rr;
+        const int i = R / p.G;
+        row_tok[r] = cur.tok0 + i;
+        row_h[r] = cur.kv * p.G + (R - i * p.G);
+        row_pos[r] = cur.ctx_len - cur.n_query + i;
+      } else {
+        row_tok[r] = -1;
+        row_h[r] = 0;
+        row_pos[r] = -1;
+      }
+      m_run[r] = -INFINITY;
+      l_run[r] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    // query fragments straight from global memory (rows g, g + 8; columns 2*t4 ...)
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        uint32_t lo = 0, hi = 0;
+        if (row_tok[r] >= 0) {
+          const uint16_t* src =
+              qptr + (static_cast<int64_t>(row_tok[r]) * p.H_q + row_h[r]) * D + kk * 16 + 2 * t4;
+          lo = __ldg(reinterpret_cast<const uint32_t*>(src));
+          hi = __ldg(reinterpret_cast<const uint32_t*>(src + 8));
+        }
+        qa[kk][r] = lo;       // a0a1 (row g) / a2a3 (row g+8): columns 2t4, 2t4+1
+        qa[kk][2 + r] = hi;   // a4a5 / a6a7: columns 2t4+8, 2t4+9
+      }
+    }
+  };
+
+  auto finish_item = [&]() {
+    // complete the row sums across the quad of lanes sharing a row
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (row_tok[r] < 0) continue;
+      const int tok = row_tok[r];
+      const int ns_t = __ldg(p.tok_ns + tok);
+      if (cur.split >= ns_t) continue;  // this split holds no key visible to the row
+      const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
+      if (ns_t == 1) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+            static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + row_h[r]) * D +
+            2 * t4);
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+          dst[j * 4] = pack2<kBF16>(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
+      } else {
+        const int64_t idx = __ldg(p.tok_base + tok) + cur.split * p.H_q + row_h[r];
+        float2* dst = reinterpret_cast<float2*>(p.part_o + idx * D + 2 * t4);
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+          dst[j * 4] = make_float2(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
+        if (t4 == 0)
+          p.part_lse[idx] = l_run[r] > 0.f ? m_run[r] + __log2f(l_run[r]) : -INFINITY;
+      }
+    }
+    have_item = false;
+  };
+
+  // fill the ring
+  for (int s = 0; s < S; ++s)
+    if (!issue_one()) break;
+
+  bool aborted = false;
+  while (true) {
+    if (comp_left == 0) {
+      if (have_item) finish_item();
+      if (ring_head == ring_tail) break;  // everything issued has been computed
+      start_item();
+    }
+    const uint32_t st = g_comp % S;
+    if (!mbar_wait(&full[st], (g_comp / S) & 1)) {
+      if (lane == 0) record_error(p.err, kDevWaitTimeout);
+      aborted = true;
+      break;
+    }
+    const uint32_t kbase = tiles_addr + st * kStage;
+    const uint32_t vbase = kbase + kPage;
+
+    // S = Q K^T for the page's 16 keys: two n8 tiles
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = (mi >> 1) * 8 + rr;
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        const int chunk = 2 * kk + (mi & 1);
+        const uint32_t addr = kbase + (chunk >> 3) * (kBlockSize * 128) + swz128(key, chunk & 7);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma_16816<kBF16>(s[0], qa[kk], b0, b1);
+        mma_16816<kBF16>(s[1], qa[kk], b2, b3);
+      }
+    }
+    // causal mask, online softmax
+    const int key0 = comp_page * kBlockSize + 2 * t4;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1;
+        const int key = key0 + nt * 8 + (e & 1);
+        const float x = key <= row_pos[r] ? s[nt][e] * scale_log2 : -INFINITY;
+        s[nt][e] = x;
+        mx[r] = fmaxf(mx[r], x);
+      }
+    float alpha[2], m_use[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float m_new = fmaxf(m_run[r], mx[r]);
+      m_use[r] = m_new == -INFINITY ? 0.f : m_new;
+      alpha[r] = exp2f(m_run[r] - m_use[r]);
+      m_run[r] = m_new;
+    }
+    float psum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1;
+        const float pe = exp2f(s[nt][e] - m_use[r]);
+        s[nt][e] = pe;
+        psum[r] += pe;
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + psum[r];
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      o[j][0] *= alpha[0];
+      o[j][1] *= alpha[0];
+      o[j][2] *= alpha[1];
+      o[j][3] *= alpha[1];
+    }
+    uint32_t pa[4];
+    pa[0] = pack2<kBF16>(s[0][0], s[0][1]);
+    pa[1] = pack2<kBF16>(s[0][2], s[0][3]);
+    pa[2] = pack2<kBF16>(s[1][0], s[1][1]);
+    pa[3] = pack2<kBF16>(s[1][2], s[1][3]);
+    // O += P V: V page is [key][d], read transposed
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = (mi & 1) * 8 + rr;
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        const int chunk = 2 * np + (mi >> 1);
+        const uint32_t addr = vbase + (chunk >> 3) * (kBlockSize * 128) + swz128(key, chunk & 7);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma_16816<kBF16>(o[2 * np], pa, b0, b1);
+        mma_16816<kBF16>(o[2 * np + 1], pa, b2, b3);
+      }
+    }
+    ++g_comp;
+    ++comp_page;
+    --comp_left;
+    __syncwarp();
+    fence_proxy_async_smem();
+    issue_one();
+  }
+  if (aborted) {
+    // let the copies already issued land before the CTA's shared memory goes away
+    for (uint32_t gg = g_comp; gg < g_issue; ++gg) mbar_wait(&full[gg % S], (gg / S) & 1, 1u << 20);
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// combine: one warp per (token, head) whose rows were split
+// ----------------------------------------------------------------------------------
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.T * p.H_q) return;
+  const int tok = wid / p.H_q, h = wid - tok * p.H_q;
+  const int ns = __ldg(p.tok_ns + tok);
+  if (ns <= 1) return;
+  const int base = __ldg(p.tok_base + tok);
+  const float lse = lane < ns ? p.part_lse[base + lane * p.H_q + h] : -INFINITY;
+  float M = lse;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = (lane < ns && lse != -INFINITY) ? exp2f(lse - M) : 0.f;
+  float Wsum = w;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) Wsum += __shfl_xor_sync(0xffffffffu, Wsum, o);
+  constexpr int kPer = D / 32;  // elements per lane
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += ws * v.x;
+      acc[1] += ws * v.y;
+      acc[2] += ws * v.z;
+      acc[3] += ws * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += ws * v.x;
+      acc[1] += ws * v.y;
+    }
+  }
+  const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
+  uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + h) * D +
+                  lane * kPer;
+  if constexpr (kPer == 4) {
+    uint2 v;
+    v.x = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+    v.y = pack2<kBF16>(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ----------------------------------------------------------------------------------
+// launchers
+// ----------------------------------------------------------------------------------
+int attention_warps(int D) { return D == 128 ? SplitCfg<128>::kWarps : SplitCfg<64>::kWarps; }
+int attention_ctas(int D, int num_sms) { (void)D; return num_sms; }
+
+cudaError_t launch_plan(const AttnParams& p, int concurrency, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(p, concurrency);
+  return cudaGetLastError();
+}
+
+template <bool kBF16, int D>
+static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
+                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+  constexpr int smem = split_smem_bytes<D>();
+  auto kern = split_attention_kernel<kBF16, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<attention_ctas(D, num_sms), SplitCfg<D>::kWarps * 32, smem, stream>>>(kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+  if (p.D == 128)
+    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, num_sms, stream)
+                : launch_split_t<false, 128>(p, kmap, vmap, num_sms, stream);
+  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, num_sms, stream)
+              : launch_split_t<false, 64>(p, kmap, vmap, num_sms, stream);
+}
+
+cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream) {
+  const int64_t warps = static_cast<int64_t>(p.T) * p.H_q;
+  if (warps == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+  if (p.D == 128) {
+    if (bf16) combine_kernel<true, 128><<<blocks, 256, 0, stream>>>(p);
+    else combine_kernel<false, 128><<<blocks, 256, 0, stream>>>(p);
+  } else {
+    if (bf16) combine_kernel<true, 64><<<blocks, 256, 0, stream>>>(p);
+    else combine_kernel<false, 64><<<blocks, 256, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ps

@@ -1,0 +1,53 @@
+// Internal launch interface between the C ABI (ps_abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ps {
+
+struct WorkItem;
+
+// Everything the planner, the attention kernels and the combine kernel read.
+struct AttnParams {
+  const void* q;                 // [T, H_q, D]
+  void* out;                     // [T, H_q, D]
+  const int32_t* block_tables;   // [B, max_blocks]
+  const int32_t* seq_lens;       // [B]
+  const int32_t* qsl;            // [B + 1]
+  int max_blocks;
+  int B, T, H_q, H_kv, D, G, num_blocks;
+  float scale_log2;              // softmax scale * log2(e)
+  // workspace
+  int* hdr;                      // [0] items, [1] fetch counter, [2] pages per split, [3] partials
+  WorkItem* items;               // [cap_items]
+  int* seq_off;                  // [B + 1] first item of each sequence
+  int* tok_ns;                   // [T] splits holding each token's rows (0 = none)
+  int* tok_base;                 // [T] first partial entry of each token
+  float* part_lse;               // [cap_part] log2-sum-exp of each partial
+  float* part_o;                 // [cap_part, D] normalised partial outputs
+  int cap_items, cap_part;
+  int* err;                      // device error word
+};
+
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                const int32_t* qsl, int B, int T, int num_blocks, int32_t* slots,
+                                int* err, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots,
+                                     void* k_pool, void* v_pool, int T, int H_kv, int D,
+                                     int num_blocks, int* err, int num_sms, cudaStream_t stream);
+
+// Number of resident attention CTAs and warps per CTA the split kernel uses.
+int attention_ctas(int D, int num_sms);
+int attention_warps(int D);
+
+cudaError_t launch_plan(const AttnParams& p, int concurrency, cudaStream_t stream);
+
+cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream);
+
+}  // namespace ps

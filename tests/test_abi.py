@@ -1,0 +1,108 @@
+"""The C ABI: the library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_18_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pagedserve.h")
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ps_\w+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ["ps_slot_mapping", "ps_reshape_and_cache", "ps_paged_attention",
+              "ps_paged_attention_workspace_size", "ps_attention_step", "ps_get_device_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    assert lib.ps_status_string(0) == b"PS_OK"
+    for rc in (-1, -2, -3, -4, -5):
+        assert lib.ps_status_string(rc).startswith(b"PS_ERR")
+
+
+def test_workspace_size(lib):
+    small = lib.ps_paged_attention_workspace_size(4, 4, 4, 2, 64, 0)
+    big = lib.ps_paged_attention_workspace_size(256, 256, 12, 2, 128, 4096)
+    assert 0 < small < big
+    assert lib.ps_paged_attention_workspace_size(4, 4, 5, 2, 64, 100) == 0  # H_q % H_kv
+    assert lib.ps_paged_attention_workspace_size(4, 4, 4, 2, 96, 100) == 0  # head_dim
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced by these calls
+
+
+def test_reshape_and_cache_rejects(lib):
+    f = lib.ps_reshape_and_cache
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 8, 1, None) == -2      # head_dim
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 7, None) == -2      # dtype
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 2, 64, 8, 1, None) == -1     # T
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 0, 1, None) == -1      # pool
+    assert f(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 1, None) == -3  # alignment
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 1, None) == -1      # null
+    assert f(None, None, None, None, None, 0, 2, 64, 8, 1, None) == 0       # empty: no-op
+
+
+def test_slot_mapping_rejects(lib):
+    f = lib.ps_slot_mapping
+    assert f(FAKE, 4, FAKE, FAKE, 0, 3, 8, FAKE, None) == -1   # B = 0 with T > 0
+    assert f(FAKE, 4, None, FAKE, 2, 3, 8, FAKE, None) == -1   # null seq_lens
+    assert f(FAKE, 4, FAKE, FAKE, 2, 3, 8, None, None) == -1   # null output
+    assert f(FAKE, 4, FAKE, FAKE, 2, 3, -1, FAKE, None) == -1  # pool
+    assert f(None, 0, None, None, 0, 0, 8, None, None) == 0    # empty batch: no-op
+
+
+def test_paged_attention_rejects(lib):
+    f = lib.ps_paged_attention
+
+    def call(**kw):
+        a = dict(q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, maxblk=4, sl=FAKE, qsl=FAKE, B=2, T=3,
+                 Hq=12, Hkv=2, D=128, NB=64, scale=0.1, out=FAKE, ws=FAKE, wsb=1 << 30,
+                 dtype=1)
+        a.update(kw)
+        return f(a["q"], a["kp"], a["vp"], a["bt"], a["maxblk"], a["sl"], a["qsl"], a["B"],
+                 a["T"], a["Hq"], a["Hkv"], a["D"], a["NB"], ctypes.c_float(a["scale"]),
+                 a["out"], a["ws"], a["wsb"], a["dtype"], None)
+
+    assert call(Hq=13) == -2
+    assert call(D=80) == -2
+    assert call(dtype=3) == -2
+    assert call(q=FAKE + 8) == -3
+    assert call(out=FAKE + 4) == -3
+    assert call(ws=None) == -4
+    assert call(ws=FAKE + 64) == -4          # workspace must be 256-byte aligned
+    assert call(wsb=16) == -4                # too small
+    assert call(B=0) == -1                   # T > 0 needs sequences
+    assert call(maxblk=0) == -1
+    assert call(T=0) == 0                    # nothing to do
+
+
+def test_attention_step_rejects(lib):
+    f = lib.ps_attention_step
+    rc = f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 3, 12, 2, 72, 64,
+           ctypes.c_float(0.1), FAKE, FAKE, FAKE, 1 << 30, 1, None)
+    assert rc == -2  # D = 72 unsupported, found before anything is enqueued
+    rc = f(FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 3, 12, 2, 128, 64,
+           ctypes.c_float(0.1), FAKE, FAKE, FAKE, 1 << 30, 1, None)
+    assert rc == -3  # k misaligned
+
+
+def test_profile_read_rejects(lib):
+    ms, n = ctypes.c_float(), ctypes.c_int()
+    assert lib.ps_profile_read(9, ctypes.addressof(ms), ctypes.addressof(n)) == -1
+    assert lib.ps_profile_begin(0) == -1

@@ -1,0 +1,195 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Slot mapping and the pools after the KV scatter must be bit-exact; attention outputs
+must agree within max-abs 2e-3 (fp16) / 1e-2 (bf16) of the fp32 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_18_gb300 import binding
+from paged_kv_attention_18_gb300 import workloads as W
+from tests.gpu_util import TOL, DevicePools, check_workload, dev, run_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_rows(st, n_seqs, rng, extra_rows=0):
+    """All rows of a random subset of sequences (plus some random rows)."""
+    qsl = st.query_start_loc
+    seqs = rng.choice(st.B, size=min(n_seqs, st.B), replace=False)
+    rows = [r for b in seqs for r in range(qsl[b], qsl[b + 1])]
+    if extra_rows and st.T:
+        rows += rng.choice(st.T, size=min(extra_rows, st.T), replace=False).tolist()
+    return sorted(set(int(r) for r in rows))
+
+
+# ------------------------------------------------------------------------------------
+# the five named workloads
+# ------------------------------------------------------------------------------------
+def test_tiny_decode():
+    check_workload(W.tiny_decode())
+
+
+def test_qwen05b_mixed():
+    check_workload(W.qwen05b_mixed())
+
+
+def test_qwen05b_mixed_separate_calls():
+    check_workload(W.qwen05b_mixed(), separate_calls=True)
+
+
+def test_qwen15b_decode_full_size():
+    wl = W.qwen15b_decode()
+    rng = np.random.default_rng(100)
+    check_workload(wl, rows_for_step=lambda i, st: _sample_rows(st, 48, rng))
+
+
+def test_prefix_chunked_prefill_all_steps():
+    wl = W.prefix_chunked_prefill()
+    assert len(wl.steps) >= 3
+    rng = np.random.default_rng(101)
+
+    def rows(i, st):
+        qsl = st.query_start_loc
+        r = list(range(32))  # every decode row
+        for b in range(32, st.B):  # first and last row of every prefill chunk
+            r += [int(qsl[b]), int(qsl[b + 1]) - 1]
+        r += rng.choice(st.T, size=200, replace=False).tolist()
+        return sorted(set(r))
+
+    check_workload(wl, rows_for_step=rows)
+
+
+def test_spec_verify_long_full_size():
+    wl = W.spec_verify_long()
+    st = wl.steps[0]
+    rng = np.random.default_rng(102)
+    long_rows = list(range(int(st.query_start_loc[-5]), st.T))  # the four 32k sequences
+    check_workload(wl, rows_for_step=lambda i, s: sorted(set(_sample_rows(s, 24, rng) +
+                                                             long_rows)))
+
+
+# ------------------------------------------------------------------------------------
+# randomized small shapes: several tiles, splits and ragged tails, compared in full
+# ------------------------------------------------------------------------------------
+SWEEP = [
+    ("f16", 64, 4, 2), ("bf16", 64, 14, 2), ("f16", 128, 12, 2), ("bf16", 128, 12, 2),
+    ("bf16", 128, 8, 8), ("f16", 64, 16, 1), ("bf16", 128, 32, 4), ("f16", 128, 6, 3),
+]
+
+
+@pytest.mark.parametrize("dtype,D,H_q,H_kv", SWEEP)
+@pytest.mark.parametrize("seed", [0, 1])
+def test_random_mix(dtype, D, H_q, H_kv, seed):
+    rng = np.random.default_rng(1000 + seed * 31 + D + H_q)
+    seqs = []
+    for _ in range(int(rng.integers(3, 9))):
+        kind = rng.integers(0, 4)
+        L = int(rng.integers(1, 1200))
+        n = {0: 1, 1: min(L, int(rng.integers(2, 9))), 2: min(L, int(rng.integers(1, 300))),
+             3: 0}[int(kind)]
+        seqs.append((L, n))
+    seqs.append((int(rng.integers(2000, 5000)), 1))  # a long decode that splits
+    wl = W.simple_workload("mix", seed=seed, dtype=dtype, H_q=H_q, H_kv=H_kv, D=D, seqs=seqs)
+    check_workload(wl)
+
+
+def test_verify_rows_many_splits():
+    seqs = [(int(L), 5) for L in np.random.default_rng(5).integers(1024, 8192, size=20)]
+    seqs += [(32768, 5)]
+    wl = W.simple_workload("verify", seed=5, dtype="bf16", H_q=12, H_kv=2, D=128, seqs=seqs)
+    check_workload(wl)
+
+
+# ------------------------------------------------------------------------------------
+# edge cases
+# ------------------------------------------------------------------------------------
+def test_context_of_one_gives_v():
+    wl = W.simple_workload("one", seed=3, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(1, 1), (1, 1), (17, 1)])
+    pools = DevicePools(wl)
+    st = wl.steps[0]
+    out, _ = run_step(wl, st, pools)
+    got = out.cpu()
+    v = dev(st.v, "bf16").cpu()
+    for t in range(2):
+        for h in range(12):
+            assert torch.equal(got[t, h], v[t, h // 6])  # softmax of one key is exactly 1
+
+
+def test_empty_and_zero_query_batches():
+    wl = W.simple_workload("z", seed=4, dtype="f16", H_q=4, H_kv=2, D=64,
+                           seqs=[(10, 0), (33, 0)])
+    pools = DevicePools(wl)
+    st = wl.steps[0]
+    assert st.T == 0
+    out, slots = run_step(wl, st, pools)
+    assert out.shape == (0, 4, 64) and slots.numel() == 0
+    assert binding.device_error() == 0
+    # zero-query sequences between real ones
+    check_workload(W.simple_workload("z2", seed=4, dtype="f16", H_q=4, H_kv=2, D=64,
+                                     seqs=[(10, 0), (50, 3), (0, 0), (20, 1), (7, 0)]))
+
+
+def test_full_block_table_and_block_boundaries():
+    # contexts ending exactly on, just before and just after block boundaries; the
+    # longest uses every entry of its block table
+    seqs = [(16, 1), (15, 1), (17, 1), (32, 16), (48, 17), (64, 64), (1, 1), (160, 2)]
+    check_workload(W.simple_workload("edge", seed=9, dtype="bf16", H_q=12, H_kv=2, D=128,
+                                     seqs=seqs, free_fraction=0.0))
+
+
+def test_negative_slots_are_skipped():
+    wl = W.simple_workload("neg", seed=11, dtype="f16", H_q=4, H_kv=2, D=64,
+                           seqs=[(30, 3), (9, 1)])
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    slots = torch.tensor([-1, 5, -1, -7], dtype=torch.int32, device="cuda")
+    binding.reshape_and_cache(dev(st.k, "f16"), dev(st.v, "f16"), slots, pools.k, pools.v)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    kref, _ = oracle.reshape_and_cache(st.k, st.v, slots.cpu().numpy(), wl.k_pool, wl.v_pool)
+    from tests.gpu_util import host_bits
+    assert np.array_equal(host_bits(pools.k), kref)
+
+
+def test_minimum_workspace_means_no_splits():
+    wl = W.simple_workload("ws", seed=12, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(3000, 1), (2500, 5), (900, 1)])
+    st = wl.steps[0]
+    n = binding.workspace_size(st.T, st.B, 12, 2, 128, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    check_workload(wl, workspace=ws)
+
+
+def test_bad_block_id_sets_device_error_without_fault():
+    wl = W.simple_workload("bad", seed=13, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(40, 1), (40, 1)])
+    st = wl.steps[0]
+    bt = st.block_tables.copy()
+    bt[1, 1] = wl.num_blocks + 5  # out of the pool: checked on the device, never read
+    pools = DevicePools(wl)
+    q = dev(st.q, "bf16")
+    out = binding.paged_attention(q, pools.k, pools.v, dev(bt), dev(st.seq_lens),
+                                  dev(st.query_start_loc), wl.scale)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 1
+    assert binding.device_error() == 0  # reading clears it
+    ref = oracle.paged_attention(st.q, wl.k_pool, wl.v_pool, st.block_tables, st.seq_lens,
+                                 st.query_start_loc, wl.scale, "bf16", acc=np.float32)
+    assert np.abs(out.float().cpu().numpy()[0] - ref[0]).max() <= TOL["bf16"]
+
+
+def test_two_calls_share_a_workspace():
+    wl = W.qwen05b_mixed()
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    ws = binding.alloc_workspace(st.T, st.B, wl.H_q, wl.H_kv, wl.D, 1024)
+    a, _ = run_step(wl, st, pools, workspace=ws)
+    b = binding.paged_attention(dev(st.q, "f16"), pools.k, pools.v, dev(st.block_tables),
+                                dev(st.seq_lens), dev(st.query_start_loc), wl.scale,
+                                workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)  # deterministic: same plan, same order of accumulation
