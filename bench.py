@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV attention step on GB300.
+
+A step is the whole hot path over one packed batch: slot mapping, KV scatter and
+paged attention (planner, split kernel, split combine), through the C ABI.
+
+Default workload: Qwen2.5-1.5B attention shapes, 256 decodes with contexts
+U[512, 4096] (12/2 heads, head_dim 128, bf16). ``value`` is the step's algorithmic HBM
+bytes / device time (GB/s, whole job). The line also carries the mixed-batch tokens/s
+of the prefix-cached chunked-prefill workload, the roofline of the dominant kernel,
+the end-to-end figure through the host-buffer entry point, the CPU-oracle baseline and
+the SM clocks seen during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+    python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...  (replicas)
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle runs single-threaded (reported as cores = 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_18_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode paged-attn HBM GB/s (% of peak); mixed-batch attention tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_attention_qwen15b_decode_traffic.json")
+KERNEL_SOURCES = ["paged_kv_attention_18_gb300/csrc/ps_attention.cu",
+                  "paged_kv_attention_18_gb300/csrc/ps_common.cuh"]
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic work of a step
+# ------------------------------------------------------------------------------------
+def step_work(wl: W.Workload, st: W.Step) -> dict:
+    """Algorithmic bytes and flops of one step (each context read once, no split partials)."""
+    es = 2  # bytes per 16-bit element
+    L = st.seq_lens.astype(np.int64)
+    n = np.diff(st.query_start_loc).astype(np.int64)
+    live = n > 0
+    kv = int((L[live] * wl.H_kv * wl.D * es * 2).sum())
+    q = st.T * wl.H_q * wl.D * es
+    out = q
+    bt = int((((L[live] + 15) // 16) * 4).sum())
+    attn = kv + q + out + bt
+    scatter = 2 * (st.T * wl.H_kv * wl.D * es * 2) + st.T * 4  # read k/v, write pool rows, slots
+    # unmasked (query, key) pairs: row at position p sees p + 1 keys
+    pairs = 0
+    for b in range(st.B):
+        if n[b]:
+            p = L[b] - n[b] + np.arange(n[b])
+            pairs += int((p + 1).sum())
+    flops = 4 * wl.D * wl.H_q * pairs
+    return {"attn_bytes": attn, "kv_bytes": kv, "step_bytes": attn + scatter, "flops": flops,
+            "tokens": st.T}
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def committed_traffic(units: int) -> float | None:
+    """DRAM bytes per launch of the split kernel from the committed ncu capture, scaled
+    to this launch by KV bytes, or None when the kernel source changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec["dram_bytes_per_launch"] * units / rec["kv_bytes_per_launch"]
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.index)], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [ln.split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip() == "Active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+# ------------------------------------------------------------------------------------
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ------------------------------------------------------------------------------------
+def oracle_seconds(wl: W.Workload, st: W.Step, seqs: list[int]) -> tuple[float, int]:
+    """Time the oracle (slot mapping, scatter, attention) on a subset of sequences.
+
+    The subset keeps only the pool blocks its sequences use, so the oracle's copy of the
+    pool in its scatter scales with the sample. Returns (seconds, algorithmic bytes)."""
+    import oracle
+    sub, sst = W.subset(wl, st, seqs)
+    t0 = time.perf_counter()
+    oracle.attention_step(sst, sub.k_pool, sub.v_pool, sub.scale, sub.dtype, acc=np.float32)
+    dt = time.perf_counter() - t0
+    return dt, step_work(sub, sst)["step_bytes"]
+
+
+def cpu_baseline(wl, st, budget_s: float = 12.0) -> dict:
+    """Oracle throughput on the same workload, whole steps repeated for ~budget_s."""
+    seqs = list(range(st.B))
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < budget_s and reps < 50:
+        dt, nb = oracle_seconds(wl, st, seqs)
+        total_t += dt
+        total_b += nb
+        reps += 1
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole step ({st.B} sequences, {st.T} tokens) x {reps}, "
+                      f"{total_t:.1f} s of single-thread CPU"}
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+def make_workload(name: str, rank: int, batch: int | None = None) -> W.Workload:
+    """The named workload; each replica rank draws its own batch (seed + 1000 * rank)."""
+    base = {"qwen15b_decode": 2, "tiny_decode": 0, "qwen05b_mixed": 1,
+            "prefix_chunked_prefill": 3, "spec_verify_long": 4}[name]
+    kw = {"batch": batch} if (batch and name == "qwen15b_decode") else {}
+    return W.named(name, seed=base + 1000 * rank, **kw)
+
+
+class DeviceWorkload:
+    """A workload's tensors resident on the GPU, ready to run steps."""
+
+    def __init__(self, wl: W.Workload, device):
+        import torch
+        dev = lambda a, dt=None: W.to_device(a, dt, device)  # noqa: E731
+        self.wl = wl
+        self.k_pool = dev(wl.k_pool, wl.dtype)
+        self.v_pool = dev(wl.v_pool, wl.dtype)
+        self.steps = []
+        max_len = max(int(st.seq_lens.max()) if st.B else 0 for st in wl.steps)
+        from paged_kv_attention_18_gb300 import binding
+        for st in wl.steps:
+            d = {"q": dev(st.q, wl.dtype), "k": dev(st.k, wl.dtype), "v": dev(st.v, wl.dtype),
+                 "bt": dev(st.block_tables), "sl": dev(st.seq_lens),
+                 "qsl": dev(st.query_start_loc)}
+            d["out"] = torch.empty_like(d["q"])
+            d["slots"] = torch.empty(st.T, dtype=torch.int32, device=device)
+            d["ws"] = binding.alloc_workspace(st.T, st.B, wl.H_q, wl.H_kv, wl.D, max_len,
+                                              device=device)
+            self.steps.append(d)
+
+    def run(self):
+        from paged_kv_attention_18_gb300 import binding
+        for d in self.steps:
+            binding.attention_step(d["q"], d["k"], d["v"], self.k_pool, self.v_pool, d["bt"],
+                                   d["sl"], d["qsl"], self.wl.scale, out=d["out"],
+                                   workspace=d["ws"], slot_buf=d["slots"])
+
+
+def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
+                clocks: ClockSampler | None, min_load_s: float = 1.5):
+    import torch
+    from paged_kv_attention_18_gb300 import binding
+    if clocks:
+        clocks.start()
+    for _ in range(warmup):
+        dw.run()
+    torch.cuda.synchronize()
+    binding.profile_begin(min(steps, 2000) * len(dw.steps))
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        dw.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    prof = binding.profile_end()
+    # keep the same load running until the clock sampler has seen enough of it
+    while time.perf_counter() - t_wall < min_load_s:
+        dw.run()
+        torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    return reduce_max(ms, world, device), prof, clk
+
+
+def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device):
+    """Same steps from pinned host buffers through ps_attention_step_host."""
+    import torch
+    from paged_kv_attention_18_gb300 import binding
+    wl = dw.wl
+    hosts, h2d, d2h = [], 0, 0
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    max_len = max(int(st.seq_lens.max()) if st.B else 0 for st in wl.steps)
+    for st in wl.steps:
+        def pin(a, dtype=None):
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
+            t = t.view(dtype) if dtype is not None else t
+            return t.pin_memory()
+        h = {"q": pin(st.q, dt), "k": pin(st.k, dt), "v": pin(st.v, dt),
+             "bt": pin(st.block_tables), "sl": pin(st.seq_lens), "qsl": pin(st.query_start_loc)}
+        h["out"] = torch.empty(h["q"].shape, dtype=dt).pin_memory()
+        n = binding.staging_size(st.T, st.B, st.max_blocks_per_seq, wl.H_q, wl.H_kv, wl.D,
+                                 max_len)
+        h["staging"] = torch.empty(n, dtype=torch.uint8, device=device)
+        h2d += sum(h[k].numel() * h[k].element_size() for k in ("q", "k", "v", "bt", "sl", "qsl"))
+        d2h += h["out"].numel() * h["out"].element_size()
+        hosts.append(h)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for h in hosts:
+            binding.attention_step_host(h["q"], h["k"], h["v"], h["bt"], h["sl"], h["qsl"],
+                                        h["out"], dw.k_pool, dw.v_pool, wl.scale, h["staging"])
+            stream.synchronize()  # the caller reads the step's output
+
+    for _ in range(warmup):
+        one()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    sec = reduce_max(time.perf_counter() - t0, world, device)
+    return sec, h2d, d2h
+
+
+def run_ours(args, rank, world, local_rank) -> dict | None:
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_attention_18_gb300 import binding
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    peaks, peaks_src = load_peaks()
+
+    wl = make_workload(args.workload, rank, args.batch)
+    work = [step_work(wl, st) for st in wl.steps]
+    step_bytes = sum(w["step_bytes"] for w in work)
+    attn_bytes = sum(w["attn_bytes"] for w in work)
+    kv_bytes = sum(w["kv_bytes"] for w in work)
+    tokens = sum(w["tokens"] for w in work)
+    flops = sum(w["flops"] for w in work)
+    dw = DeviceWorkload(wl, device)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 and not args.no_clocks \
+        else None
+    ms, prof, clk = time_device(dw, args.steps, args.warmup, world, device, clocks,
+                                min_load_s=0.0 if args.no_clocks else 1.5)
+    if binding.device_error() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    sec = ms / 1e3
+    value = world * step_bytes * args.steps / sec / 1e9
+
+    # dominant kernel: the split attention kernel, timed per launch by the library hook
+    split_ms, split_n = prof["split_attention"]
+    split_avg_s = split_ms / 1e3 / max(1, split_n)
+    per_launch_bytes = attn_bytes / len(wl.steps)
+    achieved = per_launch_bytes / split_avg_s / 1e9 if split_n else None
+    traffic = committed_traffic(kv_bytes // len(wl.steps))
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"] if achieved else None,
+                "traffic": traffic, "kernel": "split_attention_kernel",
+                "peak_source": f"{peaks_src} (hbm_gbs)",
+                "kernel_share_of_step": split_ms / (sum(t for t, _ in prof.values()) or 1)}
+
+    # mixed batch: prefix-cached chunked prefill packed with decodes
+    mixed = None
+    if args.workload == "qwen15b_decode" and not args.no_mixed:
+        wm = make_workload("prefix_chunked_prefill", rank)
+        dm = DeviceWorkload(wm, device)
+        msteps = max(3, min(args.steps, 20))
+        mms, _, _ = time_device(dm, msteps, min(args.warmup, 3), world, device, None,
+                                min_load_s=0.0)
+        mtok = sum(st.T for st in wm.steps)
+        mflops = sum(step_work(wm, st)["flops"] for st in wm.steps)
+        mixed = {"workload": wm.name, "value": world * mtok * msteps / (mms / 1e3),
+                 "unit": "tokens/s", "steps": msteps, "engine_steps_per_step": len(wm.steps),
+                 "tflops": world * mflops * msteps / (mms / 1e3) / 1e12}
+        del dm
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 200))
+        e2e_s, h2d, d2h = time_e2e(dw, e2e_steps, 3, world, device)
+        e2e = {"value": world * step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "api": "ps_attention_step_host (pinned host buffers, stream sync per step)"}
+
+    if rank != 0:
+        return None
+    base = None if args.no_cpu_baseline else cpu_baseline(wl, wl.steps[0])
+    st0 = wl.steps[0]
+    result = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) values, random block permutation)",
+        "config": {"workload": wl.name, "description": wl.description, "B": st0.B,
+                   "T": tokens, "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D,
+                   "block_size": 16, "num_blocks": wl.num_blocks,
+                   "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
+                   "flops_per_step": flops,
+                   "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step "
+                         f"vs {L2_BYTES / 1e6:.0f} MB L2); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": int(sum(n for _, n in prof.values()) * args.steps
+                            // max(1, min(args.steps, 2000))),
+        "roofline": roofline,
+        "mixed_batch": mixed,
+        "e2e": e2e,
+        "cpu_baseline": base,
+        "clocks": clk,
+    }
+    return result
+
+
+# ------------------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ------------------------------------------------------------------------------------
+def run_reference(args, rank, world) -> dict | None:
+    if rank != 0:
+        return None
+    wl = make_workload(args.workload, 0, args.batch)
+    st = wl.steps[0]
+    # a bounded sample per step so that warm-up + steps stay within ~2 minutes
+    probe = list(range(min(4, st.B)))
+    probe_t, _ = oracle_seconds(wl, st, probe)
+    per_seq = probe_t / max(1, len(probe))
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(st.B, per_step_budget / max(per_seq, 1e-5))))
+    seqs = list(range(n))
+    for _ in range(args.warmup):
+        oracle_seconds(wl, st, seqs)
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_seconds(wl, st, seqs)
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    sample = f"{n} of {st.B} sequences of step 0 per step, single-thread CPU oracle"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded N(0,1) values, random block permutation)",
+            "config": {"workload": wl.name, "description": wl.description},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen15b_decode", choices=sorted(W.NAMED))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="decode batch size for qwen15b_decode (default 256); for small "
+                         "profiling cases")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="no nvidia-smi sampling and no extra load after the timed steps")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if args.impl == "reference":
+            # only rank 0 works; the others leave at once
+            if rank != 0:
+                return 0
+            world_eff = 1
+        else:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group(backend=backend)
+            world_eff = world
+    else:
+        world_eff = 1
+    if args.impl == "reference":
+        res = run_reference(args, 0 if world_eff == 1 else rank, world)
+    else:
+        res = run_ours(args, rank, world_eff, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world_eff > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

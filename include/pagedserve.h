@@ -154,6 +154,29 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
                       int dtype, void* stream);
 
 /*
+ * ps_attention_step_host -- one step from HOST buffers: copies the step's inputs to the
+ * device, runs ps_attention_step, and copies the output back, all on `stream`.
+ *
+ *   q, k, v, block_tables, seq_lens, query_start_loc   HOST pointers (pinned memory lets
+ *                  the copies run asynchronously), shapes as for ps_attention_step.
+ *   out            HOST pointer [T, H_q, D] of dtype; valid once `stream` has completed.
+ *   k_pool, v_pool DEVICE pointers: the resident KV cache, updated in place.
+ *   staging        DEVICE scratch of at least ps_attention_step_host_staging_size() bytes,
+ *                  256-byte aligned, owned by the caller (inputs, slot mapping, output and
+ *                  the attention workspace are placed in it).
+ * Host memory must stay valid and unmodified until the stream completes. Copies are one
+ * cudaMemcpyAsync per array.
+ */
+size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq, int H_q,
+                                           int H_kv, int D, int max_seq_len);
+int ps_attention_step_host(const void* q, const void* k, const void* v,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, void* out, void* k_pool,
+                           void* v_pool, int max_blocks_per_seq, int B, int T, int H_q,
+                           int H_kv, int D, int num_blocks, float scale, void* staging,
+                           size_t staging_bytes, int dtype, void* stream);
+
+/*
  * ps_get_device_error -- read (and clear) the device error word of the current device.
  * Synchronises with the device. *code receives a ps_device_error value. Returns PS_OK or
  * PS_ERR_CUDA / PS_ERR_ARG.

@@ -26,6 +26,11 @@ SIGNATURES = {
                                    c_int, c_int, c_float, _p, _p, c_size_t, c_int, _p]),
     "ps_attention_step": (c_int, [_p, _p, _p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int,
                                   c_int, c_int, c_int, c_float, _p, _p, _p, c_size_t, c_int, _p]),
+    "ps_attention_step_host_staging_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int,
+                                                        c_int, c_int]),
+    "ps_attention_step_host": (c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, c_int, c_int, c_int,
+                                       c_int, c_int, c_int, c_int, c_float, _p, c_size_t, c_int,
+                                       _p]),
     "ps_get_device_error": (c_int, [_p]),
     "ps_status_string": (c_char_p, [c_int]),
     "ps_profile_begin": (c_int, [c_int]),

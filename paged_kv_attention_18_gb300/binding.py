@@ -180,3 +180,41 @@ def profile_end() -> dict:
                "ps_profile_read")
         res[name] = (ms.value, n.value)
     return res
+
+
+def staging_size(T: int, B: int, max_blocks: int, H_q: int, H_kv: int, D: int,
+                 max_seq_len: int) -> int:
+    return int(lib().ps_attention_step_host_staging_size(T, B, max_blocks, H_q, H_kv, D,
+                                                         max_seq_len))
+
+
+def attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                        scale: float, staging, stream=None) -> None:
+    """One step from host tensors (ps_attention_step_host); ``out`` is a host tensor.
+
+    q/k/v/block_tables/seq_lens/query_start_loc/out live in host memory (pin them for
+    asynchronous copies); k_pool/v_pool and staging live on the device. The call returns
+    once everything is enqueued: synchronise the stream before reading ``out``.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("block_tables", block_tables),
+                    ("seq_lens", seq_lens), ("query_start_loc", query_start_loc), ("out", out)):
+        if t.is_cuda or not t.is_contiguous():
+            raise PagedServeError(f"{name} must be a contiguous host tensor")
+    if q.dtype not in DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != q.dtype:
+        raise PagedServeError("q/k/v/out dtype")
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc)):
+        if t.dtype != torch.int32:
+            raise PagedServeError(f"{name} must be int32")
+    kpp = _dev(k_pool, "k_pool", q.dtype, 4)
+    vpp = _dev(v_pool, "v_pool", q.dtype, 4)
+    sp = _dev(staging, "staging", torch.uint8, 1)
+    T, H_q, D = q.shape
+    NB, _, H_kv, _ = k_pool.shape
+    B, maxblk = block_tables.shape
+    _check(lib().ps_attention_step_host(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        block_tables.data_ptr(), seq_lens.data_ptr(),
+                                        query_start_loc.data_ptr(), out.data_ptr(), kpp, vpp,
+                                        maxblk, B, T, H_q, H_kv, D, NB, float(scale), sp,
+                                        staging.numel(), DTYPE_CODE[q.dtype], _stream(stream)),
+           "ps_attention_step_host")

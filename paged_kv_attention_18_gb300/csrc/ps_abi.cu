@@ -327,6 +327,91 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
                             workspace, workspace_bytes, dtype, stream);
 }
 
+namespace {
+struct StagingLayout {
+  size_t q, k, v, bt, sl, qsl, slots, out, ws, total;
+};
+StagingLayout staging_layout(int T, int B, int max_blocks, int H_q, int H_kv, int D,
+                             size_t ws_bytes) {
+  StagingLayout l;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  l.q = take(static_cast<size_t>(T) * H_q * D * 2);
+  l.k = take(static_cast<size_t>(T) * H_kv * D * 2);
+  l.v = take(static_cast<size_t>(T) * H_kv * D * 2);
+  l.bt = take(static_cast<size_t>(B) * max_blocks * 4);
+  l.sl = take(static_cast<size_t>(B) * 4);
+  l.qsl = take(static_cast<size_t>(B + 1) * 4);
+  l.slots = take(static_cast<size_t>(T) * 4);
+  l.out = take(static_cast<size_t>(T) * H_q * D * 2);
+  l.ws = take(ws_bytes);
+  l.total = o;
+  return l;
+}
+}  // namespace
+
+size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq, int H_q,
+                                           int H_kv, int D, int max_seq_len) {
+  if (max_blocks_per_seq < 0) return 0;
+  const size_t ws = ps_paged_attention_workspace_size(T, B, H_q, H_kv, D, max_seq_len);
+  if (ws == 0) return 0;
+  return staging_layout(T, B, max_blocks_per_seq, H_q, H_kv, D, ws).total;
+}
+
+int ps_attention_step_host(const void* q, const void* k, const void* v,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, void* out, void* k_pool, void* v_pool,
+                           int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
+                           int num_blocks, float scale, void* staging, size_t staging_bytes,
+                           int dtype, void* stream) {
+  int rc = check_shapes(H_q, H_kv, D, dtype);
+  if (rc) return rc;
+  if ((rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
+                        num_blocks)))
+    return rc;
+  if (T == 0) return PS_OK;
+  if (!q || !k || !v || !out || !k_pool || !v_pool) return PS_ERR_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return PS_ERR_ALIGN;
+  if (!staging || (reinterpret_cast<uintptr_t>(staging) & 255u)) return PS_ERR_WORKSPACE;
+  // the attention workspace takes whatever the inputs leave over
+  const StagingLayout l0 = staging_layout(T, B, max_blocks_per_seq, H_q, H_kv, D, 0);
+  if (staging_bytes < l0.total) return PS_ERR_WORKSPACE;
+  const size_t ws_bytes = staging_bytes - l0.total;
+  const StagingLayout l = staging_layout(T, B, max_blocks_per_seq, H_q, H_kv, D, 0);
+  uint8_t* st = static_cast<uint8_t*>(staging);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  struct Copy {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } in[] = {
+      {st + l.q, q, static_cast<size_t>(T) * H_q * D * 2},
+      {st + l.k, k, static_cast<size_t>(T) * H_kv * D * 2},
+      {st + l.v, v, static_cast<size_t>(T) * H_kv * D * 2},
+      {st + l.bt, block_tables, static_cast<size_t>(B) * max_blocks_per_seq * 4},
+      {st + l.sl, seq_lens, static_cast<size_t>(B) * 4},
+      {st + l.qsl, query_start_loc, static_cast<size_t>(B + 1) * 4},
+  };
+  for (const Copy& c : in)
+    if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return PS_ERR_CUDA;
+  rc = ps_attention_step(st + l.q, st + l.k, st + l.v, k_pool, v_pool,
+                         reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
+                         reinterpret_cast<const int32_t*>(st + l.sl),
+                         reinterpret_cast<const int32_t*>(st + l.qsl), B, T, H_q, H_kv, D,
+                         num_blocks, scale, st + l.out, reinterpret_cast<int32_t*>(st + l.slots),
+                         st + l.ws, ws_bytes, dtype, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out, st + l.out, static_cast<size_t>(T) * H_q * D * 2,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PS_ERR_CUDA;
+  return PS_OK;
+}
+
 int ps_get_device_error(int* code) {
   if (!code) return PS_ERR_ARG;
   DeviceState* ds;

@@ -316,3 +316,51 @@ NAMED = {
 
 def named(name: str, **kw) -> Workload:
     return NAMED[name](**kw)
+
+
+# --------------------------------------------------------------------------- #
+# device upload and sub-sampling (host plumbing)
+# --------------------------------------------------------------------------- #
+def to_device(a: np.ndarray, dtype: str | None = None, device="cuda"):
+    """A torch tensor on ``device`` holding the array; uint16 bit patterns become f16/bf16."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(
+            {"f16": torch.float16, "bf16": torch.bfloat16}[dtype])
+    else:
+        t = torch.from_numpy(a)
+    return t.to(device)
+
+
+def subset(wl: Workload, step: Step, seqs: list[int]) -> tuple[Workload, Step]:
+    """The sequences ``seqs`` of one step, with a pool holding only the blocks they use.
+
+    Physical block ids are relabelled 0..m-1 in order of first use; values are unchanged.
+    """
+    seqs = list(seqs)
+    bt = step.block_tables[seqs]
+    used = []
+    seen = {}
+    for row in bt:
+        for blk in row:
+            if blk >= 0 and int(blk) not in seen:
+                seen[int(blk)] = len(used)
+                used.append(int(blk))
+    remap = np.vectorize(lambda x: seen.get(int(x), -1), otypes=[np.int32])
+    new_bt = remap(bt) if bt.size else bt.astype(np.int32)
+    n = np.diff(step.query_start_loc)[seqs]
+    qsl = np.zeros(len(seqs) + 1, dtype=np.int32)
+    np.cumsum(n, out=qsl[1:])
+    rows = np.concatenate([np.arange(step.query_start_loc[b], step.query_start_loc[b + 1])
+                           for b in seqs]).astype(np.int64) if seqs else np.zeros(0, np.int64)
+    sub = Workload(name=wl.name + f"[{len(seqs)} seqs]", dtype=wl.dtype, H_q=wl.H_q,
+                   H_kv=wl.H_kv, D=wl.D, num_blocks=max(1, len(used)),
+                   k_pool=wl.k_pool[used] if used else wl.k_pool[:1],
+                   v_pool=wl.v_pool[used] if used else wl.v_pool[:1], description=wl.description)
+    st = Step(q=step.q[rows], k=step.k[rows], v=step.v[rows],
+              block_tables=np.ascontiguousarray(new_bt, dtype=np.int32),
+              seq_lens=step.seq_lens[seqs].copy(), query_start_loc=qsl,
+              seq_ids=step.seq_ids[seqs].copy())
+    sub.steps.append(st)
+    return sub, st

@@ -2,6 +2,9 @@
 the C ABI, and compare with the CPU oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -78,6 +81,13 @@ def check_workload(wl, rows_for_step=None, check_pool=True, separate_calls=False
         err = np.abs(got[sel] - ref[sel])
         assert np.isfinite(got[sel]).all()
         e = float(err.max()) if err.size else 0.0
+        report = os.environ.get("PS_PARITY_REPORT")
+        if report:
+            with open(report, "a") as f:
+                f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "?"),
+                                    "workload": wl.name, "dtype": wl.dtype, "step": si,
+                                    "max_abs_err": e, "tol": TOL[wl.dtype],
+                                    "rows": int(got[sel].shape[0])}) + "\n")
         assert e <= TOL[wl.dtype], f"step {si}: max-abs error {e} > {TOL[wl.dtype]}"
         worst = max(worst, e)
     return worst
