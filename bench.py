@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 from paged_kv_attention_18_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode paged-attn HBM GB/s (% of peak); mixed-batch attention tokens/s"
-L2_BYTES = 129 * 1024 * 1024
+L2_BYTES = 129_000_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_attention_qwen15b_decode_traffic.json")
 KERNEL_SOURCES = ["paged_kv_attention_18_gb300/csrc/ps_attention.cu",
