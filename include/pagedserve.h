@@ -141,6 +141,37 @@ int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
                        void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
+ * ps_paged_attention_noalloc -- ps_paged_attention for callers that cannot allocate.
+ *
+ * The pages describe no such call; it exists for users of this library. Some callers
+ * are handed only their input and output buffers and may not create device memory:
+ * a plug-in inside a host framework whose allocator owns all device memory, or a
+ * latency-critical loop that must not call cudaMalloc/cudaFree (they can synchronise
+ * the device). This variant takes no workspace: its scratch is a fixed device array of
+ * PS_NOALLOC_SCRATCH_BYTES compiled into the library, held by every GPU that loads the
+ * library until the process exits. Arguments and results are those of
+ * ps_paged_attention without workspace/workspace_bytes.
+ *
+ *   - Returns PS_ERR_WORKSPACE, before doing anything, when the batch needs more scratch
+ *     than the fixed maximum (a work list of about H_kv * (T * H_q / H_kv / 16 + B)
+ *     64-byte entries plus 8 bytes per token must fit; long contexts are split into
+ *     fewer parts when the partials would not fit).
+ *   - The first call on each device (with that device current) looks up the array's
+ *     device address with cudaGetSymbolAddress; make that first call before any stream
+ *     capture.
+ *   - Every call reuses the same array and leaves its contents behind; each call
+ *     rewrites what it reads. Calls whose kernels overlap on the device (from two
+ *     streams or two host threads) race on the array: the caller must serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define PS_NOALLOC_SCRATCH_BYTES (32u << 20)
+int ps_paged_attention_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens, const int32_t* query_start_loc, int B,
+                               int T, int H_q, int H_kv, int D, int num_blocks, float scale,
+                               void* out, int dtype, void* stream);
+
+/*
  * ps_attention_step -- the whole step in one call: ps_slot_mapping, ps_reshape_and_cache,
  * then ps_paged_attention, on one stream. k, v are the step's new tokens [T, H_kv, D];
  * slot_mapping is caller-provided device scratch of T int32 (written). Other arguments as

@@ -24,6 +24,8 @@ SIGNATURES = {
     "ps_paged_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "ps_paged_attention": (c_int, [_p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
                                    c_int, c_int, c_float, _p, _p, c_size_t, c_int, _p]),
+    "ps_paged_attention_noalloc": (c_int, [_p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int,
+                                           c_int, c_int, c_int, c_float, _p, c_int, _p]),
     "ps_attention_step": (c_int, [_p, _p, _p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int,
                                   c_int, c_int, c_int, c_float, _p, _p, _p, c_size_t, c_int, _p]),
     "ps_attention_step_host_staging_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int,

@@ -150,6 +150,25 @@ int check_batch(const int32_t* block_tables, int max_blocks, const int32_t* seq_
 
 }  // namespace
 
+namespace ps {
+int current_device(int* num_sms, int** err) {
+  DeviceState* ds;
+  const int rc = current_device_state(&ds);
+  if (rc) return rc;
+  *num_sms = ds->num_sms;
+  *err = ds->err;
+  return PS_OK;
+}
+
+int encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, int D,
+                    bool bf16) {
+  DeviceState* ds;
+  const int rc = current_device_state(&ds);  // makes sure the encoder is resolved
+  if (rc) return rc;
+  return make_pool_map(map, pool, num_blocks, H_kv, D, bf16);
+}
+}  // namespace ps
+
 extern "C" {
 
 const char* ps_status_string(int status) {

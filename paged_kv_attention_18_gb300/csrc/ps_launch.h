@@ -50,4 +50,13 @@ cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtenso
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream);
 
+// Library state of the current device (set up on first use): SM count and the device
+// address of the library's device error word. Returns a ps_status.
+int current_device(int* num_sms, int** err);
+
+// TMA descriptor of a pool [num_blocks, 16, H_kv, D] as a 2-D tensor [num_blocks * 16,
+// H_kv * D] with 64 x 16 boxes and 128-byte swizzle. Returns a ps_status.
+int encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, int D,
+                    bool bf16);
+
 }  // namespace ps
