@@ -223,7 +223,8 @@ const char* ps_status_string(int status);
  * here, not in the timed calls). ps_profile_end() waits for the recorded events and
  * stops recording. ps_profile_read(kind, &ms, &launches) then gives the summed device
  * time and the launch count of one kind: 0 slot mapping, 1 KV scatter, 2 planner,
- * 3 split attention, 4 split combine.
+ * 3 split attention (decode rows), 4 split combine, 5 tile attention (prefill and verify
+ * rows, tcgen05).
  */
 int ps_profile_begin(int max_launches_per_kind);
 int ps_profile_end(void);

@@ -19,7 +19,7 @@ BLOCK_SIZE = 16
 
 # kernel kinds of the timing hook
 PROFILE_KINDS = {"slot_mapping": 0, "reshape_and_cache": 1, "plan": 2, "split_attention": 3,
-                 "combine": 4}
+                 "combine": 4, "tile_attention": 5}
 
 
 class PagedServeError(RuntimeError):

@@ -56,46 +56,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------------
-// workspace layout
-// ---------------------------------------------------------------------------------
-struct Layout {
-  size_t hdr, items, seq_off, tok_ns, tok_base, fixed_end;
-  int cap_items;
-};
-
-Layout fixed_layout(int T, int B, int H_q, int H_kv) {
-  Layout l;
-  const int64_t G = H_q / H_kv;
-  const int64_t groups = (static_cast<int64_t>(T) * G + 15) / 16;
-  const int64_t split_seqs = B < T ? B : T;
-  int64_t cap = static_cast<int64_t>(H_kv) *
-                (groups + B + split_seqs * ps::kSplitGroupLimit * (ps::kMaxSplits - 1));
-  if (cap < 1) cap = 1;
-  l.cap_items = static_cast<int>(cap);
-  l.hdr = 0;
-  l.items = 256;
-  l.seq_off = align_up(l.items + static_cast<size_t>(cap) * sizeof(ps::WorkItem), 256);
-  l.tok_ns = align_up(l.seq_off + static_cast<size_t>(B + 1) * 4, 256);
-  l.tok_base = align_up(l.tok_ns + static_cast<size_t>(T) * 4, 256);
-  l.fixed_end = align_up(l.tok_base + static_cast<size_t>(T) * 4, 256);
-  return l;
-}
-
-size_t partial_bytes(int64_t cap_part, int D) {
-  return align_up(static_cast<size_t>(cap_part) * 4, 256) + static_cast<size_t>(cap_part) * D * 4;
-}
-
-// ---------------------------------------------------------------------------------
 // timing hook
 // ---------------------------------------------------------------------------------
-constexpr int kKinds = 5;
+constexpr int kKinds = 6;
 struct Profile {
   bool on = false;
   int cap = 0;
   std::vector<cudaEvent_t> ev[kKinds];  // pairs: start, stop
-  int used[kKinds] = {0, 0, 0, 0, 0};
-  float ms[kKinds] = {0, 0, 0, 0, 0};
-  int done[kKinds] = {0, 0, 0, 0, 0};
+  int used[kKinds] = {};
+  float ms[kKinds] = {};
+  int done[kKinds] = {};
 };
 Profile g_prof;
 std::mutex g_prof_mu;
@@ -131,6 +101,23 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, 
   return r == CUDA_SUCCESS ? PS_OK : PS_ERR_CUDA;
 }
 
+// q [T, H_q, D] as a 3-D tensor (D, H_q, T) with boxes of 64 elements x G heads x tpt
+// tokens: one box is tpt whole tokens of the G query heads that share one KV head.
+int make_q_map(CUtensorMap* map, const void* q, int T, int H_q, int D, int G, int tpt, bool bf16) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_q),
+                              static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H_q) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tpt)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(
+      map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+      const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PS_OK : PS_ERR_CUDA;
+}
+
 int check_shapes(int H_q, int H_kv, int D, int dtype) {
   if (H_q <= 0 || H_kv <= 0) return PS_ERR_ARG;
   if (dtype != PS_F16 && dtype != PS_BF16) return PS_ERR_UNSUPPORTED;
@@ -151,6 +138,109 @@ int check_batch(const int32_t* block_tables, int max_blocks, const int32_t* seq_
 }  // namespace
 
 namespace ps {
+
+namespace {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+size_t workspace_fixed_bytes(int T, int B, int H_q, int H_kv, bool headroom, int* cap_items,
+                             int* cap_tile) {
+  const int64_t G = H_q / H_kv;
+  const int tpt = tile_tokens(static_cast<int>(G));
+  const int64_t split_seqs = B < T ? B : T;
+  int64_t ci = static_cast<int64_t>(H_kv) * ((static_cast<int64_t>(T) * G + 15) / 16 + B);
+  int64_t ct = tpt > 0 ? static_cast<int64_t>(H_kv) * ((T + tpt - 1) / tpt + B) : 1;
+  if (headroom) {
+    ci += static_cast<int64_t>(H_kv) * split_seqs * kSplitGroupLimit * (kMaxSplits - 1);
+    if (tpt > 0) ct += static_cast<int64_t>(H_kv) * split_seqs * kTileSplitQTiles * (kMaxSplits - 1);
+  }
+  if (ci < 1) ci = 1;
+  if (ct < 1) ct = 1;
+  if (cap_items) *cap_items = static_cast<int>(ci);
+  if (cap_tile) *cap_tile = static_cast<int>(ct);
+  size_t o = 256;                                                   // header
+  o = up256(o + static_cast<size_t>(ci) * sizeof(WorkItem));        // split items
+  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off
+  o = up256(o + static_cast<size_t>(ct) * sizeof(WorkItem));        // tile items
+  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_t
+  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_ns
+  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_base
+  return o;
+}
+
+size_t partial_bytes(int64_t cap_part, int D) {
+  return up256(static_cast<size_t>(cap_part) * 4) + static_cast<size_t>(cap_part) * D * 4;
+}
+
+bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink) {
+  int ci = 0, ct = 0;
+  size_t fixed = workspace_fixed_bytes(p.T, p.B, p.H_q, p.H_kv, true, &ci, &ct);
+  if (fixed > bytes) {
+    if (!shrink) return false;
+    fixed = workspace_fixed_bytes(p.T, p.B, p.H_q, p.H_kv, false, &ci, &ct);
+    if (fixed > bytes) return false;
+  }
+  size_t o = 256;
+  p.hdr = reinterpret_cast<int*>(ws);
+  p.items = reinterpret_cast<WorkItem*>(ws + o);
+  o = up256(o + static_cast<size_t>(ci) * sizeof(WorkItem));
+  p.seq_off = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.B + 1) * 4);
+  p.tile_items = reinterpret_cast<WorkItem*>(ws + o);
+  o = up256(o + static_cast<size_t>(ct) * sizeof(WorkItem));
+  p.seq_off_t = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.B + 1) * 4);
+  p.tok_ns = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.T) * 4);
+  p.tok_base = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.T) * 4);
+  // the rest holds split partials
+  const size_t left = bytes - o;
+  int64_t part = static_cast<int64_t>(left / ((p.D + 1) * 4));
+  while (part > 0 && partial_bytes(part, p.D) > left) --part;
+  if (part > INT32_MAX) part = INT32_MAX;
+  p.part_lse = reinterpret_cast<float*>(ws + o);
+  p.part_o = reinterpret_cast<float*>(ws + o + up256(static_cast<size_t>(part) * 4));
+  p.cap_items = ci;
+  p.cap_tile = ct;
+  p.cap_part = static_cast<int>(part);
+  return true;
+}
+
+int run_attention(const AttnParams& p0, const void* k_pool, const void* v_pool, bool bf16,
+                  cudaStream_t s) {
+  AttnParams p = p0;
+  int num_sms = 0;
+  int* err = nullptr;
+  int rc = current_device(&num_sms, &err);
+  if (rc) return rc;
+  p.err = err;
+  CUtensorMap kmap, vmap, qmap;
+  if ((rc = make_pool_map(&kmap, k_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
+  if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
+  if (p.tpt > 0 && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
+  const int concurrency = attention_ctas(p.D, num_sms) * attention_warps(p.D);
+  {
+    Timed tm(2, s);
+    if (launch_plan(p, concurrency, num_sms, s) != cudaSuccess) return PS_ERR_CUDA;
+  }
+  {
+    Timed tm(3, s);
+    if (launch_split_attention(p, bf16, kmap, vmap, num_sms, s) != cudaSuccess)
+      return PS_ERR_CUDA;
+  }
+  if (p.tpt > 0) {
+    Timed tm(5, s);
+    if (launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s) != cudaSuccess)
+      return PS_ERR_CUDA;
+  }
+  {
+    Timed tm(4, s);
+    if (launch_combine(p, bf16, s) != cudaSuccess) return PS_ERR_CUDA;
+  }
+  return PS_OK;
+}
+
 int current_device(int* num_sms, int** err) {
   DeviceState* ds;
   const int rc = current_device_state(&ds);
@@ -223,13 +313,13 @@ size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
                                          int max_seq_len) {
   if (T < 0 || B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || (D != 64 && D != 128))
     return 0;
-  const Layout l = fixed_layout(T, B, H_q, H_kv);
+  const size_t fixed = ps::workspace_fixed_bytes(T, B, H_q, H_kv, true, nullptr, nullptr);
   int64_t splits = (static_cast<int64_t>(max_seq_len) + ps::kBlockSize * ps::kMinSplitPages - 1) /
                    (ps::kBlockSize * ps::kMinSplitPages);
   if (splits > ps::kMaxSplits) splits = ps::kMaxSplits;
   if (splits < 2) splits = 0;  // nothing to split
   const int64_t cap_part = static_cast<int64_t>(T) * H_q * splits;
-  return l.fixed_end + partial_bytes(cap_part, D);
+  return fixed + ps::partial_bytes(cap_part, D);
 }
 
 namespace {
@@ -249,7 +339,8 @@ int check_attention(const void* q, const void* k_pool, const void* v_pool,
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PS_ERR_ALIGN;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PS_ERR_WORKSPACE;
-  if (workspace_bytes < fixed_layout(T, B, H_q, H_kv).fixed_end) return PS_ERR_WORKSPACE;
+  if (workspace_bytes < ps::workspace_fixed_bytes(T, B, H_q, H_kv, true, nullptr, nullptr))
+    return PS_ERR_WORKSPACE;
   return PS_OK;
 }
 }  // namespace
@@ -264,20 +355,6 @@ int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
                            workspace_bytes, dtype);
   if (rc) return rc;
   if (T == 0) return PS_OK;
-  const Layout l = fixed_layout(T, B, H_q, H_kv);
-  // the rest of the workspace holds split partials
-  int64_t cap_part = static_cast<int64_t>((workspace_bytes - l.fixed_end) / ((D + 1) * 4));
-  while (cap_part > 0 && partial_bytes(cap_part, D) > workspace_bytes - l.fixed_end) --cap_part;
-  if (cap_part > INT32_MAX) cap_part = INT32_MAX;
-
-  DeviceState* ds;
-  if ((rc = current_device_state(&ds))) return rc;
-  const bool bf16 = dtype == PS_BF16;
-  CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_pool, num_blocks, H_kv, D, bf16))) return rc;
-  if ((rc = make_pool_map(&vmap, v_pool, num_blocks, H_kv, D, bf16))) return rc;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   ps::AttnParams p{};
   p.q = q;
   p.out = out;
@@ -293,33 +370,10 @@ int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
   p.G = H_q / H_kv;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.hdr = reinterpret_cast<int*>(ws + l.hdr);
-  p.items = reinterpret_cast<ps::WorkItem*>(ws + l.items);
-  p.seq_off = reinterpret_cast<int*>(ws + l.seq_off);
-  p.tok_ns = reinterpret_cast<int*>(ws + l.tok_ns);
-  p.tok_base = reinterpret_cast<int*>(ws + l.tok_base);
-  p.part_lse = reinterpret_cast<float*>(ws + l.fixed_end);
-  p.part_o = reinterpret_cast<float*>(ws + l.fixed_end + align_up(static_cast<size_t>(cap_part) * 4, 256));
-  p.cap_items = l.cap_items;
-  p.cap_part = static_cast<int>(cap_part);
-  p.err = ds->err;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int concurrency = ps::attention_ctas(D, ds->num_sms) * ps::attention_warps(D);
-  {
-    Timed tm(2, s);
-    if (ps::launch_plan(p, concurrency, s) != cudaSuccess) return PS_ERR_CUDA;
-  }
-  {
-    Timed tm(3, s);
-    if (ps::launch_split_attention(p, bf16, kmap, vmap, ds->num_sms, s) != cudaSuccess)
-      return PS_ERR_CUDA;
-  }
-  {
-    Timed tm(4, s);
-    if (ps::launch_combine(p, bf16, s) != cudaSuccess) return PS_ERR_CUDA;
-  }
-  return PS_OK;
+  p.tpt = ps::tile_tokens(p.G);
+  if (!ps::layout_workspace(p, static_cast<uint8_t*>(workspace), workspace_bytes, false))
+    return PS_ERR_WORKSPACE;
+  return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream));
 }
 
 int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,

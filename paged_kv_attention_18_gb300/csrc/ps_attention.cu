@@ -24,9 +24,11 @@ namespace ps {
 // planner
 // ----------------------------------------------------------------------------------
 struct SeqInfo {
-  int n, L, valid, groups, pages, tok0;
+  int n, L, valid, groups, pages, tok0, tile, qtiles;
 };
 
+// groups: 16-row groups of the split kernel; tile / qtiles: the sequence goes to the tile
+// kernel (more than 16 packed rows and a tile size exists) in qtiles 128-row tiles.
 __device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
   SeqInfo s;
   s.tok0 = p.qsl[b];
@@ -36,12 +38,21 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
   s.valid = s.n >= 0 && s.n <= s.L && s.pages <= p.max_blocks;
   const int rows = s.valid ? s.n * p.G : 0;
   s.groups = (rows + 15) / 16;
+  s.tile = p.tpt > 0 && s.groups > 1;
+  s.qtiles = s.tile ? (s.n + p.tpt - 1) / p.tpt : 0;
   return s;
 }
 
-__device__ __forceinline__ int seq_splits(const SeqInfo& s, int pps) {
+__device__ __forceinline__ int seq_splits(const SeqInfo& s, int pps_dec, int pps_tile) {
   if (s.groups == 0) return 0;
-  if (s.groups > kSplitGroupLimit) return 1;
+  int pps;
+  if (s.tile) {
+    if (s.qtiles > kTileSplitQTiles) return 1;
+    pps = pps_tile;
+  } else {
+    if (s.groups > kSplitGroupLimit) return 1;
+    pps = pps_dec;
+  }
   int ns = (s.pages + pps - 1) / pps;
   ns = ns < 1 ? 1 : ns;
   ns = ns > kMaxSplits ? kMaxSplits : ns;
@@ -97,42 +108,69 @@ __device__ long long block_sum_ll(long long v, long long* sh) {
   return t;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency) {
+__device__ __forceinline__ int pages_per_split(long long work, long long workers, int align) {
+  const long long target = workers * 4;
+  long long pps = (work + target - 1) / (target > 0 ? target : 1);
+  if (pps < kMinSplitPages) pps = kMinSplitPages;
+  pps = (pps + align - 1) / align * align;
+  return static_cast<int>(pps > (1 << 24) ? (1 << 24) : pps);
+}
+
+__device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& it) {
+  const int4* src = reinterpret_cast<const int4*>(&it);
+  int4* dst = reinterpret_cast<int4*>(dst_item);
+  dst[0] = src[0];
+  dst[1] = src[1];
+  dst[2] = src[2];
+  dst[3] = src[3];
+}
+
+// One CTA turns the batch into two work lists: split-kernel items (sequences with at most
+// 16 packed rows: decodes) and tile-kernel items (prefill chunks, verify rows), plus the
+// per-token split table that the combine kernel reads.
+__global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
+                                                    int tile_ctas) {
   __shared__ int sh[32];
   __shared__ long long shl[32];
   const int tid = threadIdx.x, nth = blockDim.x;
 
-  // cost of the batch in pages read (every row group reads up to the whole context)
-  long long w = 0;
+  // cost of the batch in pages read, per kernel
+  long long wd = 0, wt = 0;
   for (int b = tid; b < p.B; b += nth) {
     const SeqInfo s = seq_info(p, b);
     if (!s.valid) {
       record_error(p.err, kDevBadSequence);
       continue;
     }
-    w += static_cast<long long>(s.groups) * s.pages;
+    if (s.tile) wt += static_cast<long long>(s.qtiles) * s.pages;
+    else wd += static_cast<long long>(s.groups) * s.pages;
   }
-  const long long W = block_sum_ll(w, shl) * p.H_kv;
-  const long long target = static_cast<long long>(concurrency) * 4;
-  long long pps_ll = (W + target - 1) / (target > 0 ? target : 1);
-  int pps = static_cast<int>(pps_ll < kMinSplitPages ? kMinSplitPages
-                             : (pps_ll > (1 << 24) ? (1 << 24) : pps_ll));
+  const long long Wd = block_sum_ll(wd, shl) * p.H_kv;
+  const long long Wt = block_sum_ll(wt, shl) * p.H_kv;
+  int pps_d = pages_per_split(Wd, concurrency, 1);
+  int pps_t = pages_per_split(Wt, tile_ctas, kTilePagesAlign);
 
-  int n_items = 0, n_part = 0;
+  int n_dec = 0, n_tile = 0, n_part = 0;
   for (int attempt = 0; attempt < 32; ++attempt) {
-    // items of every sequence
-    int running = 0;
+    int run_d = 0, run_t = 0;
     for (int base = 0; base < p.B; base += nth) {
       const int b = base + tid;
-      int cnt = 0;
+      int cd = 0, ct = 0;
       if (b < p.B) {
         const SeqInfo s = seq_info(p, b);
-        cnt = s.groups * seq_splits(s, pps) * p.H_kv;
+        const int ns = seq_splits(s, pps_d, pps_t);
+        if (s.tile) ct = s.qtiles * ns * p.H_kv;
+        else cd = s.groups * ns * p.H_kv;
       }
-      int total;
-      const int ex = block_exscan(cnt, sh, total);
-      if (b < p.B) p.seq_off[b] = running + ex;
-      running += total;
+      int td, tt;
+      const int exd = block_exscan(cd, sh, td);
+      const int ext = block_exscan(ct, sh, tt);
+      if (b < p.B) {
+        p.seq_off[b] = run_d + exd;
+        p.seq_off_t[b] = run_t + ext;
+      }
+      run_d += td;
+      run_t += tt;
     }
     // partial entries of every token whose rows are split
     int prun = 0;
@@ -143,7 +181,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
         const int b = last_le(p.qsl, p.B, t);
         const SeqInfo s = seq_info(p, b);
         if (s.valid && s.groups > 0) {
-          const int ns = seq_splits(s, pps);
+          const int ns = seq_splits(s, pps_d, pps_t);
           const int pos = s.L - s.n + (t - s.tok0);
           const int page = pos / kBlockSize;
           for (int k = 0; k < ns; ++k)
@@ -159,24 +197,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       }
       prun += total;
     }
-    n_items = running;
+    n_dec = run_d;
+    n_tile = run_t;
     n_part = prun;
-    if (n_items <= p.cap_items && n_part <= p.cap_part) break;
-    if (pps >= (1 << 24)) {  // cannot shrink further: leave nothing to do
+    if (n_dec <= p.cap_items && n_tile <= p.cap_tile && n_part <= p.cap_part) break;
+    if (pps_d >= (1 << 24) && pps_t >= (1 << 24)) {  // cannot shrink further
       record_error(p.err, kDevPlanOverflow);
-      n_items = 0;
+      n_dec = n_tile = 0;
       break;
     }
-    pps *= 2;
+    pps_d = pps_d >= (1 << 23) ? (1 << 24) : 2 * pps_d;
+    pps_t = pps_t >= (1 << 23) ? (1 << 24) : 2 * pps_t;
   }
-  if (tid == 0) p.seq_off[p.B] = n_items;
+  if (tid == 0) {
+    p.seq_off[p.B] = n_dec;
+    p.seq_off_t[p.B] = n_tile;
+  }
   __syncthreads();
 
-  // emit the items, group index fastest so rows sharing pages run back to back
-  for (int i = tid; i < n_items; i += nth) {
+  // split-kernel items, group index fastest so rows sharing pages run back to back
+  for (int i = tid; i < n_dec; i += nth) {
     const int b = last_le(p.seq_off, p.B, i);
     const SeqInfo s = seq_info(p, b);
-    const int ns = seq_splits(s, pps);
+    const int ns = seq_splits(s, pps_d, pps_t);
     const int local = i - p.seq_off[b];
     const int j = local % s.groups;
     const int rest = local / s.groups;
@@ -198,18 +241,43 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     it.n_query = s.n;
     it.tok0 = s.tok0;
     it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
-    const int4* src = reinterpret_cast<const int4*>(&it);
-    int4* dst = reinterpret_cast<int4*>(p.items + i);
-    dst[0] = src[0];
-    dst[1] = src[1];
-    dst[2] = src[2];
-    dst[3] = src[3];
+    store_item(p.items + i, it);
+  }
+  // tile-kernel items: the last (longest) query tile of a sequence first
+  for (int i = tid; i < n_tile; i += nth) {
+    const int b = last_le(p.seq_off_t, p.B, i);
+    const SeqInfo s = seq_info(p, b);
+    const int ns = seq_splits(s, pps_d, pps_t);
+    const int local = i - p.seq_off_t[b];
+    const int j = s.qtiles - 1 - local % s.qtiles;
+    const int rest = local / s.qtiles;
+    const int kv = rest % p.H_kv;
+    const int sp = rest / p.H_kv;
+    WorkItem it;
+    it.seq = b;
+    it.kv = kv;
+    it.row0 = j * p.tpt * p.G;
+    it.nrows = min(p.tpt, s.n - j * p.tpt) * p.G;
+    const int i_last = j * p.tpt + it.nrows / p.G - 1;
+    const int page_last = (s.L - s.n + i_last) / kBlockSize;
+    it.page_begin = (sp * s.pages) / ns;
+    it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
+    it.split = sp;
+    it.nsplit = ns;
+    it.ctx_len = s.L;
+    it.n_query = s.n;
+    it.tok0 = s.tok0;
+    it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
+    store_item(p.tile_items + i, it);
   }
   if (tid == 0) {
-    p.hdr[0] = n_items;
+    p.hdr[0] = n_dec;
     p.hdr[1] = 0;
-    p.hdr[2] = pps;
+    p.hdr[2] = pps_d;
     p.hdr[3] = n_part;
+    p.hdr[4] = n_tile;
+    p.hdr[5] = 0;
+    p.hdr[6] = pps_t;
   }
 }
 
@@ -435,7 +503,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
       start_item();
     }
     const uint32_t st = g_comp % S;
-    if (!mbar_wait(&full[st], (g_comp / S) & 1)) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (g_comp / S) & 1))) {
       if (lane == 0) record_error(p.err, kDevWaitTimeout);
       aborted = true;
       break;
@@ -590,8 +658,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
 int attention_warps(int D) { return D == 128 ? SplitCfg<128>::kWarps : SplitCfg<64>::kWarps; }
 int attention_ctas(int D, int num_sms) { (void)D; return num_sms; }
 
-cudaError_t launch_plan(const AttnParams& p, int concurrency, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(p, concurrency);
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
+                        cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(p, concurrency, tile_ctas);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,8 @@ constexpr int kBlockSize = 16;      // tokens per KV block (page)
 constexpr int kMaxSplits = 32;      // KV splits of one query row, at most
 constexpr int kMinSplitPages = 8;   // pages in one split, at least
 constexpr int kSplitGroupLimit = 4; // only sequences with <= this many 16-row groups split
+constexpr int kTileSplitQTiles = 2; // tile-class sequences with <= this many query tiles split
+constexpr int kTilePagesAlign = 8;  // tile-class split sizes are whole 128-key tiles
 
 // Device error codes, stored in the library's device error word. A kernel that meets
 // an invalid index records the first such code and skips the access; it never traps.
@@ -128,6 +130,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// 3-D tile load global -> shared.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 

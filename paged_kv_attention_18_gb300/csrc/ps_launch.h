@@ -20,9 +20,15 @@ struct AttnParams {
   int B, T, H_q, H_kv, D, G, num_blocks;
   float scale_log2;              // softmax scale * log2(e)
   // workspace
-  int* hdr;                      // [0] items, [1] fetch counter, [2] pages per split, [3] partials
-  WorkItem* items;               // [cap_items]
-  int* seq_off;                  // [B + 1] first item of each sequence
+  // [0] split-kernel items, [1] their fetch counter, [2] pages per split, [3] partials,
+  // [4] tile-kernel items, [5] their fetch counter, [6] tile pages per split
+  int* hdr;
+  WorkItem* items;               // [cap_items] split-kernel work (decode rows)
+  int* seq_off;                  // [B + 1] first split-kernel item of each sequence
+  WorkItem* tile_items;          // [cap_tile] tile-kernel work (prefill / verify rows)
+  int* seq_off_t;                // [B + 1] first tile-kernel item of each sequence
+  int cap_tile;
+  int tpt;                       // query tokens per 128-row tile (0: no tile kernel)
   int* tok_ns;                   // [T] splits holding each token's rows (0 = none)
   int* tok_base;                 // [T] first partial entry of each token
   float* part_lse;               // [cap_part] log2-sum-exp of each partial
@@ -43,12 +49,35 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
 int attention_ctas(int D, int num_sms);
 int attention_warps(int D);
 
-cudaError_t launch_plan(const AttnParams& p, int concurrency, cudaStream_t stream);
+// concurrency: split-kernel warps; tile_ctas: tile-kernel CTAs (work is sized for both)
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, cudaStream_t stream);
+
+// Query tokens per 128-row tile for G query heads per KV head (0 = use the split kernel).
+int tile_tokens(int G);
+
+cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
+                                  cudaStream_t stream);
 
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream);
+
+// Workspace bytes before the split partials (header, work lists, per-token tables);
+// `headroom` reserves work-list room for splitting long contexts.
+size_t workspace_fixed_bytes(int T, int B, int H_q, int H_kv, bool headroom, int* cap_items,
+                             int* cap_tile);
+size_t partial_bytes(int64_t cap_part, int D);
+
+// Point p's workspace fields into `ws` (bytes long); the partials take what is left. With
+// `shrink`, the work lists fall back to their unsplit size when the headroom does not fit.
+// False when even that does not fit.
+bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink);
+
+// Plan, split kernel, tile kernel, combine on `s` (p's problem and workspace fields set).
+int run_attention(const AttnParams& p, const void* k_pool, const void* v_pool, bool bf16,
+                  cudaStream_t s);
 
 // Library state of the current device (set up on first use): SM count and the device
 // address of the library's device error word. Returns a ps_status.

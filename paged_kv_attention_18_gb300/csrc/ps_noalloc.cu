@@ -7,7 +7,7 @@
 // latency-critical serving loop that must never call cudaMalloc/cudaFree because they
 // can synchronise the whole device and stall every stream.
 //
-// How it works: the planner's work list, the per-token split table and the split
+// How it works: the planner's work lists, the per-token split table and the split
 // partials are laid out in `g_noalloc_scratch`, a file-scope __device__ array of
 // PS_NOALLOC_SCRATCH_BYTES. Host code cannot use the array's name as a device address,
 // so the first call on each device (with that device current) looks the address up with
@@ -46,50 +46,6 @@ int scratch_address(uint8_t** out) {
   return PS_OK;
 }
 
-size_t up256(size_t x) { return (x + 255) / 256 * 256; }
-
-struct Plan {
-  size_t items, seq_off, tok_ns, tok_base, part_lse, part_o;
-  int cap_items, cap_part;
-};
-
-// Lay the plan out in the fixed array. The work list first gets room for splitting long
-// contexts; if that does not fit it shrinks to what an unsplit plan needs. The split
-// partials take the rest. Returns false when even the unsplit plan does not fit.
-bool layout(int T, int B, int H_q, int H_kv, int D, Plan* pl) {
-  const int64_t G = H_q / H_kv;
-  const int64_t min_items = static_cast<int64_t>(H_kv) * ((static_cast<int64_t>(T) * G + 15) / 16 + B);
-  const int64_t split_seqs = B < T ? B : T;
-  const int64_t want_items =
-      min_items + static_cast<int64_t>(H_kv) * split_seqs * ps::kSplitGroupLimit * (ps::kMaxSplits - 1);
-  auto fixed = [&](int64_t cap) {
-    size_t o = 256;  // header
-    o = up256(o + static_cast<size_t>(cap) * sizeof(ps::WorkItem));
-    o = up256(o + static_cast<size_t>(B + 1) * 4);
-    o = up256(o + static_cast<size_t>(T) * 4);
-    o = up256(o + static_cast<size_t>(T) * 4);
-    return o;
-  };
-  int64_t cap = want_items;
-  if (fixed(cap) > PS_NOALLOC_SCRATCH_BYTES) cap = min_items;
-  if (cap < 1) cap = 1;
-  if (fixed(cap) > PS_NOALLOC_SCRATCH_BYTES) return false;
-  pl->cap_items = static_cast<int>(cap);
-  pl->items = 256;
-  pl->seq_off = up256(pl->items + static_cast<size_t>(cap) * sizeof(ps::WorkItem));
-  pl->tok_ns = up256(pl->seq_off + static_cast<size_t>(B + 1) * 4);
-  pl->tok_base = up256(pl->tok_ns + static_cast<size_t>(T) * 4);
-  pl->part_lse = up256(pl->tok_base + static_cast<size_t>(T) * 4);
-  const size_t left = PS_NOALLOC_SCRATCH_BYTES - pl->part_lse;
-  int64_t part = static_cast<int64_t>(left / ((D + 1) * 4));
-  while (part > 0 && up256(static_cast<size_t>(part) * 4) + static_cast<size_t>(part) * D * 4 > left)
-    --part;
-  if (part > INT32_MAX) part = INT32_MAX;
-  pl->cap_part = static_cast<int>(part);
-  pl->part_o = pl->part_lse + up256(static_cast<size_t>(part) * 4);
-  return true;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -112,20 +68,14 @@ extern "C" int ps_paged_attention_noalloc(const void* q, const void* k_pool, con
     return PS_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PS_ERR_ALIGN;
-  Plan pl;
-  if (!layout(T, B, H_q, H_kv, D, &pl)) return PS_ERR_WORKSPACE;  // beyond the fixed maximum
+  // beyond the fixed maximum even without room for splitting: reject before device work
+  if (ps::workspace_fixed_bytes(T, B, H_q, H_kv, false, nullptr, nullptr) >
+      PS_NOALLOC_SCRATCH_BYTES)
+    return PS_ERR_WORKSPACE;
 
   uint8_t* ws = nullptr;
-  int rc = scratch_address(&ws);
+  const int rc = scratch_address(&ws);
   if (rc) return rc;
-  int num_sms = 0;
-  int* err = nullptr;
-  if ((rc = ps::current_device(&num_sms, &err))) return rc;
-  const bool bf16 = dtype == PS_BF16;
-  CUtensorMap kmap, vmap;
-  if ((rc = ps::encode_pool_map(&kmap, k_pool, num_blocks, H_kv, D, bf16))) return rc;
-  if ((rc = ps::encode_pool_map(&vmap, v_pool, num_blocks, H_kv, D, bf16))) return rc;
-
   ps::AttnParams p{};
   p.q = q;
   p.out = out;
@@ -141,22 +91,7 @@ extern "C" int ps_paged_attention_noalloc(const void* q, const void* k_pool, con
   p.G = H_q / H_kv;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.hdr = reinterpret_cast<int*>(ws);
-  p.items = reinterpret_cast<ps::WorkItem*>(ws + pl.items);
-  p.seq_off = reinterpret_cast<int*>(ws + pl.seq_off);
-  p.tok_ns = reinterpret_cast<int*>(ws + pl.tok_ns);
-  p.tok_base = reinterpret_cast<int*>(ws + pl.tok_base);
-  p.part_lse = reinterpret_cast<float*>(ws + pl.part_lse);
-  p.part_o = reinterpret_cast<float*>(ws + pl.part_o);
-  p.cap_items = pl.cap_items;
-  p.cap_part = pl.cap_part;
-  p.err = err;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int concurrency = ps::attention_ctas(D, num_sms) * ps::attention_warps(D);
-  if (ps::launch_plan(p, concurrency, s) != cudaSuccess) return PS_ERR_CUDA;
-  if (ps::launch_split_attention(p, bf16, kmap, vmap, num_sms, s) != cudaSuccess)
-    return PS_ERR_CUDA;
-  if (ps::launch_combine(p, bf16, s) != cudaSuccess) return PS_ERR_CUDA;
-  return PS_OK;
+  p.tpt = ps::tile_tokens(p.G);
+  if (!ps::layout_workspace(p, ws, PS_NOALLOC_SCRATCH_BYTES, true)) return PS_ERR_WORKSPACE;
+  return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream));
 }

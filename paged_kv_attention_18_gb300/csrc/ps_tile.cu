@@ -1,0 +1,437 @@
+// Tile kernel for prefill chunks and speculative-verify rows: tcgen05 MMA with TMEM
+// accumulators, K/V pages fed by TMA straight from the paged pool.
+//
+// One work item is up to 128 packed query rows of one sequence and one KV head (whole
+// query tokens x the G query heads that share the KV head), over one split of the
+// context. For each tile of 128 keys (8 pages of 16):
+//     S = Q K^T            tcgen05.mma, A = Q (smem), B = K (smem), D = S in TMEM
+//     P = exp2(S*scale*log2e - m), online row max / sum   (softmax warps, from TMEM)
+//     O += P V             tcgen05.mma, A = P (smem), B = V (smem, MN-major), D = O in TMEM
+// with the causal rule of the pages (key j visible to the query at position p iff
+// j <= p: PageServe section 01; tinyserve "How it works", stepped causal mask) and
+// grouped-query attention (tinyserve "Highlights" table).
+//
+// Warp roles (192 threads): warp 0 issues TMA and hands out work items, warp 1 owns
+// TMEM and issues the MMAs, warps 2..5 run the softmax and the epilogue with one TMEM
+// lane (one query row) per thread. S is double-buffered in TMEM so the tensor core
+// computes S for tile j+1 while the softmax works on tile j. O is rescaled lazily: only
+// when a row's running max grows by more than 2^8, so most tiles never touch O.
+#include "ps_common.cuh"
+#include "ps_launch.h"
+#include "ps_tc05.cuh"
+
+namespace ps {
+
+namespace {
+
+constexpr int kRows = 128;        // query rows per tile (MMA M)
+constexpr int kKeys = 128;        // keys per KV tile (MMA N of S, K of PV) = 8 pages
+constexpr int kPagesPerTile = kKeys / kBlockSize;
+constexpr int kSub = kRows * 128; // bytes of one [128 rows x 64 elements] swizzled sub-tile
+constexpr int kStages = 2;        // K/V tile stages
+constexpr int kItemRing = 4;
+constexpr int kThreads = 192;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 2 * kKeys;
+
+template <int D>
+struct TileSmem {
+  static constexpr int kQ = (D / 64) * kSub;        // Q tile
+  static constexpr int kK = (D / 64) * kSub;        // K tile (128 keys)
+  static constexpr int kStage = 2 * kK;             // K + V
+  static constexpr int kP = 2 * kSub;               // P tile (128 rows x 128 keys)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kQ;
+  static constexpr int kOffP = kOffKV + kStages * kStage;
+  static constexpr int kOffBar = kOffP + kP;
+  static constexpr int kBytes = kOffBar + 512 + 1024;  // barriers, ring, slack for alignment
+};
+
+struct TileBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full, o_done, o_free, mma_final;
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
+  int item_idx[kItemRing];
+  uint32_t tmem_base;
+  int abort;
+};
+
+}  // namespace
+
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tile_attention_kernel(const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ CUtensorMap qmap, const AttnParams p) {
+  using L = TileSmem<D>;
+  constexpr int kHalves = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  TileBars* bars = reinterpret_cast<TileBars*>(smem + L::kOffBar);
+  const uint32_t sQ = smem_u32(smem + L::kOffQ);
+  const uint32_t sKV = smem_u32(smem + L::kOffKV);
+  const uint32_t sP = smem_u32(smem + L::kOffP);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
+  if (n_items == 0) return;  // nothing planned for this kernel (uniform across the grid)
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_free, 4);
+    mbar_init(&bars->mma_final, 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 5);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort;
+
+  // Bounded wait with a warp-uniform outcome: if any lane gives up (or another role has
+  // given up), the whole warp leaves its loop together.
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    bool ok = !*abort_flag && mbar_wait(bar, parity);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) {
+      record_error(p.err, kDevWaitTimeout);
+      *abort_flag = 1;
+    }
+    return ok;
+  };
+
+  if (warp == 0) {
+    // ============================ producer ==========================================
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&qmap);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t g = 0, qi = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it % kItemRing;
+      if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
+      int idx = 0;
+      if (lane == 0) {
+        idx = atomicAdd(p.hdr + 5, 1);
+        if (idx >= n_items) idx = -1;
+        bars->item_idx[slot] = idx;
+        mbar_arrive(&bars->item_full[slot]);
+      }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx < 0) break;
+      const WorkItem& w = p.tile_items[idx];
+      const int pb = w.page_begin, pe = w.page_end;
+      if (pe <= pb) continue;
+      const int seq = w.seq, kv = w.kv;
+      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
+      // Q tile: whole tokens x the G heads of this KV head
+      if (!wait(&bars->q_empty, (qi & 1) ^ 1)) break;
+      if (lane == 0) {
+        const int tok = w.tok0 + w.row0 / p.G;
+        mbar_arrive_expect_tx(&bars->q_full, kHalves * 64 * 2 * p.G * p.tpt);
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_3d(smem + L::kOffQ + h * kSub, &qmap, &bars->q_full, h * 64, kv * p.G, tok);
+      }
+      ++qi;
+      // K/V tiles, 8 pages each; pages past the split read the zero fill
+      const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
+      int bt_base = -1000, bt_reg = -1;
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const int first = pb + j * kPagesPerTile;
+        if (first - bt_base + kPagesPerTile > 32) {
+          bt_base = first;
+          bt_reg = first + lane < pe ? __ldg(bt + first + lane) : -1;
+        }
+        const uint32_t st = g % kStages;
+        if (!wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1)) { ok = false; break; }
+        int blk[kPagesPerTile];
+#pragma unroll
+        for (int pp = 0; pp < kPagesPerTile; ++pp)
+          blk[pp] = __shfl_sync(0xffffffffu, bt_reg, first - bt_base + pp);
+        if (lane == 0) {
+          uint8_t* kdst = smem + L::kOffKV + st * L::kStage;
+          uint8_t* vdst = kdst + L::kK;
+          mbar_arrive_expect_tx(&bars->kv_full[st], L::kStage);
+#pragma unroll
+          for (int pp = 0; pp < kPagesPerTile; ++pp) {
+            int row;
+            if (first + pp >= pe) {
+              row = p.num_blocks * kBlockSize;  // past the pool: zero fill, no HBM read
+            } else if (blk[pp] < 0 || blk[pp] >= p.num_blocks) {
+              record_error(p.err, kDevBadBlockId);
+              row = p.num_blocks * kBlockSize;
+            } else {
+              row = blk[pp] * kBlockSize;
+            }
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h) {
+              tma_load_2d_hint(kdst + h * kSub + pp * (kBlockSize * 128), &kmap,
+                               &bars->kv_full[st], kv * D + h * 64, row, policy);
+              tma_load_2d_hint(vdst + h * kSub + pp * (kBlockSize * 128), &vmap,
+                               &bars->kv_full[st], kv * D + h * 64, row, policy);
+            }
+          }
+        }
+        ++g;
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ========================================
+    constexpr uint32_t idS = idesc_f16(kBF16, kRows, kKeys, false);
+    constexpr uint32_t idPV = idesc_f16(kBF16, kRows, D, true);
+    uint32_t g = 0, gs = 0, gp = 0, qi = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it % kItemRing;
+      if (!wait(&bars->item_full[slot], (it / kItemRing) & 1)) break;
+      const int idx = bars->item_idx[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+      if (idx < 0) break;
+      const WorkItem& w = p.tile_items[idx];
+      const int pb = w.page_begin, pe = w.page_end;
+      if (pe <= pb) continue;
+      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
+      if (!wait(&bars->q_full, qi & 1)) break;
+      bool ok = true;
+      const uint32_t g0 = g;  // tile counter at the item's first tile
+      auto pv = [&](int jj) -> bool {
+        const uint32_t st = (g0 + jj) % kStages;  // stage holding tile jj
+        if (!wait(&bars->p_full, gp & 1)) return false;
+        if (jj == 0 && !wait(&bars->o_free, (qi & 1) ^ 1)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vbase = sKV + st * L::kStage + L::kK;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sP + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
+            umma_f16(tmem + kColO, a, b, idPV, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars->o_done);
+          umma_commit(&bars->kv_empty[st]);
+        }
+        __syncwarp();
+        ++gp;
+        return true;
+      };
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t st = g % kStages;
+        if (!wait(&bars->kv_full[st], (g / kStages) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kbase = sKV + st * L::kStage;
+          const uint32_t dS = tmem + kColS + (gs & 1) * kKeys;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sQ + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(kbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
+            umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->s_full[gs & 1]);
+          if (j == nt - 1) umma_commit(&bars->q_empty);
+        }
+        __syncwarp();
+        ++gs;
+        ++g;
+        if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+      }
+      if (!ok || !pv(nt - 1)) break;
+      ++qi;
+    }
+    // every MMA issued by this thread has completed before TMEM is released
+    if (lane == 0) umma_commit(&bars->mma_final);
+    __syncwarp();
+    mbar_wait(&bars->mma_final, 0, 1u << 22);
+  } else {
+    // ============================ softmax + epilogue ================================
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    uint32_t gs = 0, np = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it % kItemRing;
+      if (!wait(&bars->item_full[slot], (it / kItemRing) & 1)) break;
+      const int idx = bars->item_idx[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+      if (idx < 0) break;
+      const WorkItem& w = p.tile_items[idx];
+      const int pb = w.page_begin, pe = w.page_end;
+      if (pe <= pb) continue;
+      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
+      // this thread's query row
+      const bool valid = r < w.nrows;
+      const int qtok = (w.row0 + r) / p.G;  // query index within the sequence
+      const int tok = w.tok0 + qtok;
+      const int head = w.kv * p.G + (w.row0 + r) - qtok * p.G;
+      const int pos = valid ? w.ctx_len - w.n_query + qtok : -1;
+      const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nt; ++j) {
+        const int lim = key_hi - (pb * kBlockSize + j * kKeys);  // visible columns: c <= lim
+        if (!wait(&bars->s_full[gs & 1], (gs >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tS = trow + kColS + (gs & 1) * kKeys;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
+        }
+        const float m_new = fmaxf(m_ref, mx);
+        // P and O are free once the previous tile's PV has completed
+        if (j > 0 && !wait(&bars->o_done, (np - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const bool need = m_ref != -INFINITY && m_new > m_ref + kRescaleLog2;
+        if (m_ref == -INFINITY) m_ref = m_new;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(trow + kColO + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(trow + kColO + c * 32, v);
+          }
+          tmem_st_wait();
+          l *= alpha;
+          if (need) m_ref = m_new;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        uint8_t* prow = smem + L::kOffP + r * 128;
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + c * 32, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = c * 32 + e <= lim ? exp2f(__uint_as_float(v[e]) * sl2 - m_use) : 0.f;
+            const float p1 =
+                c * 32 + e + 1 <= lim ? exp2f(__uint_as_float(v[e + 1]) * sl2 - m_use) : 0.f;
+            l += p0 + p1;
+            pk[e / 2] = pack2<kBF16>(p0, p1);
+          }
+          uint8_t* sub = prow + (c / 2) * kSub;
+          const int cb = 4 * (c & 1);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sub + (((cb + q) ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+        ++gs;
+        ++np;
+      }
+      if (!ok) break;
+      // epilogue: O / l to the output, or to the split partials
+      if (!wait(&bars->o_done, (np - 1) & 1)) break;
+      tc_fence_after();
+      int ns_t = 0;
+      if (valid) ns_t = __ldg(p.tok_ns + tok);
+      const bool write = valid && w.split < ns_t;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(trow + kColO + c * 32, v);
+        tmem_ld_wait();
+        if (!write) continue;
+        if (ns_t == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                (static_cast<int64_t>(tok) * p.H_q + head) * D +
+                                                c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack2<kBF16>(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+            u.y = pack2<kBF16>(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+            u.z = pack2<kBF16>(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+            u.w = pack2<kBF16>(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+            dst[q] = u;
+          }
+        } else {
+          const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
+          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          if (c == 0) p.part_lse[pidx] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int tile_tokens(int G) { return G >= 1 && G <= 16 ? kRows / G : 0; }
+
+template <bool kBF16, int D>
+static cudaError_t launch_tile_t(const AttnParams& p, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
+                                 cudaStream_t stream) {
+  constexpr int smem = TileSmem<D>::kBytes;
+  auto kern = tile_attention_kernel<kBF16, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kThreads, smem, stream>>>(kmap, vmap, qmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
+                                  cudaStream_t stream) {
+  if (p.D == 128)
+    return bf16 ? launch_tile_t<true, 128>(p, kmap, vmap, qmap, num_sms, stream)
+                : launch_tile_t<false, 128>(p, kmap, vmap, qmap, num_sms, stream);
+  return bf16 ? launch_tile_t<true, 64>(p, kmap, vmap, qmap, num_sms, stream)
+              : launch_tile_t<false, 64>(p, kmap, vmap, qmap, num_sms, stream);
+}
+
+}  // namespace ps
