@@ -51,26 +51,32 @@ KERNEL_SOURCES = ["paged_kv_attention_18_gb300/csrc/ps_attention.cu",
 # algorithmic work of a step
 # ------------------------------------------------------------------------------------
 def step_work(wl: W.Workload, st: W.Step) -> dict:
-    """Algorithmic bytes and flops of one step (each context read once, no split partials)."""
+    """Algorithmic bytes and flops of one step (each context read once, no split partials).
+
+    Also split by the kernel that serves each sequence: sequences with more than 16
+    packed rows (n * G) go to the tile kernel, the others to the split kernel."""
     es = 2  # bytes per 16-bit element
     L = st.seq_lens.astype(np.int64)
     n = np.diff(st.query_start_loc).astype(np.int64)
+    G = wl.H_q // wl.H_kv
+    tile = (n * G > 16) & (G <= 16)
     live = n > 0
-    kv = int((L[live] * wl.H_kv * wl.D * es * 2).sum())
-    q = st.T * wl.H_q * wl.D * es
-    out = q
-    bt = int((((L[live] + 15) // 16) * 4).sum())
-    attn = kv + q + out + bt
-    scatter = 2 * (st.T * wl.H_kv * wl.D * es * 2) + st.T * 4  # read k/v, write pool rows, slots
-    # unmasked (query, key) pairs: row at position p sees p + 1 keys
-    pairs = 0
+    kv_b = L * wl.H_kv * wl.D * es * 2
+    qo_b = 2 * n * wl.H_q * wl.D * es
+    bt_b = ((L + 15) // 16) * 4
+    attn_b = np.where(live, kv_b + qo_b + bt_b, 0)
+    pairs = np.zeros(st.B, dtype=np.int64)
     for b in range(st.B):
         if n[b]:
             p = L[b] - n[b] + np.arange(n[b])
-            pairs += int((p + 1).sum())
-    flops = 4 * wl.D * wl.H_q * pairs
-    return {"attn_bytes": attn, "kv_bytes": kv, "step_bytes": attn + scatter, "flops": flops,
-            "tokens": st.T}
+            pairs[b] = int((p + 1).sum())  # row at position p sees p + 1 keys
+    flops_b = 4 * wl.D * wl.H_q * pairs
+    scatter = 2 * (st.T * wl.H_kv * wl.D * es * 2) + st.T * 4  # read k/v, write pool rows, slots
+    return {"attn_bytes": int(attn_b.sum()), "kv_bytes": int(np.where(live, kv_b, 0).sum()),
+            "step_bytes": int(attn_b.sum()) + scatter, "flops": int(flops_b.sum()),
+            "tokens": st.T,
+            "split_bytes": int(attn_b[~tile].sum()), "split_kv_bytes": int(np.where(live & ~tile, kv_b, 0).sum()),
+            "tile_bytes": int(attn_b[tile].sum()), "tile_flops": int(flops_b[tile].sum())}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -189,19 +195,21 @@ def oracle_seconds(wl: W.Workload, st: W.Step, seqs: list[int]) -> tuple[float, 
     t0 = time.perf_counter()
     oracle.attention_step(sst, sub.k_pool, sub.v_pool, sub.scale, sub.dtype, acc=np.float32)
     dt = time.perf_counter() - t0
-    return dt, step_work(sub, sst)["step_bytes"]
+    return dt, step_work(sub, sst)["step_bytes"], sst.T
 
 
-def cpu_baseline(wl, st, budget_s: float = 12.0) -> dict:
+def cpu_baseline(wl, st, unit: str = "GB/s", budget_s: float = 12.0) -> dict:
     """Oracle throughput on the same workload, whole steps repeated for ~budget_s."""
     seqs = list(range(st.B))
-    total_t, total_b, reps = 0.0, 0, 0
+    total_t, total_b, total_tok, reps = 0.0, 0, 0, 0
     while total_t < budget_s and reps < 50:
-        dt, nb = oracle_seconds(wl, st, seqs)
+        dt, nb, nt = oracle_seconds(wl, st, seqs)
         total_t += dt
         total_b += nb
+        total_tok += nt
         reps += 1
-    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    value = total_b / total_t / 1e9 if unit == "GB/s" else total_tok / total_t
+    return {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
             "sample": f"the whole step ({st.B} sequences, {st.T} tokens) x {reps}, "
                       f"{total_t:.1f} s of single-thread CPU"}
 
@@ -212,7 +220,7 @@ def cpu_baseline(wl, st, budget_s: float = 12.0) -> dict:
 def make_workload(name: str, rank: int, batch: int | None = None) -> W.Workload:
     """The named workload; each replica rank draws its own batch (seed + 1000 * rank)."""
     base = {"qwen15b_decode": 2, "tiny_decode": 0, "qwen05b_mixed": 1,
-            "prefix_chunked_prefill": 3, "spec_verify_long": 4}[name]
+            "prefix_chunked_prefill": 3, "spec_verify_long": 4, "long_prefill": 5}[name]
     kw = {"batch": batch} if (batch and name == "qwen15b_decode") else {}
     return W.named(name, seed=base + 1000 * rank, **kw)
 
@@ -342,19 +350,40 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     if binding.device_error() != 0:
         raise RuntimeError("device error word set during the benchmark")
     sec = ms / 1e3
-    value = world * step_bytes * args.steps / sec / 1e9
+    if args.workload == "qwen15b_decode":
+        value, unit = world * step_bytes * args.steps / sec / 1e9, "GB/s"
+    else:
+        value, unit = world * tokens * args.steps / sec, "tokens/s"
 
-    # dominant kernel: the split attention kernel, timed per launch by the library hook
-    split_ms, split_n = prof["split_attention"]
-    split_avg_s = split_ms / 1e3 / max(1, split_n)
-    per_launch_bytes = attn_bytes / len(wl.steps)
-    achieved = per_launch_bytes / split_avg_s / 1e9 if split_n else None
-    traffic = committed_traffic(kv_bytes // len(wl.steps))
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"] if achieved else None,
-                "traffic": traffic, "kernel": "split_attention_kernel",
-                "peak_source": f"{peaks_src} (hbm_gbs)",
-                "kernel_share_of_step": split_ms / (sum(t for t, _ in prof.values()) or 1)}
+    # dominant kernel (largest share of the summed kernel time), timed per launch by the
+    # library hook on the launching stream
+    kernel_ms = {k: t for k, (t, n) in prof.items() if n > 0}
+    dom = max(kernel_ms, key=kernel_ms.get)
+    dom_ms, dom_n = prof[dom]
+    avg_s = dom_ms / 1e3 / max(1, dom_n)
+    nsteps = len(wl.steps)
+    share = dom_ms / (sum(kernel_ms.values()) or 1)
+    if dom == "tile_attention":
+        flops_launch = sum(w["tile_flops"] for w in work) / nsteps
+        peak = peaks["bf16_tflops_sustained"]
+        achieved = flops_launch / avg_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "kernel": "tile_attention_kernel (tcgen05)",
+                    "peak_source": f"{peaks_src} (bf16_tflops_sustained; fp16 runs at the bf16 "
+                                   "rate)",
+                    "kernel_share_of_step": share}
+    else:
+        bytes_launch = sum(w["split_bytes"] for w in work) / nsteps
+        achieved = bytes_launch / avg_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": committed_traffic(sum(w["split_kv_bytes"] for w in work) // nsteps)
+                    if args.workload == "qwen15b_decode" else None,
+                    "kernel": "split_attention_kernel", "peak_source": f"{peaks_src} (hbm_gbs)",
+                    "kernel_share_of_step": share}
+    roofline["per_kernel_ms_per_step"] = {k: t / max(1, prof[k][1]) * nsteps
+                                          for k, t in kernel_ms.items()}
 
     # mixed batch: prefix-cached chunked prefill packed with decodes
     mixed = None
@@ -375,16 +404,18 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 200))
         e2e_s, h2d, d2h = time_e2e(dw, e2e_steps, 3, world, device)
-        e2e = {"value": world * step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+        e2e_value = (world * step_bytes * e2e_steps / e2e_s / 1e9 if unit == "GB/s"
+                     else world * tokens * e2e_steps / e2e_s)
+        e2e = {"value": e2e_value, "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "api": "ps_attention_step_host (pinned host buffers, stream sync per step)"}
 
     if rank != 0:
         return None
-    base = None if args.no_cpu_baseline else cpu_baseline(wl, wl.steps[0])
+    base = None if args.no_cpu_baseline else cpu_baseline(wl, wl.steps[0], unit)
     st0 = wl.steps[0]
     result = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded N(0,1) values, random block permutation)",
@@ -393,6 +424,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
                    "block_size": 16, "num_blocks": wl.num_blocks,
                    "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
                    "flops_per_step": flops,
+                   "tflops": world * flops * args.steps / sec / 1e12,
                    "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step "
                          f"vs {L2_BYTES / 1e6:.0f} MB L2); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -417,29 +449,31 @@ def run_reference(args, rank, world) -> dict | None:
     st = wl.steps[0]
     # a bounded sample per step so that warm-up + steps stay within ~2 minutes
     probe = list(range(min(4, st.B)))
-    probe_t, _ = oracle_seconds(wl, st, probe)
+    probe_t, _, _ = oracle_seconds(wl, st, probe)
     per_seq = probe_t / max(1, len(probe))
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(st.B, per_step_budget / max(per_seq, 1e-5))))
     seqs = list(range(n))
     for _ in range(args.warmup):
         oracle_seconds(wl, st, seqs)
-    total_t, total_b = 0.0, 0
+    total_t, total_b, total_tok = 0.0, 0, 0
     for _ in range(args.steps):
-        dt, nb = oracle_seconds(wl, st, seqs)
+        dt, nb, nt = oracle_seconds(wl, st, seqs)
         total_t += dt
         total_b += nb
-    value = total_b / total_t / 1e9
+        total_tok += nt
+    unit = "GB/s" if args.workload == "qwen15b_decode" else "tokens/s"
+    value = total_b / total_t / 1e9 if unit == "GB/s" else total_tok / total_t
     sample = f"{n} of {st.B} sequences of step 0 per step, single-thread CPU oracle"
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded N(0,1) values, random block permutation)",
             "config": {"workload": wl.name, "description": wl.description},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 

@@ -16,6 +16,7 @@ constexpr int kBlockSize = 16;      // tokens per KV block (page)
 constexpr int kMaxSplits = 32;      // KV splits of one query row, at most
 constexpr int kMinSplitPages = 8;   // pages in one split, at least
 constexpr int kSplitGroupLimit = 4; // only sequences with <= this many 16-row groups split
+constexpr int kTileMinGroups = 1;   // sequences with more 16-row groups than this use tiles
 constexpr int kTileSplitQTiles = 2; // tile-class sequences with <= this many query tiles split
 constexpr int kTilePagesAlign = 8;  // tile-class split sizes are whole 128-key tiles
 
@@ -181,6 +182,13 @@ __device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
+}
+
+// 2^x with the hardware approximation (ex2.approx, flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Two floats -> packed 16-bit pair (low half = first), round to nearest even.

@@ -2,20 +2,23 @@
 // accumulators, K/V pages fed by TMA straight from the paged pool.
 //
 // One work item is up to 128 packed query rows of one sequence and one KV head (whole
-// query tokens x the G query heads that share the KV head), over one split of the
-// context. For each tile of 128 keys (8 pages of 16):
-//     S = Q K^T            tcgen05.mma, A = Q (smem), B = K (smem), D = S in TMEM
-//     P = exp2(S*scale*log2e - m), online row max / sum   (softmax warps, from TMEM)
-//     O += P V             tcgen05.mma, A = P (smem), B = V (smem, MN-major), D = O in TMEM
+// query tokens x the G query heads that share the KV head) over one split of the
+// context. The context is walked in tiles of 128 keys (8 pages of 16):
+//     S = Q K^T          tcgen05.mma: A = Q (smem), B = K (smem)      -> S in TMEM
+//     P = exp2(S*scale*log2e - m) with the online row max / sum (softmax threads)
+//     O += P V           tcgen05.mma: A = P (TMEM), B = V (smem)      -> O in TMEM
 // with the causal rule of the pages (key j visible to the query at position p iff
 // j <= p: PageServe section 01; tinyserve "How it works", stepped causal mask) and
 // grouped-query attention (tinyserve "Highlights" table).
 //
-// Warp roles (192 threads): warp 0 issues TMA and hands out work items, warp 1 owns
-// TMEM and issues the MMAs, warps 2..5 run the softmax and the epilogue with one TMEM
-// lane (one query row) per thread. S is double-buffered in TMEM so the tensor core
-// computes S for tile j+1 while the softmax works on tile j. O is rescaled lazily: only
-// when a row's running max grows by more than 2^8, so most tiles never touch O.
+// Warp roles (384 threads): warp 0 issues TMA and hands out work items; warp 1 owns TMEM
+// and issues the MMAs; warps 4..7 and 8..11 are two softmax groups, one TMEM lane (one
+// query row) per thread. The groups take alternate KV tiles of an item (even / odd), each
+// with its own S and O in TMEM, so one group's exponentials run while the tensor core
+// computes the other group's products. P is written back over S in TMEM and read from
+// there by the PV product. At the end of an item group 0 merges the two partial
+// results (reading group 1's O straight from TMEM) and writes the output. O is rescaled
+// lazily, only when a row's running max grows by more than 2^8.
 #include "ps_common.cuh"
 #include "ps_launch.h"
 #include "ps_tc05.cuh"
@@ -28,36 +31,39 @@ constexpr int kRows = 128;        // query rows per tile (MMA M)
 constexpr int kKeys = 128;        // keys per KV tile (MMA N of S, K of PV) = 8 pages
 constexpr int kPagesPerTile = kKeys / kBlockSize;
 constexpr int kSub = kRows * 128; // bytes of one [128 rows x 64 elements] swizzled sub-tile
-constexpr int kStages = 2;        // K/V tile stages
+constexpr int kStages = 3;        // K/V tile stages
 constexpr int kItemRing = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 2 * kKeys;
+// TMEM columns of softmax group g: S (and P over it) at g*256, O at g*256 + 128
+__host__ __device__ constexpr uint32_t col_s(int g) { return g * 256u; }
+__host__ __device__ constexpr uint32_t col_o(int g) { return g * 256u + 128u; }
 
 template <int D>
 struct TileSmem {
-  static constexpr int kQ = (D / 64) * kSub;        // Q tile
-  static constexpr int kK = (D / 64) * kSub;        // K tile (128 keys)
-  static constexpr int kStage = 2 * kK;             // K + V
-  static constexpr int kP = 2 * kSub;               // P tile (128 rows x 128 keys)
+  static constexpr int kQ = (D / 64) * kSub;  // Q tile
+  static constexpr int kK = (D / 64) * kSub;  // K tile (128 keys)
+  static constexpr int kStage = 2 * kK;       // K + V
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQ;
-  static constexpr int kOffP = kOffKV + kStages * kStage;
-  static constexpr int kOffBar = kOffP + kP;
-  static constexpr int kBytes = kOffBar + 512 + 1024;  // barriers, ring, slack for alignment
+  static constexpr int kOffML = kOffKV + kStages * kStage;  // group 1's row max / sum
+  static constexpr int kOffBar = kOffML + kRows * 8;
+  static constexpr int kBytes = kOffBar + 256 + 1024;  // barriers, ring; alignment slack
 };
+static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
 
 struct TileBars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full, o_done, o_free, mma_final;
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t ml_ready, o_free, mma_final;
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   int item_idx[kItemRing];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(TileBars) <= 256, "barrier block");
 
 }  // namespace
 
@@ -68,17 +74,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap qmap, const AttnParams p) {
   using L = TileSmem<D>;
   constexpr int kHalves = D / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
+  if (n_items == 0) return;  // nothing planned for this kernel (uniform across the grid)
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   TileBars* bars = reinterpret_cast<TileBars*>(smem + L::kOffBar);
+  float2* ml = reinterpret_cast<float2*>(smem + L::kOffML);
   const uint32_t sQ = smem_u32(smem + L::kOffQ);
   const uint32_t sKV = smem_u32(smem + L::kOffKV);
-  const uint32_t sP = smem_u32(smem + L::kOffP);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
-  if (n_items == 0) return;  // nothing planned for this kernel (uniform across the grid)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -86,15 +93,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->o_done, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->p_full[g], 4);
+      mbar_init(&bars->o_done[g], 1);
+    }
+    mbar_init(&bars->ml_ready, 4);
     mbar_init(&bars->o_free, 4);
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 5);
+      mbar_init(&bars->item_empty[s], 9);  // the MMA warp and the 8 softmax warps
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -119,6 +128,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     return ok;
+  };
+  // next work item from the ring (consumer side); -1 at the end or on a time-out
+  auto next_item = [&](int it) -> int {
+    const int slot = it % kItemRing;
+    if (!wait(&bars->item_full[slot], (it / kItemRing) & 1)) return -1;
+    const int idx = bars->item_idx[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    return idx;
   };
 
   if (warp == 0) {
@@ -160,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
       int bt_base = -1000, bt_reg = -1;
       bool ok = true;
-      for (int j = 0; j < nt && ok; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const int first = pb + j * kPagesPerTile;
         if (first - bt_base + kPagesPerTile > 32) {
           bt_base = first;
@@ -204,82 +222,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ MMA issuer ========================================
     constexpr uint32_t idS = idesc_f16(kBF16, kRows, kKeys, false);
     constexpr uint32_t idPV = idesc_f16(kBF16, kRows, D, true);
-    uint32_t g = 0, gs = 0, gp = 0, qi = 0;
-    for (int it = 0;; ++it) {
-      const int slot = it % kItemRing;
-      if (!wait(&bars->item_full[slot], (it / kItemRing) & 1)) break;
-      const int idx = bars->item_idx[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    uint32_t g = 0, qi = 0, pc[2] = {0, 0};
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int idx = next_item(it);
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       if (!wait(&bars->q_full, qi & 1)) break;
-      bool ok = true;
-      const uint32_t g0 = g;  // tile counter at the item's first tile
-      auto pv = [&](int jj) -> bool {
-        const uint32_t st = (g0 + jj) % kStages;  // stage holding tile jj
-        if (!wait(&bars->p_full, gp & 1)) return false;
-        if (jj == 0 && !wait(&bars->o_free, (qi & 1) ^ 1)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t vbase = sKV + st * L::kStage + L::kK;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sP + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
-            umma_f16(tmem + kColO, a, b, idPV, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bars->o_done);
-          umma_commit(&bars->kv_empty[st]);
-        }
-        __syncwarp();
-        ++gp;
-        return true;
-      };
-      for (int j = 0; j < nt; ++j) {
-        const uint32_t st = g % kStages;
-        if (!wait(&bars->kv_full[st], (g / kStages) & 1)) { ok = false; break; }
+      const uint32_t g0 = g;
+      // S of tile j into the TMEM of group j & 1
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t st = (g0 + j) % kStages;
+        if (!wait(&bars->kv_full[st], ((g0 + j) / kStages) & 1)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t kbase = sKV + st * L::kStage;
-          const uint32_t dS = tmem + kColS + (gs & 1) * kKeys;
+          const uint32_t dS = tmem + col_s(j & 1);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t a = sdesc_sw128(sQ + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
             const uint64_t b = sdesc_sw128(kbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
             umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&bars->s_full[gs & 1]);
-          if (j == nt - 1) umma_commit(&bars->q_empty);
+          umma_commit(&bars->s_full[j & 1]);
+          if (j == nt - 1) umma_commit(&bars->q_empty);  // Q is no longer needed
         }
         __syncwarp();
-        ++gs;
-        ++g;
-        if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+        return true;
+      };
+      if (!issue_s(0) || (nt > 1 && !issue_s(1))) break;
+      for (int j = 0; j < nt; ++j) {
+        const int grp = j & 1;
+        if (!wait(&bars->p_full[grp], pc[grp] & 1)) { ok = false; break; }
+        ++pc[grp];
+        // the previous item's epilogue has read both groups' O
+        if (j == 0 && !wait(&bars->o_free, (qi & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t st = (g0 + j) % kStages;
+        if (lane == 0) {
+          const uint32_t vbase = sKV + st * L::kStage + L::kK;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t b = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
+            umma_f16_ts(tmem + col_o(grp), tmem + col_s(grp) + kk * 8, b, idPV,
+                        (j >= 2 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars->kv_empty[st]);
+        }
+        __syncwarp();
+        // the next S of this group overwrites its P: issued after this PV (in order)
+        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
       }
-      if (!ok || !pv(nt - 1)) break;
+      if (!ok) break;
+      if (lane == 0) {
+        umma_commit(&bars->o_done[0]);
+        umma_commit(&bars->o_done[1]);
+      }
+      __syncwarp();
+      g += nt;
       ++qi;
     }
     // every MMA issued by this thread has completed before TMEM is released
     if (lane == 0) umma_commit(&bars->mma_final);
     __syncwarp();
     mbar_wait(&bars->mma_final, 0, 1u << 22);
-  } else {
-    // ============================ softmax + epilogue ================================
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+  } else if (warp >= 4) {
+    // ============================ softmax groups + epilogue =========================
+    const int grp = (warp - 4) >> 2;   // 0: even KV tiles, 1: odd KV tiles
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = trow + col_s(grp), tO = trow + col_o(grp);
     const float sl2 = p.scale_log2;
-    uint32_t gs = 0, np = 0;
-    for (int it = 0;; ++it) {
-      const int slot = it % kItemRing;
-      if (!wait(&bars->item_full[slot], (it / kItemRing) & 1)) break;
-      const int idx = bars->item_idx[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+    uint32_t sc = 0, qi = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int idx = next_item(it);
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
@@ -293,12 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = valid ? w.ctx_len - w.n_query + qtok : -1;
       const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
       float m_ref = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < nt; ++j) {
+      for (int j = grp; j < nt; j += 2) {
         const int lim = key_hi - (pb * kBlockSize + j * kKeys);  // visible columns: c <= lim
-        if (!wait(&bars->s_full[gs & 1], (gs >> 1) & 1)) { ok = false; break; }
+        if (!wait(&bars->s_full[grp], sc & 1)) { ok = false; break; }
+        ++sc;
         tc_fence_after();
-        const uint32_t tS = trow + kColS + (gs & 1) * kKeys;
+        // pass 1: row max over the visible keys
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kKeys / 32; ++c) {
@@ -307,31 +328,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
+            if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
         }
-        const float m_new = fmaxf(m_ref, mx);
-        // P and O are free once the previous tile's PV has completed
-        if (j > 0 && !wait(&bars->o_done, (np - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
+        const float m_new = mx == -INFINITY ? m_ref : fmaxf(m_ref, mx * sl2);
+        // the previous PV of this group has completed (S was issued after it), so O is
+        // stable and may be rescaled here
         const bool need = m_ref != -INFINITY && m_new > m_ref + kRescaleLog2;
         if (m_ref == -INFINITY) m_ref = m_new;
         if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
+          const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(trow + kColO + c * 32, v);
+            tmem_ld32(tO + c * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st32(trow + kColO + c * 32, v);
+            tmem_st32(tO + c * 32, v);
           }
           tmem_st_wait();
           l *= alpha;
           if (need) m_ref = m_new;
         }
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        uint8_t* prow = smem + L::kOffP + r * 128;
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        // pass 2: P = 2^(s*scale*log2e - m) as 16-bit pairs written over S (chunk c of P
+        // lands on columns 16c..16c+15, which pass 2 has already read)
 #pragma unroll
         for (int c = 0; c < kKeys / 32; ++c) {
           uint32_t v[32];
@@ -340,66 +361,81 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = c * 32 + e <= lim ? exp2f(__uint_as_float(v[e]) * sl2 - m_use) : 0.f;
+            const float p0 =
+                c * 32 + e <= lim ? fast_exp2(fmaf(__uint_as_float(v[e]), sl2, neg_m)) : 0.f;
             const float p1 =
-                c * 32 + e + 1 <= lim ? exp2f(__uint_as_float(v[e + 1]) * sl2 - m_use) : 0.f;
+                c * 32 + e + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[e + 1]), sl2, neg_m))
+                                      : 0.f;
             l += p0 + p1;
             pk[e / 2] = pack2<kBF16>(p0, p1);
           }
-          uint8_t* sub = prow + (c / 2) * kSub;
-          const int cb = 4 * (c & 1);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(sub + (((cb + q) ^ (r & 7)) << 4)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          tmem_st16(tS + c * 16, pk);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full);
-        ++gs;
-        ++np;
+        if (lane == 0) mbar_arrive(&bars->p_full[grp]);
       }
       if (!ok) break;
-      // epilogue: O / l to the output, or to the split partials
-      if (!wait(&bars->o_done, (np - 1) & 1)) break;
+      // epilogue: wait for this item's last products
+      if (!wait(&bars->o_done[grp], qi & 1)) break;
       tc_fence_after();
-      int ns_t = 0;
-      if (valid) ns_t = __ldg(p.tok_ns + tok);
-      const bool write = valid && w.split < ns_t;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (grp == 1) {
+        ml[r] = make_float2(m_ref, l);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ml_ready);
+      } else {
+        if (!wait(&bars->ml_ready, qi & 1)) break;
+        const float2 other = ml[r];
+        const float M = fmaxf(m_ref, other.x);
+        const float a = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - M);
+        const float b = other.x == -INFINITY ? 0.f : fast_exp2(other.x - M);
+        const float lt = a * l + b * other.y;
+        int ns_t = 0;
+        if (valid) ns_t = __ldg(p.tok_ns + tok);
+        const bool write = valid && w.split < ns_t && lt > 0.f;
+        const float inv = write ? 1.f / lt : 0.f;
+        const float ca = a * inv, cb = b * inv;
+        const bool any_b = __any_sync(0xffffffffu, b != 0.f);
+        const uint32_t tO1 = trow + col_o(1);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(trow + kColO + c * 32, v);
-        tmem_ld_wait();
-        if (!write) continue;
-        if (ns_t == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                (static_cast<int64_t>(tok) * p.H_q + head) * D +
-                                                c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32], u[32];
+          tmem_ld32(tO + c * 32, v);
+          if (any_b) tmem_ld32(tO1 + c * 32, u);
+          tmem_ld_wait();
+          if (!write) continue;
+          float* o = reinterpret_cast<float*>(v);  // merged row, in place
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack2<kBF16>(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-            u.y = pack2<kBF16>(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-            u.z = pack2<kBF16>(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-            u.w = pack2<kBF16>(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-            dst[q] = u;
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(v[e]) * ca;
+            if (any_b && b != 0.f) x = fmaf(__uint_as_float(u[e]), cb, x);
+            o[e] = x;
           }
-        } else {
-          const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
+          if (ns_t == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                  (static_cast<int64_t>(tok) * p.H_q + head) * D +
+                                                  c * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-          if (c == 0) p.part_lse[pidx] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack2<kBF16>(o[8 * q + 0], o[8 * q + 1]),
+                                  pack2<kBF16>(o[8 * q + 2], o[8 * q + 3]),
+                                  pack2<kBF16>(o[8 * q + 4], o[8 * q + 5]),
+                                  pack2<kBF16>(o[8 * q + 6], o[8 * q + 7]));
+          } else {
+            const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
+            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            if (c == 0) p.part_lse[pidx] = M + __log2f(lt);
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_free);
+      ++qi;
     }
   }
   tc_fence_before();

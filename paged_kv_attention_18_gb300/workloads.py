@@ -305,12 +305,24 @@ def spec_verify_long(seed: int = 4, n_seq: int = 128, lo: int = 1024, hi: int = 
                     f"{k_plus_1} verify tokens; 12/2 heads, D 128, bf16")
 
 
+def long_prefill(seed: int = 5, n_seq: int = 4, prompt: int = 4096) -> Workload:
+    """Whole prompts prefilled in one step (no cached prefix): a tensor-core stress case."""
+    rng = np.random.default_rng(seed)
+    return build_workload(
+        f"qwen2.5-1.5b_prefill_{n_seq}x{prompt}", seed=seed, rng=rng, dtype="bf16", H_q=12,
+        H_kv=2, D=128, capacities=[prompt] * n_seq,
+        steps=[[(i, prompt, prompt) for i in range(n_seq)]],
+        description=f"{n_seq} prompts of {prompt} tokens prefilled at once, causal; 12/2 "
+                    "heads, D 128, bf16")
+
+
 NAMED = {
     "tiny_decode": tiny_decode,
     "qwen05b_mixed": qwen05b_mixed,
     "qwen15b_decode": qwen15b_decode,
     "prefix_chunked_prefill": prefix_chunked_prefill,
     "spec_verify_long": spec_verify_long,
+    "long_prefill": long_prefill,
 }
 
 
