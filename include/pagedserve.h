@@ -214,6 +214,13 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
  */
 int ps_get_device_error(int* code);
 
+/*
+ * ps_last_error_message -- after a call returned PS_ERR_CUDA, the step that failed and
+ * CUDA's message, for the calling host thread ("" if none). The string stays valid until
+ * the next failing call on the same thread.
+ */
+const char* ps_last_error_message(void);
+
 /* Human-readable name of a ps_status value. The string is static. */
 const char* ps_status_string(int status);
 

@@ -35,6 +35,7 @@ SIGNATURES = {
                                        _p]),
     "ps_get_device_error": (c_int, [_p]),
     "ps_status_string": (c_char_p, [c_int]),
+    "ps_last_error_message": (c_char_p, []),
     "ps_profile_begin": (c_int, [c_int]),
     "ps_profile_end": (c_int, []),
     "ps_profile_read": (c_int, [c_int, _p, _p]),

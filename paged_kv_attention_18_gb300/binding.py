@@ -33,6 +33,8 @@ def lib():
 def _check(rc: int, what: str) -> None:
     if rc != 0:
         msg = lib().ps_status_string(rc).decode()
+        if rc == -5:
+            msg += f" [{lib().ps_last_error_message().decode()}]"
         raise PagedServeError(f"{what} failed: {msg} ({rc})")
 
 

@@ -2,6 +2,8 @@
 // TMA descriptors, kernel launches and the benchmark timing hook.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+
 #include <mutex>
 #include <vector>
 
@@ -85,7 +87,18 @@ struct Timed {
   }
 };
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? PS_OK : PS_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+// PS_ERR_CUDA, remembering which step failed and CUDA's message for ps_last_error_message.
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+           static_cast<int>(e));
+  return PS_ERR_CUDA;
+}
+
+int cuda_status(cudaError_t e, const char* where = "kernel launch") {
+  return e == cudaSuccess ? PS_OK : cuda_fail(e, where);
+}
 
 int make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, int D, bool bf16) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H_kv) * D,
@@ -98,7 +111,9 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int H_kv, 
       const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PS_OK : PS_ERR_CUDA;
+  if (r == CUDA_SUCCESS) return PS_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "pool tensor map: CUresult %d", static_cast<int>(r));
+  return PS_ERR_CUDA;
 }
 
 // q [T, H_q, D] as a 3-D tensor (D, H_q, T) with boxes of 64 elements x G heads x tpt
@@ -115,7 +130,9 @@ int make_q_map(CUtensorMap* map, const void* q, int T, int H_q, int D, int G, in
       const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PS_OK : PS_ERR_CUDA;
+  if (r == CUDA_SUCCESS) return PS_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "query tensor map: CUresult %d", static_cast<int>(r));
+  return PS_ERR_CUDA;
 }
 
 int check_shapes(int H_q, int H_kv, int D, int dtype) {
@@ -220,23 +237,25 @@ int run_attention(const AttnParams& p0, const void* k_pool, const void* v_pool, 
   if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if (p.tpt > 0 && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
   const int concurrency = attention_ctas(p.D, num_sms) * attention_warps(p.D);
+  cudaError_t e;
   {
     Timed tm(2, s);
-    if (launch_plan(p, concurrency, num_sms, s) != cudaSuccess) return PS_ERR_CUDA;
+    if ((e = launch_plan(p, concurrency, num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "plan kernel");
   }
   {
     Timed tm(3, s);
-    if (launch_split_attention(p, bf16, kmap, vmap, num_sms, s) != cudaSuccess)
-      return PS_ERR_CUDA;
+    if ((e = launch_split_attention(p, bf16, kmap, vmap, num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "split attention kernel");
   }
   if (p.tpt > 0) {
     Timed tm(5, s);
-    if (launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s) != cudaSuccess)
-      return PS_ERR_CUDA;
+    if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "tile attention kernel");
   }
   {
     Timed tm(4, s);
-    if (launch_combine(p, bf16, s) != cudaSuccess) return PS_ERR_CUDA;
+    if ((e = launch_combine(p, bf16, s)) != cudaSuccess) return cuda_fail(e, "combine kernel");
   }
   return PS_OK;
 }
@@ -287,7 +306,8 @@ int ps_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq, const i
   Timed tm(0, s);
   return cuda_status(ps::launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens,
                                              query_start_loc, B, T, num_blocks, slot_mapping,
-                                             ds->err, s));
+                                             ds->err, s),
+                     "slot mapping kernel");
 }
 
 int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, void* k_pool,
@@ -306,7 +326,8 @@ int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Timed tm(1, s);
   return cuda_status(ps::launch_reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, T, H_kv, D,
-                                                  num_blocks, ds->err, ds->num_sms, s));
+                                                  num_blocks, ds->err, ds->num_sms, s),
+                     "KV scatter kernel");
 }
 
 size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
@@ -484,6 +505,8 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
     return PS_ERR_CUDA;
   return PS_OK;
 }
+
+const char* ps_last_error_message(void) { return g_last_error; }
 
 int ps_get_device_error(int* code) {
   if (!code) return PS_ERR_ARG;

@@ -546,21 +546,21 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
       const float m_new = fmaxf(m_run[r], mx[r]);
       m_use[r] = m_new == -INFINITY ? 0.f : m_new;
-      alpha[r] = exp2f(m_run[r] - m_use[r]);
+      alpha[r] = fast_exp2(m_run[r] - m_use[r]);
       m_run[r] = m_new;
     }
-    float psum[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1;
-        const float pe = exp2f(s[nt][e] - m_use[r]);
-        s[nt][e] = pe;
-        psum[r] += pe;
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + psum[r];
+      for (int e = 0; e < 4; ++e) s[nt][e] = fast_exp2(s[nt][e] - m_use[e >> 1]);
+    uint32_t pa[4];
+    pa[0] = pack2<kBF16>(s[0][0], s[0][1]);
+    pa[1] = pack2<kBF16>(s[0][2], s[0][3]);
+    pa[2] = pack2<kBF16>(s[1][0], s[1][1]);
+    pa[3] = pack2<kBF16>(s[1][2], s[1][3]);
+    // the row sums use the rounded P the tensor core multiplies with
+    l_run[0] = l_run[0] * alpha[0] + pair_sum<kBF16>(pa[0]) + pair_sum<kBF16>(pa[2]);
+    l_run[1] = l_run[1] * alpha[1] + pair_sum<kBF16>(pa[1]) + pair_sum<kBF16>(pa[3]);
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
       o[j][0] *= alpha[0];
@@ -568,11 +568,6 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
       o[j][2] *= alpha[1];
       o[j][3] *= alpha[1];
     }
-    uint32_t pa[4];
-    pa[0] = pack2<kBF16>(s[0][0], s[0][1]);
-    pa[1] = pack2<kBF16>(s[0][2], s[0][3]);
-    pa[2] = pack2<kBF16>(s[1][0], s[1][1]);
-    pa[3] = pack2<kBF16>(s[1][2], s[1][3]);
     // O += P V: V page is [key][d], read transposed
     {
       const int mi = lane >> 3, rr = lane & 7;

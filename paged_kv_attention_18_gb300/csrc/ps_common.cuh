@@ -191,6 +191,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Two floats -> packed 16-bit pair (low half = first), round to nearest even.
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -200,6 +207,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Sum of the two 16-bit values of a packed pair, in fp32.
+template <bool kBF16>
+__device__ __forceinline__ float pair_sum(uint32_t packed) {
+  if constexpr (kBF16) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&packed));
+    return f.x + f.y;
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&packed));
+    return f.x + f.y;
+  }
+}
+
+// Both 16-bit halves of a packed pair multiplied by a, rounded back.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t packed, float a) {
+  if constexpr (kBF16) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&packed);
+    const float2 f = __bfloat1622float2(v);
+    return pack2<true>(f.x * a, f.y * a);
+  } else {
+    const __half2 v = *reinterpret_cast<const __half2*>(&packed);
+    const float2 f = __half22float2(v);
+    return pack2<false>(f.x * a, f.y * a);
   }
 }
 

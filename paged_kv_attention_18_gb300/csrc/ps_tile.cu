@@ -12,8 +12,9 @@
 // grouped-query attention (tinyserve "Highlights" table).
 //
 // Warp roles (384 threads): warp 0 issues TMA and hands out work items; warp 1 owns TMEM
-// and issues the MMAs; warps 4..7 and 8..11 are two softmax groups, one TMEM lane (one
-// query row) per thread. The groups take alternate KV tiles of an item (even / odd), each
+// and issues the MMAs (warps 2, 3 idle); warps 4..7 and 8..11 are two softmax groups, one
+// TMEM lane (one query row) per thread (a warp reaches the 32 TMEM lanes of its warp index
+// mod 4). The groups take alternate KV tiles of an item (even / odd), each
 // with its own S and O in TMEM, so one group's exponentials run while the tensor core
 // computes the other group's products. P is written back over S in TMEM and read from
 // there by the PV product. At the end of an item group 0 merges the two partial
@@ -35,6 +36,10 @@ constexpr int kStages = 3;        // K/V tile stages
 constexpr int kItemRing = 4;
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
+// A larger jump inside a tile moves the reference at once; below it P can reach 2^kMove,
+// which must stay finite in the 16-bit type (fp16 tops out near 2^16, bf16 near 2^128).
+template <bool kBF16>
+constexpr float kMoveLog2 = kBF16 ? 64.f : 15.f;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of softmax group g: S (and P over it) at g*256, O at g*256 + 128
 __host__ __device__ constexpr uint32_t col_s(int g) { return g * 256u; }
@@ -313,30 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = w.kv * p.G + (w.row0 + r) - qtok * p.G;
       const int pos = valid ? w.ctx_len - w.n_query + qtok : -1;
       const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
-      float m_ref = -INFINITY, l = 0.f;
+      // m_ref: the reference max (log2 units) that P, O and l are currently taken against;
+      // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
+      float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
+      bool started = false;  // this group has written O for this item
       for (int j = grp; j < nt; j += 2) {
         const int lim = key_hi - (pb * kBlockSize + j * kKeys);  // visible columns: c <= lim
         if (!wait(&bars->s_full[grp], sc & 1)) { ok = false; break; }
         ++sc;
         tc_fence_after();
-        // pass 1: row max over the visible keys
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
-        }
-        const float m_new = mx == -INFINITY ? m_ref : fmaxf(m_ref, mx * sl2);
-        // the previous PV of this group has completed (S was issued after it), so O is
-        // stable and may be rescaled here
-        const bool need = m_ref != -INFINITY && m_new > m_ref + kRescaleLog2;
-        if (m_ref == -INFINITY) m_ref = m_new;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
+        // This group's previous PV has completed (this S was issued after it): O is stable.
+        auto rescale_o = [&](float alpha) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
@@ -347,30 +339,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c * 32, v);
           }
           tmem_st_wait();
+        };
+        if (__any_sync(0xffffffffu, m_next > m_ref)) {
+          const bool need = m_next > m_ref;
+          const float alpha = need ? fast_exp2(m_ref - m_next) : 1.f;
+          if (started) rescale_o(alpha);
           l *= alpha;
-          if (need) m_ref = m_new;
+          if (need) m_ref = m_next;
         }
-        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-        // pass 2: P = 2^(s*scale*log2e - m) as 16-bit pairs written over S (chunk c of P
-        // lands on columns 16c..16c+15, which pass 2 has already read)
+        // P = 2^(s*scale*log2e - m_ref) as 16-bit pairs written over S; half h of P lands
+        // on columns 32h..32h+31, which the loads of halves <= h have already read
+        const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
+        float m_tile = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + c * 32, v);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[64];
+          tmem_ld32(tS + 64 * h, v);
+          tmem_ld32(tS + 64 * h + 32, v + 32);
           tmem_ld_wait();
-          uint32_t pk[16];
+          if (!full) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 =
-                c * 32 + e <= lim ? fast_exp2(fmaf(__uint_as_float(v[e]), sl2, neg_m)) : 0.f;
-            const float p1 =
-                c * 32 + e + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[e + 1]), sl2, neg_m))
-                                      : 0.f;
-            l += p0 + p1;
-            pk[e / 2] = pack2<kBF16>(p0, p1);
+            for (int e = 0; e < 64; ++e)
+              if (64 * h + e > lim) v[e] = __float_as_uint(-INFINITY);
           }
-          tmem_st16(tS + c * 16, pk);
+          // four independent max chains
+          float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int e = 0; e < 64; e += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mq[k] = fmax3(mq[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
+          const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+          const float m_half = mx == -INFINITY ? -INFINITY : mx * sl2;
+          m_tile = fmaxf(m_tile, m_half);
+          // no reference yet, or a jump P could overflow on: move the reference now,
+          // rescaling what is already taken against the old one
+          const bool move = m_half > m_ref + kMoveLog2<kBF16> ||
+                            (m_ref == -INFINITY && m_half != -INFINITY);
+          if (__any_sync(0xffffffffu, move)) {
+            const float alpha = move && m_ref != -INFINITY ? fast_exp2(m_ref - m_half) : 1.f;
+            if (started) rescale_o(alpha);
+            l *= alpha;
+            if (h == 1) {  // the half of P already written: columns 0..31
+              uint32_t q[32];
+              tmem_ld32(tS, q);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) q[e] = scale_pair<kBF16>(q[e], alpha);
+              tmem_st32(tS, q);
+              tmem_st_wait();
+            }
+            if (move) m_ref = m_half;
+          }
+          const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+          uint32_t pk[32];
+          float lq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(v[e]), sl2, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), sl2, neg_m));
+            pk[e / 2] = pack2<kBF16>(p0, p1);
+            lq[(e / 2) & 3] += pair_sum<kBF16>(pk[e / 2]);  // the row sum uses the P the MMA sees
+          }
+          l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+          tmem_st16(tS + 32 * h, pk);
+          tmem_st16(tS + 32 * h + 16, pk + 16);
         }
+        m_next = m_tile > m_ref + kRescaleLog2 ? m_tile : m_ref;
+        started = true;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

@@ -53,12 +53,22 @@ def run_step(wl, st, pools: DevicePools, workspace=None, separate_calls=False):
     return out, slots
 
 
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Half a unit in the last place of |x| in the output type (the output rounding)."""
+    mant = {"f16": 10, "bf16": 7}[dtype]
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -14)))
+    return 0.5 * 2.0 ** (e - mant)
+
+
 def check_workload(wl, rows_for_step=None, check_pool=True, separate_calls=False,
-                   workspace=None):
+                   workspace=None, output_rounding_slack=False):
     """Run every step of a workload on GPU and oracle; compare slots, pools and outputs.
 
     rows_for_step(step_index, step) -> list of packed rows to compare, or None for all.
-    Returns the largest max-abs error seen.
+    With output_rounding_slack the bound per element is the tolerance plus half an ulp of
+    the reference value in the output type: an output of |o| >= 2 in bf16 is rounded by up
+    to 2^-8, so for the short or sharply peaked contexts some tests build, the rounding of
+    the result alone can approach the plain bound. Returns the largest max-abs error seen.
     """
     pools = DevicePools(wl)
     kref, vref = wl.k_pool, wl.v_pool
@@ -80,6 +90,8 @@ def check_workload(wl, rows_for_step=None, check_pool=True, separate_calls=False
         sel = slice(None) if rows is None else np.asarray(rows, dtype=np.int64)
         err = np.abs(got[sel] - ref[sel])
         assert np.isfinite(got[sel]).all()
+        if output_rounding_slack:
+            err = err - half_ulp(ref[sel], wl.dtype)
         e = float(err.max()) if err.size else 0.0
         report = os.environ.get("PS_PARITY_REPORT")
         if report:

@@ -138,7 +138,7 @@ def test_full_block_table_and_block_boundaries():
     # longest uses every entry of its block table
     seqs = [(16, 1), (15, 1), (17, 1), (32, 16), (48, 17), (64, 64), (1, 1), (160, 2)]
     check_workload(W.simple_workload("edge", seed=9, dtype="bf16", H_q=12, H_kv=2, D=128,
-                                     seqs=seqs, free_fraction=0.0))
+                                     seqs=seqs, free_fraction=0.0), output_rounding_slack=True)
 
 
 def test_negative_slots_are_skipped():
@@ -193,3 +193,20 @@ def test_two_calls_share_a_workspace():
                                 workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, b)  # deterministic: same plan, same order of accumulation
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_large_score_jumps_mid_context(dtype):
+    # Keys of a few pool blocks are scaled up so the running max jumps by far more than
+    # 2^8 (and often 2^64) in the middle of KV tiles: every rescale path of the kernels
+    # must keep the result equal to the plain softmax.
+    seqs = [(700, 300), (900, 5), (1500, 1), (400, 128), (2100, 40)]
+    wl = W.simple_workload("jumps", seed=31, dtype=dtype, H_q=12, H_kv=2, D=128, seqs=seqs)
+    vals = oracle.decode_bits(wl.k_pool, dtype)
+    rng = np.random.default_rng(32)
+    hot = rng.choice(wl.num_blocks, size=wl.num_blocks // 6, replace=False)
+    vals[hot] *= 40.0
+    wl.k_pool = W.round_to_bits(vals.astype(np.float32), dtype)
+    # sharply peaked rows return nearly one V row, |o| up to ~4.5: bf16 output rounding
+    # alone reaches 2^-7 there, so the bound carries half an output ulp
+    check_workload(wl, output_rounding_slack=True)
