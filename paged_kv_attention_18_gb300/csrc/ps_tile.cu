@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&vmap);
       tma_prefetch_desc(&qmap);
     }
-    const uint64_t policy = l2_policy_evict_first();
     uint32_t g = 0, qi = 0;
     for (int it = 0;; ++it) {
       const int slot = it % kItemRing;
@@ -191,33 +190,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = g % kStages;
         if (!wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1)) { ok = false; break; }
-        int blk[kPagesPerTile];
-#pragma unroll
-        for (int pp = 0; pp < kPagesPerTile; ++pp)
-          blk[pp] = __shfl_sync(0xffffffffu, bt_reg, first - bt_base + pp);
-        if (lane == 0) {
-          uint8_t* kdst = smem + L::kOffKV + st * L::kStage;
-          uint8_t* vdst = kdst + L::kK;
-          mbar_arrive_expect_tx(&bars->kv_full[st], L::kStage);
-#pragma unroll
-          for (int pp = 0; pp < kPagesPerTile; ++pp) {
-            int row;
-            if (first + pp >= pe) {
-              row = p.num_blocks * kBlockSize;  // past the pool: zero fill, no HBM read
-            } else if (blk[pp] < 0 || blk[pp] >= p.num_blocks) {
-              record_error(p.err, kDevBadBlockId);
-              row = p.num_blocks * kBlockSize;
-            } else {
-              row = blk[pp] * kBlockSize;
-            }
-#pragma unroll
-            for (int h = 0; h < kHalves; ++h) {
-              tma_load_2d_hint(kdst + h * kSub + pp * (kBlockSize * 128), &kmap,
-                               &bars->kv_full[st], kv * D + h * 64, row, policy);
-              tma_load_2d_hint(vdst + h * kSub + pp * (kBlockSize * 128), &vmap,
-                               &bars->kv_full[st], kv * D + h * 64, row, policy);
-            }
+        // one lane per copy: lane = page * 4 + tensor * 2 + half (K/V, 64-element half)
+        constexpr int kCopies = kPagesPerTile * 2 * kHalves;
+        const int pp = lane / (2 * kHalves), tensor = (lane / kHalves) & 1, h = lane % kHalves;
+        const int blk = __shfl_sync(0xffffffffu, bt_reg, (first - bt_base + pp) & 31);
+        uint8_t* kdst = smem + L::kOffKV + st * L::kStage;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[st], L::kStage);
+        __syncwarp();
+        if (lane < kCopies) {
+          int row;
+          if (first + pp >= pe) {
+            row = p.num_blocks * kBlockSize;  // past the pool: zero fill, no HBM read
+          } else if (blk < 0 || blk >= p.num_blocks) {
+            record_error(p.err, kDevBadBlockId);
+            row = p.num_blocks * kBlockSize;
+          } else {
+            row = blk * kBlockSize;
           }
+          tma_load_2d(kdst + tensor * L::kK + h * kSub + pp * (kBlockSize * 128),
+                      tensor ? &vmap : &kmap, &bars->kv_full[st], kv * D + h * 64, row);
         }
         ++g;
       }
