@@ -172,9 +172,11 @@ int ps_paged_attention_noalloc(const void* q, const void* k_pool, const void* v_
                                void* out, int dtype, void* stream);
 
 /*
- * ps_attention_step -- the whole step in one call: ps_slot_mapping, ps_reshape_and_cache,
- * then ps_paged_attention, on one stream. k, v are the step's new tokens [T, H_kv, D];
- * slot_mapping is caller-provided device scratch of T int32 (written). Other arguments as
+ * ps_attention_step -- the whole step in one call, with the results of ps_slot_mapping,
+ * ps_reshape_and_cache and then ps_paged_attention, on one stream (the slot mapping is
+ * computed by the attention planner and the kernels are chained with programmatic
+ * dependent launch). k, v are the step's new tokens [T, H_kv, D]; slot_mapping is
+ * caller-provided device memory of T int32 (written with the slots). Other arguments as
  * above.
  */
 int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,

@@ -224,8 +224,8 @@ bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink) {
   return true;
 }
 
-int run_attention(const AttnParams& p0, const void* k_pool, const void* v_pool, bool bf16,
-                  cudaStream_t s) {
+int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, cudaStream_t s,
+                  const ScatterArgs* scatter) {
   AttnParams p = p0;
   int num_sms = 0;
   int* err = nullptr;
@@ -243,19 +243,26 @@ int run_attention(const AttnParams& p0, const void* k_pool, const void* v_pool, 
     if ((e = launch_plan(p, concurrency, num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "plan kernel");
   }
+  if (scatter) {
+    Timed tm(1, s);
+    if ((e = launch_reshape_and_cache(scatter->k, scatter->v, p.slots, k_pool, v_pool, p.T,
+                                      p.H_kv, p.D, p.num_blocks, err, num_sms, s, true)) !=
+        cudaSuccess)
+      return cuda_fail(e, "KV scatter kernel");
+  }
   {
     Timed tm(3, s);
-    if ((e = launch_split_attention(p, bf16, kmap, vmap, num_sms, s)) != cudaSuccess)
+    if ((e = launch_split_attention(p, bf16, kmap, vmap, num_sms, s, true)) != cudaSuccess)
       return cuda_fail(e, "split attention kernel");
   }
   if (p.tpt > 0) {
     Timed tm(5, s);
-    if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s)) != cudaSuccess)
+    if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s, true)) != cudaSuccess)
       return cuda_fail(e, "tile attention kernel");
   }
   {
     Timed tm(4, s);
-    if ((e = launch_combine(p, bf16, s)) != cudaSuccess) return cuda_fail(e, "combine kernel");
+    if ((e = launch_combine(p, bf16, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
   }
   return PS_OK;
 }
@@ -394,7 +401,8 @@ int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
   p.tpt = ps::tile_tokens(p.G);
   if (!ps::layout_workspace(p, static_cast<uint8_t*>(workspace), workspace_bytes, false))
     return PS_ERR_WORKSPACE;
-  return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream));
+  return ps::run_attention(p, const_cast<void*>(k_pool), const_cast<void*>(v_pool),
+                           dtype == PS_BF16, static_cast<cudaStream_t>(stream));
 }
 
 int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
@@ -410,15 +418,28 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
   if (T == 0) return PS_OK;
   if (!k || !v || !slot_mapping) return PS_ERR_ARG;
   if (!aligned16(k) || !aligned16(v)) return PS_ERR_ALIGN;
-  rc = ps_slot_mapping(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
-                           num_blocks, slot_mapping, stream);
-  if (rc) return rc;
-  rc = ps_reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, T, H_kv, D, num_blocks, dtype,
-                            stream);
-  if (rc) return rc;
-  return ps_paged_attention(q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
-                            query_start_loc, B, T, H_q, H_kv, D, num_blocks, scale, out,
-                            workspace, workspace_bytes, dtype, stream);
+  ps::AttnParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.max_blocks = max_blocks_per_seq;
+  p.B = B;
+  p.T = T;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.D = D;
+  p.G = H_q / H_kv;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tpt = ps::tile_tokens(p.G);
+  p.slots = slot_mapping;
+  if (!ps::layout_workspace(p, static_cast<uint8_t*>(workspace), workspace_bytes, false))
+    return PS_ERR_WORKSPACE;
+  const ps::ScatterArgs sc{k, v};
+  return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream),
+                           &sc);
 }
 
 namespace {

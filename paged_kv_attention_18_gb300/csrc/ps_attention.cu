@@ -29,11 +29,12 @@ struct SeqInfo {
 
 // groups: 16-row groups of the split kernel; tile / qtiles: the sequence goes to the tile
 // kernel (more than 16 packed rows and a tile size exists) in qtiles 128-row tiles.
-__device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
+__device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, const int* qsl,
+                                            const int* lens, int b) {
   SeqInfo s;
-  s.tok0 = p.qsl[b];
-  s.n = p.qsl[b + 1] - s.tok0;
-  s.L = p.seq_lens[b];
+  s.tok0 = qsl[b];
+  s.n = qsl[b + 1] - s.tok0;
+  s.L = lens[b];
   s.pages = (s.L + kBlockSize - 1) / kBlockSize;
   s.valid = s.n >= 0 && s.n <= s.L && s.pages <= p.max_blocks;
   const int rows = s.valid ? s.n * p.G : 0;
@@ -127,17 +128,42 @@ __device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& i
 
 // One CTA turns the batch into two work lists: split-kernel items (sequences with at most
 // 16 packed rows: decodes) and tile-kernel items (prefill chunks, verify rows), plus the
-// per-token split table that the combine kernel reads.
+// per-token split table that the combine kernel reads. The per-sequence metadata is
+// staged in shared memory when the batch is small enough (kPlanSmemSeqs sequences), so
+// the passes and binary searches below read shared memory instead of global memory.
+constexpr int kPlanSmemSeqs = 4096;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
                                                     int tile_ctas) {
   __shared__ int sh[32];
   __shared__ long long shl[32];
+  extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const bool in_smem = p.B <= kPlanSmemSeqs;
+  int* s_qsl = plan_smem;                 // [B + 1]
+  int* s_len = s_qsl + (p.B + 1);         // [B]
+  int* s_offd = s_len + p.B;              // [B + 1]
+  int* s_offt = s_offd + (p.B + 1);       // [B + 1]
+  const int* qsl = p.qsl;
+  const int* lens = p.seq_lens;
+  int* off_d = p.seq_off;
+  int* off_t = p.seq_off_t;
+  if (in_smem) {
+    for (int b = tid; b <= p.B; b += nth) s_qsl[b] = p.qsl[b];
+    for (int b = tid; b < p.B; b += nth) s_len[b] = p.seq_lens[b];
+    qsl = s_qsl;
+    lens = s_len;
+    off_d = s_offd;
+    off_t = s_offt;
+    __syncthreads();
+  }
 
   // cost of the batch in pages read, per kernel
   long long wd = 0, wt = 0;
   for (int b = tid; b < p.B; b += nth) {
-    const SeqInfo s = seq_info(p, b);
+    const SeqInfo s = seq_info(p, qsl, lens, b);
     if (!s.valid) {
       record_error(p.err, kDevBadSequence);
       continue;
@@ -157,7 +183,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       const int b = base + tid;
       int cd = 0, ct = 0;
       if (b < p.B) {
-        const SeqInfo s = seq_info(p, b);
+        const SeqInfo s = seq_info(p, qsl, lens, b);
         const int ns = seq_splits(s, pps_d, pps_t);
         if (s.tile) ct = s.qtiles * ns * p.H_kv;
         else cd = s.groups * ns * p.H_kv;
@@ -166,8 +192,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       const int exd = block_exscan(cd, sh, td);
       const int ext = block_exscan(ct, sh, tt);
       if (b < p.B) {
-        p.seq_off[b] = run_d + exd;
-        p.seq_off_t[b] = run_t + ext;
+        off_d[b] = run_d + exd;
+        off_t[b] = run_t + ext;
       }
       run_d += td;
       run_t += tt;
@@ -178,14 +204,30 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       const int t = base + tid;
       int cnt = 0, ns_t = 0;
       if (t < p.T) {
-        const int b = last_le(p.qsl, p.B, t);
-        const SeqInfo s = seq_info(p, b);
+        const int b = last_le(qsl, p.B, t);
+        const SeqInfo s = seq_info(p, qsl, lens, b);
+        if (p.slots && attempt == 0) {
+          // the slot of this token: block_table[pos / 16] * 16 + pos % 16
+          int slot = -1;
+          if (s.valid) {
+            const int pos = s.L - s.n + (t - s.tok0);
+            const int blk =
+                __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pos / kBlockSize);
+            if (blk >= 0 && blk < p.num_blocks) slot = blk * kBlockSize + pos % kBlockSize;
+            else record_error(p.err, kDevBadBlockId);
+          }
+          p.slots[t] = slot;
+        }
         if (s.valid && s.groups > 0) {
           const int ns = seq_splits(s, pps_d, pps_t);
-          const int pos = s.L - s.n + (t - s.tok0);
-          const int page = pos / kBlockSize;
-          for (int k = 0; k < ns; ++k)
-            if ((k * s.pages) / ns <= page) ns_t = k + 1;
+          if (ns > 1) {
+            const int pos = s.L - s.n + (t - s.tok0);
+            const int page = pos / kBlockSize;
+            for (int k = 0; k < ns; ++k)
+              if ((k * s.pages) / ns <= page) ns_t = k + 1;
+          } else {
+            ns_t = 1;
+          }
           cnt = ns_t > 1 ? ns_t * p.H_q : 0;
         }
       }
@@ -210,17 +252,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     pps_t = pps_t >= (1 << 23) ? (1 << 24) : 2 * pps_t;
   }
   if (tid == 0) {
-    p.seq_off[p.B] = n_dec;
-    p.seq_off_t[p.B] = n_tile;
+    off_d[p.B] = n_dec;
+    off_t[p.B] = n_tile;
   }
   __syncthreads();
 
   // split-kernel items, group index fastest so rows sharing pages run back to back
   for (int i = tid; i < n_dec; i += nth) {
-    const int b = last_le(p.seq_off, p.B, i);
-    const SeqInfo s = seq_info(p, b);
+    const int b = last_le(off_d, p.B, i);
+    const SeqInfo s = seq_info(p, qsl, lens, b);
     const int ns = seq_splits(s, pps_d, pps_t);
-    const int local = i - p.seq_off[b];
+    const int local = i - off_d[b];
     const int j = local % s.groups;
     const int rest = local / s.groups;
     const int kv = rest % p.H_kv;
@@ -245,10 +287,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   }
   // tile-kernel items: the last (longest) query tile of a sequence first
   for (int i = tid; i < n_tile; i += nth) {
-    const int b = last_le(p.seq_off_t, p.B, i);
-    const SeqInfo s = seq_info(p, b);
+    const int b = last_le(off_t, p.B, i);
+    const SeqInfo s = seq_info(p, qsl, lens, b);
     const int ns = seq_splits(s, pps_d, pps_t);
-    const int local = i - p.seq_off_t[b];
+    const int local = i - off_t[b];
     const int j = s.qtiles - 1 - local % s.qtiles;
     const int rest = local / s.qtiles;
     const int kv = rest % p.H_kv;
@@ -326,6 +368,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
       reinterpret_cast<WorkItem*>(smem + W * S * kStage + W * S * 8) + warp * kRing;
   const uint32_t tiles_addr = smem_u32(tiles);
 
+  pdl_launch_dependents();
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
@@ -333,6 +376,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
     tma_prefetch_desc(&vmap);
   }
   __syncwarp();
+  pdl_wait();  // the plan (and the KV scatter) before this kernel are complete
 
   const int n_items = *reinterpret_cast<volatile int*>(p.hdr);
   const uint64_t policy = l2_policy_evict_first();
@@ -600,6 +644,8 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
 // ----------------------------------------------------------------------------------
 template <bool kBF16, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= p.T * p.H_q) return;
@@ -655,42 +701,47 @@ int attention_ctas(int D, int num_sms) { (void)D; return num_sms; }
 
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
                         cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(p, concurrency, tile_ctas);
+  const int smem = p.B <= kPlanSmemSeqs ? (4 * p.B + 3) * static_cast<int>(sizeof(int)) : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  plan_kernel<<<1, 1024, smem, stream>>>(p, concurrency, tile_ctas);
   return cudaGetLastError();
 }
 
 template <bool kBF16, int D>
 static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                  bool pdl) {
   constexpr int smem = split_smem_bytes<D>();
   auto kern = split_attention_kernel<kBF16, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<attention_ctas(D, num_sms), SplitCfg<D>::kWarps * 32, smem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(attention_ctas(D, num_sms)), dim3(SplitCfg<D>::kWarps * 32),
+                       smem, stream, pdl, kmap, vmap, p);
 }
 
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                   bool pdl) {
   if (p.D == 128)
-    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, num_sms, stream)
-                : launch_split_t<false, 128>(p, kmap, vmap, num_sms, stream);
-  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, num_sms, stream)
-              : launch_split_t<false, 64>(p, kmap, vmap, num_sms, stream);
+    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, num_sms, stream, pdl)
+                : launch_split_t<false, 128>(p, kmap, vmap, num_sms, stream, pdl);
+  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, num_sms, stream, pdl)
+              : launch_split_t<false, 64>(p, kmap, vmap, num_sms, stream, pdl);
 }
 
-cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream) {
+cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream, bool pdl) {
   const int64_t warps = static_cast<int64_t>(p.T) * p.H_q;
   if (warps == 0) return cudaSuccess;
-  const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  if (p.D == 128) {
-    if (bf16) combine_kernel<true, 128><<<blocks, 256, 0, stream>>>(p);
-    else combine_kernel<false, 128><<<blocks, 256, 0, stream>>>(p);
-  } else {
-    if (bf16) combine_kernel<true, 64><<<blocks, 256, 0, stream>>>(p);
-    else combine_kernel<false, 64><<<blocks, 256, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>((warps * 32 + 255) / 256));
+  if (p.D == 128)
+    return bf16 ? launch_kernel(combine_kernel<true, 128>, grid, dim3(256), 0, stream, pdl, p)
+                : launch_kernel(combine_kernel<false, 128>, grid, dim3(256), 0, stream, pdl, p);
+  return bf16 ? launch_kernel(combine_kernel<true, 64>, grid, dim3(256), 0, stream, pdl, p)
+              : launch_kernel(combine_kernel<false, 64>, grid, dim3(256), 0, stream, pdl, p);
 }
 
 }  // namespace ps

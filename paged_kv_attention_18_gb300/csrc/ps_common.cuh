@@ -31,6 +31,14 @@ enum DevError : int {
   kDevPlanOverflow = 5,   // the work plan did not fit the workspace
 };
 
+// Programmatic dependent launch: let the next kernel on the stream start launching, and
+// wait until the previous kernel has finished and its writes are visible. Both are no-ops
+// for a kernel launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }

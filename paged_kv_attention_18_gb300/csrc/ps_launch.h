@@ -35,7 +35,26 @@ struct AttnParams {
   float* part_o;                 // [cap_part, D] normalised partial outputs
   int cap_items, cap_part;
   int* err;                      // device error word
+  int32_t* slots;                // [T] slot of every token, written by the planner (or null)
 };
+
+// Launch `kern` on `s`; with `pdl` the launch may overlap the tail of the previous kernel
+// on the stream (the kernel waits with pdl_wait before using that kernel's results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                                 const int32_t* qsl, int B, int T, int num_blocks, int32_t* slots,
@@ -43,7 +62,8 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, con
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots,
                                      void* k_pool, void* v_pool, int T, int H_kv, int D,
-                                     int num_blocks, int* err, int num_sms, cudaStream_t stream);
+                                     int num_blocks, int* err, int num_sms, cudaStream_t stream,
+                                     bool pdl = false);
 
 // Number of resident attention CTAs and warps per CTA the split kernel uses.
 int attention_ctas(int D, int num_sms);
@@ -57,12 +77,13 @@ int tile_tokens(int G);
 
 cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, bool pdl);
 
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
+                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                   bool pdl);
 
-cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream);
+cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream, bool pdl);
 
 // Workspace bytes before the split partials (header, work lists, per-token tables);
 // `headroom` reserves work-list room for splitting long contexts.
@@ -75,9 +96,17 @@ size_t partial_bytes(int64_t cap_part, int D);
 // False when even that does not fit.
 bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink);
 
-// Plan, split kernel, tile kernel, combine on `s` (p's problem and workspace fields set).
-int run_attention(const AttnParams& p, const void* k_pool, const void* v_pool, bool bf16,
-                  cudaStream_t s);
+// The new tokens' K/V to scatter into the pools right after planning (the planner writes
+// their slots into AttnParams::slots).
+struct ScatterArgs {
+  const void* k;
+  const void* v;
+};
+
+// Plan, [KV scatter], split kernel, tile kernel, combine on `s` (p's problem and workspace
+// fields set). The kernels after the first are chained with programmatic dependent launch.
+int run_attention(const AttnParams& p, void* k_pool, void* v_pool, bool bf16, cudaStream_t s,
+                  const ScatterArgs* scatter = nullptr);
 
 // Library state of the current device (set up on first use): SM count and the device
 // address of the library's device error word. Returns a ps_status.

@@ -93,5 +93,6 @@ extern "C" int ps_paged_attention_noalloc(const void* q, const void* k_pool, con
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tpt = ps::tile_tokens(p.G);
   if (!ps::layout_workspace(p, ws, PS_NOALLOC_SCRATCH_BYTES, true)) return PS_ERR_WORKSPACE;
-  return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream));
+  return ps::run_attention(p, const_cast<void*>(k_pool), const_cast<void*>(v_pool),
+                           dtype == PS_BF16, static_cast<cudaStream_t>(stream));
 }

@@ -51,6 +51,8 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
                                          const int32_t* __restrict__ slots,
                                          uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                                          int T, int row_vecs, int64_t num_slots, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();  // the slots may come from the kernel before this one
   const int64_t total = static_cast<int64_t>(T) * row_vecs;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -85,7 +87,7 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, con
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots,
                                      void* k_pool, void* v_pool, int T, int H_kv, int D,
                                      int num_blocks, int* err, int num_sms,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int row_vecs = H_kv * D / 8;  // 16-byte chunks per token row
   const int64_t total = static_cast<int64_t>(T) * row_vecs;
@@ -93,11 +95,11 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  reshape_and_cache_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), T, row_vecs,
-      static_cast<int64_t>(num_blocks) * kBlockSize, err);
-  return cudaGetLastError();
+  return launch_kernel(reshape_and_cache_kernel, dim3(static_cast<unsigned>(blocks)),
+                       dim3(threads), 0, stream, pdl, static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_pool),
+                       static_cast<uint4*>(v_pool), T, row_vecs,
+                       static_cast<int64_t>(num_blocks) * kBlockSize, err);
 }
 
 }  // namespace ps

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = TileSmem<D>;
   constexpr int kHalves = D / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();  // the plan and the kernels before this one are complete
   const int n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
   if (n_items == 0) return;  // nothing planned for this kernel (uniform across the grid)
 
@@ -478,23 +480,23 @@ int tile_tokens(int G) { return G >= 1 && G <= 16 ? kRows / G : 0; }
 template <bool kBF16, int D>
 static cudaError_t launch_tile_t(const AttnParams& p, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool pdl) {
   constexpr int smem = TileSmem<D>::kBytes;
   auto kern = tile_attention_kernel<kBF16, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, stream>>>(kmap, vmap, qmap, p);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(num_sms), dim3(kThreads), smem, stream, pdl, kmap, vmap, qmap,
+                       p);
 }
 
 cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool pdl) {
   if (p.D == 128)
-    return bf16 ? launch_tile_t<true, 128>(p, kmap, vmap, qmap, num_sms, stream)
-                : launch_tile_t<false, 128>(p, kmap, vmap, qmap, num_sms, stream);
-  return bf16 ? launch_tile_t<true, 64>(p, kmap, vmap, qmap, num_sms, stream)
-              : launch_tile_t<false, 64>(p, kmap, vmap, qmap, num_sms, stream);
+    return bf16 ? launch_tile_t<true, 128>(p, kmap, vmap, qmap, num_sms, stream, pdl)
+                : launch_tile_t<false, 128>(p, kmap, vmap, qmap, num_sms, stream, pdl);
+  return bf16 ? launch_tile_t<true, 64>(p, kmap, vmap, qmap, num_sms, stream, pdl)
+              : launch_tile_t<false, 64>(p, kmap, vmap, qmap, num_sms, stream, pdl);
 }
 
 }  // namespace ps
