@@ -53,13 +53,14 @@ KERNEL_SOURCES = ["paged_kv_attention_18_gb300/csrc/ps_attention.cu",
 def step_work(wl: W.Workload, st: W.Step) -> dict:
     """Algorithmic bytes and flops of one step (each context read once, no split partials).
 
-    Also split by the kernel that serves each sequence: sequences with more than 16
-    packed rows (n * G) go to the tile kernel, the others to the split kernel."""
+    Also split by the kernel that serves each sequence: sequences with more than 64
+    packed rows (n * G, four 16-row groups) go to the tile kernel, the others (decodes,
+    verify rows) to the split kernel."""
     es = 2  # bytes per 16-bit element
     L = st.seq_lens.astype(np.int64)
     n = np.diff(st.query_start_loc).astype(np.int64)
     G = wl.H_q // wl.H_kv
-    tile = (n * G > 16) & (G <= 16)
+    tile = (n * G > 64) & (G <= 16)
     live = n > 0
     kv_b = L * wl.H_kv * wl.D * es * 2
     qo_b = 2 * n * wl.H_q * wl.D * es

@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       if (b < p.B) {
         const SeqInfo s = seq_info(p, qsl, lens, b);
         const int ns = seq_splits(s, pps_d, pps_t);
-        if (s.tile) ct = s.qtiles * ns * p.H_kv;
+        if (s.tile) ct = (s.qtiles + 1) / 2 * ns * p.H_kv;  // pairs of query tiles
         else cd = s.groups * ns * p.H_kv;
       }
       int td, tt;
@@ -285,22 +285,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
     store_item(p.items + i, it);
   }
-  // tile-kernel items: the last (longest) query tile of a sequence first
+  // tile-kernel items: pairs of consecutive query tiles (A, B), the last (longest) pair of
+  // a sequence first
   for (int i = tid; i < n_tile; i += nth) {
     const int b = last_le(off_t, p.B, i);
     const SeqInfo s = seq_info(p, qsl, lens, b);
     const int ns = seq_splits(s, pps_d, pps_t);
+    const int npairs = (s.qtiles + 1) / 2;
     const int local = i - off_t[b];
-    const int j = s.qtiles - 1 - local % s.qtiles;
-    const int rest = local / s.qtiles;
+    const int j = npairs - 1 - local % npairs;
+    const int rest = local / npairs;
     const int kv = rest % p.H_kv;
     const int sp = rest / p.H_kv;
+    const int qa = 2 * j * p.tpt, qb = qa + p.tpt;  // first query of tiles A and B
+    const int na = min(p.tpt, s.n - qa), nb = qb < s.n ? min(p.tpt, s.n - qb) : 0;
     WorkItem it;
     it.seq = b;
     it.kv = kv;
-    it.row0 = j * p.tpt * p.G;
-    it.nrows = min(p.tpt, s.n - j * p.tpt) * p.G;
-    const int i_last = j * p.tpt + it.nrows / p.G - 1;
+    it.row0 = qa * p.G;
+    it.nrows = na * p.G;
+    const int i_last = nb > 0 ? qb + nb - 1 : qa + na - 1;
     const int page_last = (s.L - s.n + i_last) / kBlockSize;
     it.page_begin = (sp * s.pages) / ns;
     it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
@@ -309,7 +313,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     it.ctx_len = s.L;
     it.n_query = s.n;
     it.tok0 = s.tok0;
-    it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
+    it.pad[0] = nb * p.G;
+    it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
     store_item(p.tile_items + i, it);
   }
   if (tid == 0) {
@@ -326,15 +331,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
 // ----------------------------------------------------------------------------------
 // split kernel: one warp = one work item at a time
 // ----------------------------------------------------------------------------------
+// Shape of the split kernel: warps per CTA, ring stages per warp (one page of K and V per
+// stage) and CTAs per SM. Overridable at build time for tuning sweeps.
+#ifndef PS_SPLIT_WARPS
+#define PS_SPLIT_WARPS 8
+#endif
+#ifndef PS_SPLIT_STAGES
+#define PS_SPLIT_STAGES 3
+#endif
+#ifndef PS_SPLIT_CTAS_PER_SM
+#define PS_SPLIT_CTAS_PER_SM 1
+#endif
 template <int D>
 struct SplitCfg;
 template <>
 struct SplitCfg<128> {
-  static constexpr int kWarps = 4, kStages = 4;
+  static constexpr int kWarps = PS_SPLIT_WARPS, kStages = PS_SPLIT_STAGES;
 };
 template <>
 struct SplitCfg<64> {
-  static constexpr int kWarps = 4, kStages = 8;
+  static constexpr int kWarps = PS_SPLIT_WARPS, kStages = 2 * PS_SPLIT_STAGES;
 };
 
 template <int D>
@@ -346,7 +362,7 @@ constexpr int split_smem_bytes() {
 }
 
 template <bool kBF16, int D>
-__global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, 1)
+__global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM)
     split_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   constexpr int W = SplitCfg<D>::kWarps;
@@ -697,7 +713,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
 // launchers
 // ----------------------------------------------------------------------------------
 int attention_warps(int D) { return D == 128 ? SplitCfg<128>::kWarps : SplitCfg<64>::kWarps; }
-int attention_ctas(int D, int num_sms) { (void)D; return num_sms; }
+int attention_ctas(int D, int num_sms) { (void)D; return num_sms * PS_SPLIT_CTAS_PER_SM; }
 
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
                         cudaStream_t stream) {

@@ -16,7 +16,7 @@ constexpr int kBlockSize = 16;      // tokens per KV block (page)
 constexpr int kMaxSplits = 32;      // KV splits of one query row, at most
 constexpr int kMinSplitPages = 8;   // pages in one split, at least
 constexpr int kSplitGroupLimit = 4; // only sequences with <= this many 16-row groups split
-constexpr int kTileMinGroups = 1;   // sequences with more 16-row groups than this use tiles
+constexpr int kTileMinGroups = 4;   // sequences with more 16-row groups than this use tiles
 constexpr int kTileSplitQTiles = 2; // tile-class sequences with <= this many query tiles split
 constexpr int kTilePagesAlign = 8;  // tile-class split sizes are whole 128-key tiles
 
@@ -57,7 +57,7 @@ struct __align__(16) WorkItem {
   int ctx_len;     // context length L after this step
   int n_query;     // query tokens n of the sequence this step
   int tok0;        // packed index of the sequence's first query token
-  int pad[5];
+  int pad[5];      // tile items: pad[0] = rows of the second query tile (0 = none)
 };
 static_assert(sizeof(WorkItem) == 64, "WorkItem is one 64-byte record");
 

@@ -1,25 +1,24 @@
-// Tile kernel for prefill chunks and speculative-verify rows: tcgen05 MMA with TMEM
-// accumulators, K/V pages fed by TMA straight from the paged pool.
+// Tile kernel for prefill chunks: tcgen05 MMA with TMEM accumulators, K/V pages fed by
+// TMA straight from the paged pool.
 //
-// One work item is up to 128 packed query rows of one sequence and one KV head (whole
-// query tokens x the G query heads that share the KV head) over one split of the
-// context. The context is walked in tiles of 128 keys (8 pages of 16):
-//     S = Q K^T          tcgen05.mma: A = Q (smem), B = K (smem)      -> S in TMEM
-//     P = exp2(S*scale*log2e - m) with the online row max / sum (softmax threads)
-//     O += P V           tcgen05.mma: A = P (TMEM), B = V (smem)      -> O in TMEM
+// One work item is a pair of query tiles of one sequence and one KV head: tile A and the
+// tile after it, B, each up to 128 packed rows (whole query tokens x the G query heads
+// that share the KV head), over one split of the context. The context is walked in
+// tiles of 128 keys (8 pages of 16); each K/V tile serves both query tiles:
+//     S_g = Q_g K^T        tcgen05.mma: A = Q_g (smem), B = K (smem)    -> S_g in TMEM
+//     P_g = exp2(S_g*scale*log2e - m) with the online row max / sum (softmax group g)
+//     O_g += P_g V         tcgen05.mma: A = P_g (TMEM), B = V (smem)    -> O_g in TMEM
 // with the causal rule of the pages (key j visible to the query at position p iff
-// j <= p: PageServe section 01; tinyserve "How it works", stepped causal mask) and
-// grouped-query attention (tinyserve "Highlights" table).
+// j <= p: PageServe section 01; tinyserve "How it works") and grouped-query attention
+// (tinyserve "Highlights" table).
 //
-// Warp roles (384 threads): warp 0 issues TMA and hands out work items; warp 1 owns TMEM
-// and issues the MMAs (warps 2, 3 idle); warps 4..7 and 8..11 are two softmax groups, one
+// Warp roles (384 threads): warp 0 issues TMA and hands out work items (the page copies of
+// a K/V tile are spread over its 32 lanes); warp 1 owns TMEM and issues the MMAs (warps 2,
+// 3 idle); warps 4..7 (query tile A) and 8..11 (query tile B) are two softmax groups, one
 // TMEM lane (one query row) per thread (a warp reaches the 32 TMEM lanes of its warp index
-// mod 4). The groups take alternate KV tiles of an item (even / odd), each
-// with its own S and O in TMEM, so one group's exponentials run while the tensor core
-// computes the other group's products. P is written back over S in TMEM and read from
-// there by the PV product. At the end of an item group 0 merges the two partial
-// results (reading group 1's O straight from TMEM) and writes the output. O is rescaled
-// lazily, only when a row's running max grows by more than 2^8.
+// mod 4). While one group computes its exponentials the tensor core works on the other
+// group's products. P is written back over S in TMEM and read from there by the PV
+// product. O is rescaled lazily, only when a row's running max grows by more than 2^8.
 #include "ps_common.cuh"
 #include "ps_launch.h"
 #include "ps_tc05.cuh"
@@ -32,7 +31,7 @@ constexpr int kRows = 128;        // query rows per tile (MMA M)
 constexpr int kKeys = 128;        // keys per KV tile (MMA N of S, K of PV) = 8 pages
 constexpr int kPagesPerTile = kKeys / kBlockSize;
 constexpr int kSub = kRows * 128; // bytes of one [128 rows x 64 elements] swizzled sub-tile
-constexpr int kStages = 3;        // K/V tile stages
+constexpr int kStages = 2;        // K/V tile stages
 constexpr int kItemRing = 4;
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
@@ -47,13 +46,12 @@ __host__ __device__ constexpr uint32_t col_o(int g) { return g * 256u + 128u; }
 
 template <int D>
 struct TileSmem {
-  static constexpr int kQ = (D / 64) * kSub;  // Q tile
+  static constexpr int kQ = (D / 64) * kSub;  // one query tile
   static constexpr int kK = (D / 64) * kSub;  // K tile (128 keys)
   static constexpr int kStage = 2 * kK;       // K + V
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kQ;
-  static constexpr int kOffML = kOffKV + kStages * kStage;  // group 1's row max / sum
-  static constexpr int kOffBar = kOffML + kRows * 8;
+  static constexpr int kOffQ = 0;             // query tiles A, B
+  static constexpr int kOffKV = kOffQ + 2 * kQ;
+  static constexpr int kOffBar = kOffKV + kStages * kStage;
   static constexpr int kBytes = kOffBar + 256 + 1024;  // barriers, ring; alignment slack
 };
 static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
@@ -61,8 +59,8 @@ static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
 struct TileBars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_done[2];
-  uint64_t ml_ready, o_free, mma_final;
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t mma_final;
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   int item_idx[kItemRing];
   uint32_t tmem_base;
@@ -89,7 +87,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   TileBars* bars = reinterpret_cast<TileBars*>(smem + L::kOffBar);
-  float2* ml = reinterpret_cast<float2*>(smem + L::kOffML);
   const uint32_t sQ = smem_u32(smem + L::kOffQ);
   const uint32_t sKV = smem_u32(smem + L::kOffKV);
 
@@ -104,9 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->p_full[g], 4);
       mbar_init(&bars->o_done[g], 1);
+      mbar_init(&bars->o_free[g], 4);
     }
-    mbar_init(&bars->ml_ready, 4);
-    mbar_init(&bars->o_free, 4);
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(&bars->item_full[s], 1);
@@ -170,14 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
       const int seq = w.seq, kv = w.kv;
+      const bool has_b = w.pad[0] > 0;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-      // Q tile: whole tokens x the G heads of this KV head
+      // query tiles: whole tokens x the G heads of this KV head
       if (!wait(&bars->q_empty, (qi & 1) ^ 1)) break;
       if (lane == 0) {
         const int tok = w.tok0 + w.row0 / p.G;
-        mbar_arrive_expect_tx(&bars->q_full, kHalves * 64 * 2 * p.G * p.tpt);
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_3d(smem + L::kOffQ + h * kSub, &qmap, &bars->q_full, h * 64, kv * p.G, tok);
+        const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
+        mbar_arrive_expect_tx(&bars->q_full, has_b ? 2 * tile_bytes : tile_bytes);
+        for (int q = 0; q < (has_b ? 2 : 1); ++q)
+          for (int h = 0; h < kHalves; ++h)
+            tma_load_3d(smem + L::kOffQ + q * L::kQ + h * kSub, &qmap, &bars->q_full, h * 64,
+                        kv * p.G, tok + q * p.tpt);
       }
       ++qi;
       // K/V tiles, 8 pages each; pages past the split read the zero fill
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ MMA issuer ========================================
     constexpr uint32_t idS = idesc_f16(kBF16, kRows, kKeys, false);
     constexpr uint32_t idPV = idesc_f16(kBF16, kRows, D, true);
-    uint32_t g = 0, qi = 0, pc[2] = {0, 0};
+    uint32_t g = 0, qi = 0, pc[2] = {0, 0}, act[2] = {0, 0};
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
@@ -228,36 +228,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
+      const bool has_b = w.pad[0] > 0;
+      const int ng = has_b ? 2 : 1;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       if (!wait(&bars->q_full, qi & 1)) break;
       const uint32_t g0 = g;
-      // S of tile j into the TMEM of group j & 1
-      auto issue_s = [&](int j) -> bool {
+      // S of query tile `grp` against K tile j
+      auto issue_s = [&](int grp, int j) -> bool {
         const uint32_t st = (g0 + j) % kStages;
         if (!wait(&bars->kv_full[st], ((g0 + j) / kStages) & 1)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t kbase = sKV + st * L::kStage;
-          const uint32_t dS = tmem + col_s(j & 1);
+          const uint32_t qbase = sQ + grp * L::kQ;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sQ + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
+            const uint64_t a = sdesc_sw128(qbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
             const uint64_t b = sdesc_sw128(kbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
-            umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
+            umma_f16(tmem + col_s(grp), a, b, idS, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&bars->s_full[j & 1]);
-          if (j == nt - 1) umma_commit(&bars->q_empty);  // Q is no longer needed
+          umma_commit(&bars->s_full[grp]);
+          if (j == nt - 1 && grp == ng - 1) umma_commit(&bars->q_empty);  // Q no longer needed
         }
         __syncwarp();
         return true;
       };
-      if (!issue_s(0) || (nt > 1 && !issue_s(1))) break;
-      for (int j = 0; j < nt; ++j) {
-        const int grp = j & 1;
-        if (!wait(&bars->p_full[grp], pc[grp] & 1)) { ok = false; break; }
+      // O of query tile `grp` += P V of K/V tile j
+      auto issue_pv = [&](int grp, int j) -> bool {
+        if (!wait(&bars->p_full[grp], pc[grp] & 1)) return false;
         ++pc[grp];
-        // the previous item's epilogue has read both groups' O
-        if (j == 0 && !wait(&bars->o_free, (qi & 1) ^ 1)) { ok = false; break; }
+        // the previous item's epilogue of this group has read its O
+        if (j == 0 && !wait(&bars->o_free[grp], (act[grp] & 1) ^ 1)) return false;
         tc_fence_after();
         const uint32_t st = (g0 + j) % kStages;
         if (lane == 0) {
@@ -266,20 +267,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kKeys / 16; ++kk) {
             const uint64_t b = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
             umma_f16_ts(tmem + col_o(grp), tmem + col_s(grp) + kk * 8, b, idPV,
-                        (j >= 2 || kk > 0) ? 1u : 0u);
+                        (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&bars->kv_empty[st]);
+          if (grp == ng - 1) umma_commit(&bars->kv_empty[st]);  // last reader of the stage
         }
         __syncwarp();
-        // the next S of this group overwrites its P: issued after this PV (in order)
-        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
-      }
+        return true;
+      };
+      for (int q = 0; q < ng && ok; ++q) ok = issue_s(q, 0);
+      // per K/V tile: PV of A, next S of A, PV of B, next S of B. A query tile's next S
+      // overwrites its P in TMEM, so it is issued after that tile's PV (in order).
+      for (int j = 0; j < nt && ok; ++j)
+        for (int q = 0; q < ng && ok; ++q) {
+          ok = issue_pv(q, j);
+          if (ok && j + 1 < nt) ok = issue_s(q, j + 1);
+        }
       if (!ok) break;
-      if (lane == 0) {
-        umma_commit(&bars->o_done[0]);
-        umma_commit(&bars->o_done[1]);
-      }
+      if (lane == 0)
+        for (int q = 0; q < ng; ++q) umma_commit(&bars->o_done[q]);
       __syncwarp();
+      for (int q = 0; q < ng; ++q) ++act[q];
       g += nt;
       ++qi;
     }
@@ -289,13 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(&bars->mma_final, 0, 1u << 22);
   } else if (warp >= 4) {
     // ============================ softmax groups + epilogue =========================
-    const int grp = (warp - 4) >> 2;   // 0: even KV tiles, 1: odd KV tiles
+    const int grp = (warp - 4) >> 2;   // 0: query tile A, 1: query tile B
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t tS = trow + col_s(grp), tO = trow + col_o(grp);
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, qi = 0;
+    uint32_t sc = 0, act = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
@@ -303,19 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
+      const int nrows = grp == 0 ? w.nrows : w.pad[0];
+      if (nrows == 0) continue;  // no query tile B in this item
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       // this thread's query row
-      const bool valid = r < w.nrows;
-      const int qtok = (w.row0 + r) / p.G;  // query index within the sequence
+      const bool valid = r < nrows;
+      const int R = w.row0 + grp * p.tpt * p.G + r;  // packed row within the sequence
+      const int qtok = R / p.G;                        // query index within the sequence
       const int tok = w.tok0 + qtok;
-      const int head = w.kv * p.G + (w.row0 + r) - qtok * p.G;
+      const int head = w.kv * p.G + R - qtok * p.G;
       const int pos = valid ? w.ctx_len - w.n_query + qtok : -1;
       const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
       // m_ref: the reference max (log2 units) that P, O and l are currently taken against;
       // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
       float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
-      bool started = false;  // this group has written O for this item
-      for (int j = grp; j < nt; j += 2) {
+      for (int j = 0; j < nt; ++j) {
         const int lim = key_hi - (pb * kBlockSize + j * kKeys);  // visible columns: c <= lim
         if (!wait(&bars->s_full[grp], sc & 1)) { ok = false; break; }
         ++sc;
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, m_next > m_ref)) {
           const bool need = m_next > m_ref;
           const float alpha = need ? fast_exp2(m_ref - m_next) : 1.f;
-          if (started) rescale_o(alpha);
+          if (j > 0) rescale_o(alpha);
           l *= alpha;
           if (need) m_ref = m_next;
         }
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (m_ref == -INFINITY && m_half != -INFINITY);
           if (__any_sync(0xffffffffu, move)) {
             const float alpha = move && m_ref != -INFINITY ? fast_exp2(m_ref - m_half) : 1.f;
-            if (started) rescale_o(alpha);
+            if (j > 0) rescale_o(alpha);
             l *= alpha;
             if (h == 1) {  // the half of P already written: columns 0..31
               uint32_t q[32];
@@ -399,72 +408,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tS + 32 * h + 16, pk + 16);
         }
         m_next = m_tile > m_ref + kRescaleLog2 ? m_tile : m_ref;
-        started = true;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[grp]);
       }
       if (!ok) break;
-      // epilogue: wait for this item's last products
-      if (!wait(&bars->o_done[grp], qi & 1)) break;
+      // epilogue: O / l of this group's rows to the output, or to the split partials
+      if (!wait(&bars->o_done[grp], act & 1)) break;
       tc_fence_after();
-      if (grp == 1) {
-        ml[r] = make_float2(m_ref, l);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ml_ready);
-      } else {
-        if (!wait(&bars->ml_ready, qi & 1)) break;
-        const float2 other = ml[r];
-        const float M = fmaxf(m_ref, other.x);
-        const float a = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - M);
-        const float b = other.x == -INFINITY ? 0.f : fast_exp2(other.x - M);
-        const float lt = a * l + b * other.y;
-        int ns_t = 0;
-        if (valid) ns_t = __ldg(p.tok_ns + tok);
-        const bool write = valid && w.split < ns_t && lt > 0.f;
-        const float inv = write ? 1.f / lt : 0.f;
-        const float ca = a * inv, cb = b * inv;
-        const bool any_b = __any_sync(0xffffffffu, b != 0.f);
-        const uint32_t tO1 = trow + col_o(1);
+      int ns_t = 0;
+      if (valid) ns_t = __ldg(p.tok_ns + tok);
+      const bool write = valid && w.split < ns_t && l > 0.f;
+      const float inv = write ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32], u[32];
-          tmem_ld32(tO + c * 32, v);
-          if (any_b) tmem_ld32(tO1 + c * 32, u);
-          tmem_ld_wait();
-          if (!write) continue;
-          float* o = reinterpret_cast<float*>(v);  // merged row, in place
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        tmem_ld_wait();
+        if (!write) continue;
+        if (ns_t == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                (static_cast<int64_t>(tok) * p.H_q + head) * D +
+                                                c * 32);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(v[e]) * ca;
-            if (any_b && b != 0.f) x = fmaf(__uint_as_float(u[e]), cb, x);
-            o[e] = x;
-          }
-          if (ns_t == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                  (static_cast<int64_t>(tok) * p.H_q + head) * D +
-                                                  c * 32);
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(
+                pack2<kBF16>(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+        } else {
+          const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
+          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack2<kBF16>(o[8 * q + 0], o[8 * q + 1]),
-                                  pack2<kBF16>(o[8 * q + 2], o[8 * q + 3]),
-                                  pack2<kBF16>(o[8 * q + 4], o[8 * q + 5]),
-                                  pack2<kBF16>(o[8 * q + 6], o[8 * q + 7]));
-          } else {
-            const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
-            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            if (c == 0) p.part_lse[pidx] = M + __log2f(lt);
-          }
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          if (c == 0) p.part_lse[pidx] = m_ref + __log2f(l);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_free);
       }
-      ++qi;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[grp]);
+      ++act;
     }
   }
   tc_fence_before();
