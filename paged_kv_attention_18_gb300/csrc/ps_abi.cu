@@ -182,6 +182,9 @@ size_t workspace_fixed_bytes(int T, int B, int H_q, int H_kv, bool headroom, int
   o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_t
   o = up256(o + static_cast<size_t>(T) * 4);                        // tok_ns
   o = up256(o + static_cast<size_t>(T) * 4);                        // tok_base
+  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_p
+  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_s
+  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_list
   return o;
 }
 
@@ -210,6 +213,12 @@ bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink) {
   p.tok_ns = reinterpret_cast<int*>(ws + o);
   o = up256(o + static_cast<size_t>(p.T) * 4);
   p.tok_base = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.T) * 4);
+  p.seq_off_p = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.B + 1) * 4);
+  p.seq_off_s = reinterpret_cast<int*>(ws + o);
+  o = up256(o + static_cast<size_t>(p.B + 1) * 4);
+  p.tok_list = reinterpret_cast<int*>(ws + o);
   o = up256(o + static_cast<size_t>(p.T) * 4);
   // the rest holds split partials
   const size_t left = bytes - o;
@@ -262,7 +271,7 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   }
   {
     Timed tm(4, s);
-    if ((e = launch_combine(p, bf16, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
+    if ((e = launch_combine(p, bf16, num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
   }
   return PS_OK;
 }

@@ -97,14 +97,99 @@ __device__ int block_exscan(int v, int* sh, int& total) {
   return prefix + x - v;
 }
 
-__device__ long long block_sum_ll(long long v, long long* sh) {
+// Exclusive scan of four counters at once (one set of barriers for all four).
+__device__ int4 block_exscan4(int4 v, int4* sh, int4& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int4 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, x.x, o), b = __shfl_up_sync(0xffffffffu, x.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, x.z, o), d = __shfl_up_sync(0xffffffffu, x.w, o);
+    if (lane >= o) {
+      x.x += a;
+      x.y += b;
+      x.z += c;
+      x.w += d;
+    }
+  }
+  if (lane == 31) sh[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int4 w = lane < nw ? sh[lane] : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, w.x, o), b = __shfl_up_sync(0xffffffffu, w.y, o);
+      const int c = __shfl_up_sync(0xffffffffu, w.z, o), d = __shfl_up_sync(0xffffffffu, w.w, o);
+      if (lane >= o) {
+        w.x += a;
+        w.y += b;
+        w.z += c;
+        w.w += d;
+      }
+    }
+    sh[lane] = w;
+  }
+  __syncthreads();
+  const int4 pre = wid ? sh[wid - 1] : make_int4(0, 0, 0, 0);
+  total = sh[nw - 1];
+  __syncthreads();
+  return make_int4(pre.x + x.x - v.x, pre.y + x.y - v.y, pre.z + x.z - v.z, pre.w + x.w - v.w);
+}
+
+// Token i (0-based within its sequence, at position L - n + i) lies on page (L - n + i) / 16;
+// split k of a sequence split ns ways starts at page (k * pages) / ns, so the first token
+// that split k covers is first_k = max(0, 16 * start_k - (L - n)). A token's rows are held
+// by the splits with first_k <= i; with more than one, each holds H_q partial entries.
+__device__ __forceinline__ int split_first_token(const SeqInfo& s, int ns, int k) {
+  const int f = (k * s.pages) / ns * kBlockSize - (s.L - s.n);
+  return f > 0 ? f : 0;
+}
+
+// For token i: the splits holding its rows (*held) and, summed over the tokens before it,
+// the splits holding each token held by at least two (the tokens from first_1 on). The
+// split starts k * pages / ns are stepped with a running remainder, without dividing.
+__device__ __forceinline__ int split_entries_before(const SeqInfo& s, int ns, int i,
+                                                    int* held = nullptr) {
+  const int q = s.pages / ns, r = s.pages - q * ns, p0 = s.L - s.n;
+  const int f1 = max(0, q * kBlockSize - p0);  // start_1 = q (r < ns)
+  int acc = 0, cnt = 0, start = 0, rem = 0;
+  for (int k = 0; k < ns; ++k) {
+    const int fk = max(0, start * kBlockSize - p0);
+    cnt += fk <= i ? 1 : 0;
+    const int from = fk > f1 ? fk : f1;
+    acc += i > from ? i - from : 0;
+    start += q;
+    rem += r;
+    if (rem >= ns) {
+      rem -= ns;
+      ++start;
+    }
+  }
+  if (held) *held = cnt;
+  return acc;
+}
+
+// Sums of two values over the block, returned to every thread.
+__device__ longlong2 block_sum2_ll(longlong2 v, longlong2* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
   if (lane == 0) sh[wid] = v;
   __syncthreads();
-  long long t = 0;
-  for (int i = 0; i < nw; ++i) t += sh[i];
+  if (wid == 0) {
+    longlong2 w = lane < nw ? sh[lane] : make_longlong2(0, 0);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      w.x += __shfl_xor_sync(0xffffffffu, w.x, o);
+      w.y += __shfl_xor_sync(0xffffffffu, w.y, o);
+    }
+    if (lane == 0) sh[0] = w;
+  }
+  __syncthreads();
+  const longlong2 t = sh[0];
   __syncthreads();
   return t;
 }
@@ -126,37 +211,44 @@ __device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& i
   dst[3] = src[3];
 }
 
-// One CTA turns the batch into two work lists: split-kernel items (sequences with at most
-// 16 packed rows: decodes) and tile-kernel items (prefill chunks, verify rows), plus the
-// per-token split table that the combine kernel reads. The per-sequence metadata is
-// staged in shared memory when the batch is small enough (kPlanSmemSeqs sequences), so
-// the passes and binary searches below read shared memory instead of global memory.
+// The planner turns the batch into two work lists: split-kernel items (sequences with at
+// most 64 packed rows: decodes, verify rows) and tile-kernel items (prefill chunks), plus
+// the per-token split table that the combine kernel reads and the slot of every new
+// token. Every count is taken per sequence (one scan over the batch); the token table
+// follows from closed forms per sequence. Each CTA of the grid repeats the scan (the
+// results are identical) and then writes its own share of the tokens and of the
+// sequences' items, so no CTA waits on another. The per-sequence metadata is staged in
+// shared memory when the batch is small enough (kPlanSmemSeqs sequences).
 constexpr int kPlanSmemSeqs = 4096;
+constexpr int kPlanSmemArrays = 6;  // qsl, lens and four offset arrays, B + 1 ints each
+constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
                                                     int tile_ctas) {
-  __shared__ int sh[32];
-  __shared__ long long shl[32];
+  __shared__ int4 sh4[32];
+  __shared__ longlong2 shl[32];
   extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
   pdl_launch_dependents();
   pdl_wait();
   const bool in_smem = p.B <= kPlanSmemSeqs;
-  int* s_qsl = plan_smem;                 // [B + 1]
-  int* s_len = s_qsl + (p.B + 1);         // [B]
-  int* s_offd = s_len + p.B;              // [B + 1]
-  int* s_offt = s_offd + (p.B + 1);       // [B + 1]
   const int* qsl = p.qsl;
   const int* lens = p.seq_lens;
   int* off_d = p.seq_off;
   int* off_t = p.seq_off_t;
+  int* off_p = p.seq_off_p;
+  int* off_s = p.seq_off_s;
   if (in_smem) {
+    int* s_qsl = plan_smem;
+    int* s_len = s_qsl + (p.B + 1);
     for (int b = tid; b <= p.B; b += nth) s_qsl[b] = p.qsl[b];
     for (int b = tid; b < p.B; b += nth) s_len[b] = p.seq_lens[b];
     qsl = s_qsl;
     lens = s_len;
-    off_d = s_offd;
-    off_t = s_offt;
+    off_d = s_len + (p.B + 1);
+    off_t = off_d + (p.B + 1);
+    off_p = off_t + (p.B + 1);
+    off_s = off_p + (p.B + 1);
     __syncthreads();
   }
 
@@ -171,160 +263,185 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     if (s.tile) wt += static_cast<long long>(s.qtiles) * s.pages;
     else wd += static_cast<long long>(s.groups) * s.pages;
   }
-  const long long Wd = block_sum_ll(wd, shl) * p.H_kv;
-  const long long Wt = block_sum_ll(wt, shl) * p.H_kv;
+  const longlong2 W = block_sum2_ll(make_longlong2(wd, wt), shl);
+  const long long Wd = W.x * p.H_kv, Wt = W.y * p.H_kv;
   int pps_d = pages_per_split(Wd, concurrency, 1);
   int pps_t = pages_per_split(Wt, tile_ctas, kTilePagesAlign);
 
-  int n_dec = 0, n_tile = 0, n_part = 0;
+  // per sequence: split-kernel items, tile-kernel items (pairs of query tiles), partial
+  // entries and split tokens; coarser splits while the lists overflow the workspace
+  int4 tot = make_int4(0, 0, 0, 0);
   for (int attempt = 0; attempt < 32; ++attempt) {
-    int run_d = 0, run_t = 0;
+    int4 run = make_int4(0, 0, 0, 0);
     for (int base = 0; base < p.B; base += nth) {
       const int b = base + tid;
-      int cd = 0, ct = 0;
+      int4 c = make_int4(0, 0, 0, 0);
       if (b < p.B) {
         const SeqInfo s = seq_info(p, qsl, lens, b);
         const int ns = seq_splits(s, pps_d, pps_t);
-        if (s.tile) ct = (s.qtiles + 1) / 2 * ns * p.H_kv;  // pairs of query tiles
-        else cd = s.groups * ns * p.H_kv;
+        if (s.tile) c.y = (s.qtiles + 1) / 2 * ns * p.H_kv;
+        else c.x = s.groups * ns * p.H_kv;
+        if (ns > 1) {
+          c.z = split_entries_before(s, ns, s.n) * p.H_q;
+          c.w = s.n - split_first_token(s, ns, 1);
+        }
       }
-      int td, tt;
-      const int exd = block_exscan(cd, sh, td);
-      const int ext = block_exscan(ct, sh, tt);
+      int4 t4;
+      const int4 ex = block_exscan4(c, sh4, t4);
       if (b < p.B) {
-        off_d[b] = run_d + exd;
-        off_t[b] = run_t + ext;
+        off_d[b] = run.x + ex.x;
+        off_t[b] = run.y + ex.y;
+        off_p[b] = run.z + ex.z;
+        off_s[b] = run.w + ex.w;
       }
-      run_d += td;
-      run_t += tt;
+      run.x += t4.x;
+      run.y += t4.y;
+      run.z += t4.z;
+      run.w += t4.w;
     }
-    // partial entries of every token whose rows are split
-    int prun = 0;
-    for (int base = 0; base < p.T; base += nth) {
-      const int t = base + tid;
-      int cnt = 0, ns_t = 0;
-      if (t < p.T) {
-        const int b = last_le(qsl, p.B, t);
-        const SeqInfo s = seq_info(p, qsl, lens, b);
-        if (p.slots && attempt == 0) {
-          // the slot of this token: block_table[pos / 16] * 16 + pos % 16
-          int slot = -1;
-          if (s.valid) {
-            const int pos = s.L - s.n + (t - s.tok0);
-            const int blk =
-                __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pos / kBlockSize);
-            if (blk >= 0 && blk < p.num_blocks) slot = blk * kBlockSize + pos % kBlockSize;
-            else record_error(p.err, kDevBadBlockId);
-          }
-          p.slots[t] = slot;
-        }
-        if (s.valid && s.groups > 0) {
-          const int ns = seq_splits(s, pps_d, pps_t);
-          if (ns > 1) {
-            const int pos = s.L - s.n + (t - s.tok0);
-            const int page = pos / kBlockSize;
-            for (int k = 0; k < ns; ++k)
-              if ((k * s.pages) / ns <= page) ns_t = k + 1;
-          } else {
-            ns_t = 1;
-          }
-          cnt = ns_t > 1 ? ns_t * p.H_q : 0;
-        }
-      }
-      int total;
-      const int ex = block_exscan(cnt, sh, total);
-      if (t < p.T) {
-        p.tok_ns[t] = ns_t;
-        p.tok_base[t] = prun + ex;
-      }
-      prun += total;
-    }
-    n_dec = run_d;
-    n_tile = run_t;
-    n_part = prun;
-    if (n_dec <= p.cap_items && n_tile <= p.cap_tile && n_part <= p.cap_part) break;
+    tot = run;
+    if (tot.x <= p.cap_items && tot.y <= p.cap_tile && tot.z <= p.cap_part) break;
     if (pps_d >= (1 << 24) && pps_t >= (1 << 24)) {  // cannot shrink further
       record_error(p.err, kDevPlanOverflow);
-      n_dec = n_tile = 0;
+      tot = make_int4(0, 0, 0, 0);
       break;
     }
     pps_d = pps_d >= (1 << 23) ? (1 << 24) : 2 * pps_d;
     pps_t = pps_t >= (1 << 23) ? (1 << 24) : 2 * pps_t;
   }
   if (tid == 0) {
-    off_d[p.B] = n_dec;
-    off_t[p.B] = n_tile;
+    off_d[p.B] = tot.x;
+    off_t[p.B] = tot.y;
+    off_p[p.B] = tot.z;
+    off_s[p.B] = tot.w;
   }
   __syncthreads();
+  const bool planned = tot.x > 0 || tot.y > 0;
 
-  // split-kernel items, group index fastest so rows sharing pages run back to back
-  for (int i = tid; i < n_dec; i += nth) {
-    const int b = last_le(off_d, p.B, i);
-    const SeqInfo s = seq_info(p, qsl, lens, b);
-    const int ns = seq_splits(s, pps_d, pps_t);
-    const int local = i - off_d[b];
-    const int j = local % s.groups;
-    const int rest = local / s.groups;
-    const int kv = rest % p.H_kv;
-    const int sp = rest / p.H_kv;
-    const int rows = s.n * p.G;
-    WorkItem it;
-    it.seq = b;
-    it.kv = kv;
-    it.row0 = 16 * j;
-    it.nrows = min(16, rows - 16 * j);
-    const int i_last = (it.row0 + it.nrows - 1) / p.G;
-    const int page_last = (s.L - s.n + i_last) / kBlockSize;
-    it.page_begin = (sp * s.pages) / ns;
-    it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
-    it.split = sp;
-    it.nsplit = ns;
-    it.ctx_len = s.L;
-    it.n_query = s.n;
-    it.tok0 = s.tok0;
-    it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
-    store_item(p.items + i, it);
+  // tokens: splits holding the rows, first partial entry, the combine's token list and the
+  // slot of the token's new K/V (block_table[pos / 16] * 16 + pos % 16). Four tokens per
+  // round so their block-table reads are in flight together.
+  constexpr int kTokUnroll = 4;
+  for (int base = blockIdx.x * kTokUnroll * nth; base < p.T; base += gridDim.x * kTokUnroll * nth) {
+    int bb[kTokUnroll], blk[kTokUnroll];
+#pragma unroll
+    for (int u = 0; u < kTokUnroll; ++u) {
+      const int t = base + u * nth + tid;
+      bb[u] = -1;
+      blk[u] = -1;
+      if (t < p.T) {
+        const int b = last_le(qsl, p.B, t);
+        const SeqInfo s = seq_info(p, qsl, lens, b);
+        bb[u] = b;
+        if (p.slots && s.valid) {
+          const int pos = s.L - s.n + (t - s.tok0);
+          blk[u] = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pos / kBlockSize);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTokUnroll; ++u) {
+      const int t = base + u * nth + tid;
+      if (t >= p.T) continue;
+      const int b = bb[u];
+      const SeqInfo s = seq_info(p, qsl, lens, b);
+      const int i = t - s.tok0;
+      if (p.slots) {
+        int slot = -1;
+        if (s.valid) {
+          const int pos = s.L - s.n + i;
+          if (blk[u] >= 0 && blk[u] < p.num_blocks) slot = blk[u] * kBlockSize + pos % kBlockSize;
+          else record_error(p.err, kDevBadBlockId);
+        }
+        p.slots[t] = slot;
+      }
+      int ns_t = 0, tb = 0;
+      if (planned && s.valid && s.groups > 0) {
+        const int ns = seq_splits(s, pps_d, pps_t);
+        ns_t = 1;
+        if (ns > 1) {
+          tb = off_p[b] + split_entries_before(s, ns, i, &ns_t) * p.H_q;
+          const int f1 = split_first_token(s, ns, 1);
+          if (i >= f1) p.tok_list[off_s[b] + (i - f1)] = t;
+        }
+      }
+      p.tok_ns[t] = ns_t;
+      p.tok_base[t] = tb;
+    }
   }
-  // tile-kernel items: pairs of consecutive query tiles (A, B), the last (longest) pair of
-  // a sequence first
-  for (int i = tid; i < n_tile; i += nth) {
-    const int b = last_le(off_t, p.B, i);
+
+  // work items, one warp per sequence: split-kernel items with the group index fastest
+  // (rows sharing pages run back to back); tile-kernel items as pairs of consecutive query
+  // tiles (A, B), the last (longest) pair of a sequence first
+  const int lane = tid & 31, nw = nth >> 5;
+  const int gw = blockIdx.x * nw + (tid >> 5);
+  for (int b = planned ? gw : p.B; b < p.B; b += gridDim.x * nw) {
     const SeqInfo s = seq_info(p, qsl, lens, b);
+    if (!s.valid || s.groups == 0) continue;
     const int ns = seq_splits(s, pps_d, pps_t);
-    const int npairs = (s.qtiles + 1) / 2;
-    const int local = i - off_t[b];
-    const int j = npairs - 1 - local % npairs;
-    const int rest = local / npairs;
-    const int kv = rest % p.H_kv;
-    const int sp = rest / p.H_kv;
-    const int qa = 2 * j * p.tpt, qb = qa + p.tpt;  // first query of tiles A and B
-    const int na = min(p.tpt, s.n - qa), nb = qb < s.n ? min(p.tpt, s.n - qb) : 0;
-    WorkItem it;
-    it.seq = b;
-    it.kv = kv;
-    it.row0 = qa * p.G;
-    it.nrows = na * p.G;
-    const int i_last = nb > 0 ? qb + nb - 1 : qa + na - 1;
-    const int page_last = (s.L - s.n + i_last) / kBlockSize;
-    it.page_begin = (sp * s.pages) / ns;
-    it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
-    it.split = sp;
-    it.nsplit = ns;
-    it.ctx_len = s.L;
-    it.n_query = s.n;
-    it.tok0 = s.tok0;
-    it.pad[0] = nb * p.G;
-    it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
-    store_item(p.tile_items + i, it);
+    if (!s.tile) {
+      const int cnt = s.groups * ns * p.H_kv, first = off_d[b], rows = s.n * p.G;
+      for (int local = lane; local < cnt; local += 32) {
+        const int j = local % s.groups;
+        const int rest = local / s.groups;
+        const int kv = rest % p.H_kv;
+        const int sp = rest / p.H_kv;
+        WorkItem it;
+        it.seq = b;
+        it.kv = kv;
+        it.row0 = 16 * j;
+        it.nrows = min(16, rows - 16 * j);
+        const int i_last = (it.row0 + it.nrows - 1) / p.G;
+        const int page_last = (s.L - s.n + i_last) / kBlockSize;
+        it.page_begin = (sp * s.pages) / ns;
+        it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
+        it.split = sp;
+        it.nsplit = ns;
+        it.ctx_len = s.L;
+        it.n_query = s.n;
+        it.tok0 = s.tok0;
+        it.pad[0] = it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
+        store_item(p.items + first + local, it);
+      }
+    } else {
+      const int npairs = (s.qtiles + 1) / 2;
+      const int cnt = npairs * ns * p.H_kv, first = off_t[b];
+      for (int local = lane; local < cnt; local += 32) {
+        const int j = npairs - 1 - local % npairs;
+        const int rest = local / npairs;
+        const int kv = rest % p.H_kv;
+        const int sp = rest / p.H_kv;
+        const int qa = 2 * j * p.tpt, qb = qa + p.tpt;  // first query of tiles A and B
+        const int na = min(p.tpt, s.n - qa), nb = qb < s.n ? min(p.tpt, s.n - qb) : 0;
+        WorkItem it;
+        it.seq = b;
+        it.kv = kv;
+        it.row0 = qa * p.G;
+        it.nrows = na * p.G;
+        const int i_last = nb > 0 ? qb + nb - 1 : qa + na - 1;
+        const int page_last = (s.L - s.n + i_last) / kBlockSize;
+        it.page_begin = (sp * s.pages) / ns;
+        it.page_end = min(((sp + 1) * s.pages) / ns, page_last + 1);
+        it.split = sp;
+        it.nsplit = ns;
+        it.ctx_len = s.L;
+        it.n_query = s.n;
+        it.tok0 = s.tok0;
+        it.pad[0] = nb * p.G;
+        it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
+        store_item(p.tile_items + first + local, it);
+      }
+    }
   }
-  if (tid == 0) {
-    p.hdr[0] = n_dec;
+  if (blockIdx.x == 0 && tid == 0) {
+    p.hdr[0] = tot.x;
     p.hdr[1] = 0;
     p.hdr[2] = pps_d;
-    p.hdr[3] = n_part;
-    p.hdr[4] = n_tile;
+    p.hdr[3] = tot.z;
+    p.hdr[4] = tot.y;
     p.hdr[5] = 0;
     p.hdr[6] = pps_t;
+    p.hdr[7] = planned ? tot.w : 0;
   }
 }
 
@@ -658,54 +775,58 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
 // ----------------------------------------------------------------------------------
 // combine: one warp per (token, head) whose rows were split
 // ----------------------------------------------------------------------------------
+// A fixed grid walks the planner's list of split tokens, so a batch with no split rows
+// costs one small launch.
 template <bool kBF16, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int n = *reinterpret_cast<volatile const int*>(p.hdr + 7) * p.H_q;
   const int lane = threadIdx.x & 31;
-  if (wid >= p.T * p.H_q) return;
-  const int tok = wid / p.H_q, h = wid - tok * p.H_q;
-  const int ns = __ldg(p.tok_ns + tok);
-  if (ns <= 1) return;
-  const int base = __ldg(p.tok_base + tok);
-  const float lse = lane < ns ? p.part_lse[base + lane * p.H_q + h] : -INFINITY;
-  float M = lse;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wid < n; wid += nwarps) {
+    const int li = wid / p.H_q, h = wid - li * p.H_q;
+    const int tok = p.tok_list[li];
+    const int ns = p.tok_ns[tok];
+    const int base = p.tok_base[tok];
+    const float lse = lane < ns ? p.part_lse[base + lane * p.H_q + h] : -INFINITY;
+    float M = lse;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w = (lane < ns && lse != -INFINITY) ? exp2f(lse - M) : 0.f;
-  float Wsum = w;
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (lane < ns && lse != -INFINITY) ? exp2f(lse - M) : 0.f;
+    float Wsum = w;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) Wsum += __shfl_xor_sync(0xffffffffu, Wsum, o);
-  constexpr int kPer = D / 32;  // elements per lane
-  float acc[kPer];
+    for (int o = 16; o; o >>= 1) Wsum += __shfl_xor_sync(0xffffffffu, Wsum, o);
+    constexpr int kPer = D / 32;  // elements per lane
+    float acc[kPer];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, w, s);
-    const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
-    if constexpr (kPer == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += ws * v.x;
-      acc[1] += ws * v.y;
-      acc[2] += ws * v.z;
-      acc[3] += ws * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += ws * v.x;
-      acc[1] += ws * v.y;
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += ws * v.x;
+        acc[1] += ws * v.y;
+        acc[2] += ws * v.z;
+        acc[3] += ws * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += ws * v.x;
+        acc[1] += ws * v.y;
+      }
     }
-  }
-  const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
-  uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + h) * D +
-                  lane * kPer;
-  if constexpr (kPer == 4) {
-    uint2 v;
-    v.x = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
-    v.y = pack2<kBF16>(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(dst) = v;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+    const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + h) * D +
+                    lane * kPer;
+    if constexpr (kPer == 4) {
+      uint2 v;
+      v.x = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+      v.y = pack2<kBF16>(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+    }
   }
 }
 
@@ -717,13 +838,18 @@ int attention_ctas(int D, int num_sms) { (void)D; return num_sms * PS_SPLIT_CTAS
 
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
                         cudaStream_t stream) {
-  const int smem = p.B <= kPlanSmemSeqs ? (4 * p.B + 3) * static_cast<int>(sizeof(int)) : 0;
+  const int smem =
+      p.B <= kPlanSmemSeqs ? kPlanSmemArrays * (p.B + 1) * static_cast<int>(sizeof(int)) : 0;
   if (smem > 48 * 1024) {
     const cudaError_t e =
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  plan_kernel<<<1, 1024, smem, stream>>>(p, concurrency, tile_ctas);
+  // enough CTAs that the token and item passes are short; each repeats the batch scan
+  const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 32;
+  // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
+  const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
+  plan_kernel<<<ctas, 1024, smem, stream>>>(p, concurrency, tile_ctas);
   return cudaGetLastError();
 }
 
@@ -749,10 +875,12 @@ cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtenso
               : launch_split_t<false, 64>(p, kmap, vmap, num_sms, stream, pdl);
 }
 
-cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream, bool pdl) {
+cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,
+                           bool pdl) {
   const int64_t warps = static_cast<int64_t>(p.T) * p.H_q;
   if (warps == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((warps * 32 + 255) / 256));
+  const int64_t ctas = (warps + 7) / 8;  // 8 warps per CTA
+  const dim3 grid(static_cast<unsigned>(ctas < 4 * num_sms ? ctas : 4 * num_sms));
   if (p.D == 128)
     return bf16 ? launch_kernel(combine_kernel<true, 128>, grid, dim3(256), 0, stream, pdl, p)
                 : launch_kernel(combine_kernel<false, 128>, grid, dim3(256), 0, stream, pdl, p);

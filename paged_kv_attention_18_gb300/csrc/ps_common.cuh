@@ -230,6 +230,31 @@ __device__ __forceinline__ float pair_sum(uint32_t packed) {
   }
 }
 
+// a * b + c on two fp32 lanes in one packed instruction (sm_100 f32x2 arithmetic).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// s0 += low 16-bit value of the pair, s1 += high one: mixed-precision adds (a 16-bit
+// operand into an fp32 sum, exact widening), so no unpacking instructions are needed.
+template <bool kBF16>
+__device__ __forceinline__ void add_halves(float& s0, float& s1, uint32_t packed) {
+  if constexpr (kBF16)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(s0), "+f"(s1) : "r"(packed));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(s0), "+f"(s1) : "r"(packed));
+}
+
 // Both 16-bit halves of a packed pair multiplied by a, rounded back.
 template <bool kBF16>
 __device__ __forceinline__ uint32_t scale_pair(uint32_t packed, float a) {

@@ -21,7 +21,8 @@ struct AttnParams {
   float scale_log2;              // softmax scale * log2(e)
   // workspace
   // [0] split-kernel items, [1] their fetch counter, [2] pages per split, [3] partials,
-  // [4] tile-kernel items, [5] their fetch counter, [6] tile pages per split
+  // [4] tile-kernel items, [5] their fetch counter, [6] tile pages per split,
+  // [7] tokens whose rows are split (entries of tok_list)
   int* hdr;
   WorkItem* items;               // [cap_items] split-kernel work (decode rows)
   int* seq_off;                  // [B + 1] first split-kernel item of each sequence
@@ -31,6 +32,9 @@ struct AttnParams {
   int tpt;                       // query tokens per 128-row tile (0: no tile kernel)
   int* tok_ns;                   // [T] splits holding each token's rows (0 = none)
   int* tok_base;                 // [T] first partial entry of each token
+  int* seq_off_p;                // [B + 1] first partial entry of each sequence
+  int* seq_off_s;                // [B + 1] first tok_list entry of each sequence
+  int* tok_list;                 // [T] the tokens whose rows are split, for the combine
   float* part_lse;               // [cap_part] log2-sum-exp of each partial
   float* part_o;                 // [cap_part, D] normalised partial outputs
   int cap_items, cap_part;
@@ -83,7 +87,8 @@ cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtenso
                                    const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
                                    bool pdl);
 
-cudaError_t launch_combine(const AttnParams& p, bool bf16, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,
+                           bool pdl);
 
 // Workspace bytes before the split partials (header, work lists, per-token tables);
 // `headroom` reserves work-list room for splitting long contexts.

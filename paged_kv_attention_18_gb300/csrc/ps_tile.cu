@@ -12,13 +12,15 @@
 // j <= p: PageServe section 01; tinyserve "How it works") and grouped-query attention
 // (tinyserve "Highlights" table).
 //
-// Warp roles (384 threads): warp 0 issues TMA and hands out work items (the page copies of
-// a K/V tile are spread over its 32 lanes); warp 1 owns TMEM and issues the MMAs (warps 2,
-// 3 idle); warps 4..7 (query tile A) and 8..11 (query tile B) are two softmax groups, one
-// TMEM lane (one query row) per thread (a warp reaches the 32 TMEM lanes of its warp index
-// mod 4). While one group computes its exponentials the tensor core works on the other
-// group's products. P is written back over S in TMEM and read from there by the PV
-// product. O is rescaled lazily, only when a row's running max grows by more than 2^8.
+// Warp roles (384 threads): warp 0 hands out work items and loads Q and K (three K stages,
+// freed as soon as both S products have read them); warp 2 loads V (two stages); the page
+// copies of a tile are spread over the lanes, one TMA copy per lane. Warp 1 owns TMEM and
+// one of its threads issues the MMAs (warp 3 idle). Warps 4..7 (query tile A) and 8..11
+// (query tile B) are two softmax groups, one TMEM lane (one query row) per thread (a warp
+// reaches the 32 TMEM lanes of its warp index mod 4). While one group computes its
+// exponentials the tensor core works on the other group's products. P is written back
+// over S in TMEM and read from there by the PV product. O is rescaled lazily, only when a
+// row's running max grows by more than 2^8.
 #include "ps_common.cuh"
 #include "ps_launch.h"
 #include "ps_tc05.cuh"
@@ -31,7 +33,8 @@ constexpr int kRows = 128;        // query rows per tile (MMA M)
 constexpr int kKeys = 128;        // keys per KV tile (MMA N of S, K of PV) = 8 pages
 constexpr int kPagesPerTile = kKeys / kBlockSize;
 constexpr int kSub = kRows * 128; // bytes of one [128 rows x 64 elements] swizzled sub-tile
-constexpr int kStages = 2;        // K/V tile stages
+constexpr int kKStages = 3;       // K tile stages (freed once both products S have read them)
+constexpr int kVStages = 2;       // V tile stages (freed once both products PV have read them)
 constexpr int kItemRing = 4;
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
@@ -40,6 +43,7 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2
 template <bool kBF16>
 constexpr float kMoveLog2 = kBF16 ? 64.f : 15.f;
 constexpr uint32_t kTmemCols = 512;
+
 // TMEM columns of softmax group g: S (and P over it) at g*256, O at g*256 + 128
 __host__ __device__ constexpr uint32_t col_s(int g) { return g * 256u; }
 __host__ __device__ constexpr uint32_t col_o(int g) { return g * 256u + 128u; }
@@ -47,18 +51,19 @@ __host__ __device__ constexpr uint32_t col_o(int g) { return g * 256u + 128u; }
 template <int D>
 struct TileSmem {
   static constexpr int kQ = (D / 64) * kSub;  // one query tile
-  static constexpr int kK = (D / 64) * kSub;  // K tile (128 keys)
-  static constexpr int kStage = 2 * kK;       // K + V
+  static constexpr int kK = (D / 64) * kSub;  // one K or V tile (128 keys)
   static constexpr int kOffQ = 0;             // query tiles A, B
-  static constexpr int kOffKV = kOffQ + 2 * kQ;
-  static constexpr int kOffBar = kOffKV + kStages * kStage;
-  static constexpr int kBytes = kOffBar + 256 + 1024;  // barriers, ring; alignment slack
+  static constexpr int kOffK = kOffQ + 2 * kQ;
+  static constexpr int kOffV = kOffK + kKStages * kK;
+  static constexpr int kOffBar = kOffV + kVStages * kK;
+  static constexpr int kBytes = kOffBar + 512 + 1024;  // barriers, ring; alignment slack
 };
 static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
 
 struct TileBars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t mma_final;
   uint64_t item_full[kItemRing], item_empty[kItemRing];
@@ -66,7 +71,7 @@ struct TileBars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(TileBars) <= 256, "barrier block");
+static_assert(sizeof(TileBars) <= 512, "barrier block");
 
 }  // namespace
 
@@ -88,14 +93,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   TileBars* bars = reinterpret_cast<TileBars*>(smem + L::kOffBar);
   const uint32_t sQ = smem_u32(smem + L::kOffQ);
-  const uint32_t sKV = smem_u32(smem + L::kOffKV);
+  const uint32_t sK = smem_u32(smem + L::kOffK);
+  const uint32_t sV = smem_u32(smem + L::kOffV);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&bars->s_full[g], 1);
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 9);  // the MMA warp and the 8 softmax warps
+      mbar_init(&bars->item_empty[s], 10);  // V producer, MMA warp, the 8 softmax warps
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -142,64 +152,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     return idx;
   };
 
-  if (warp == 0) {
-    // ============================ producer ==========================================
+  if (warp == 0 || warp == 2) {
+    // ===================== producers: warp 0 (items, Q, K), warp 2 (V) ================
+    const bool is_k = warp == 0;
     if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(is_k ? &kmap : &vmap);
+      if (is_k) tma_prefetch_desc(&qmap);
     }
+    const int n_stages = is_k ? kKStages : kVStages;
     uint32_t g = 0, qi = 0;
     for (int it = 0;; ++it) {
-      const int slot = it % kItemRing;
-      if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
       int idx = 0;
-      if (lane == 0) {
-        idx = atomicAdd(p.hdr + 5, 1);
-        if (idx >= n_items) idx = -1;
-        bars->item_idx[slot] = idx;
-        mbar_arrive(&bars->item_full[slot]);
+      if (is_k) {
+        const int slot = it % kItemRing;
+        if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
+        if (lane == 0) {
+          idx = atomicAdd(p.hdr + 5, 1);
+          if (idx >= n_items) idx = -1;
+          bars->item_idx[slot] = idx;
+          mbar_arrive(&bars->item_full[slot]);
+        }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      } else {
+        idx = next_item(it);
       }
-      idx = __shfl_sync(0xffffffffu, idx, 0);
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
       const int seq = w.seq, kv = w.kv;
-      const bool has_b = w.pad[0] > 0;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-      // query tiles: whole tokens x the G heads of this KV head
-      if (!wait(&bars->q_empty, (qi & 1) ^ 1)) break;
-      if (lane == 0) {
-        const int tok = w.tok0 + w.row0 / p.G;
-        const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
-        mbar_arrive_expect_tx(&bars->q_full, has_b ? 2 * tile_bytes : tile_bytes);
-        for (int q = 0; q < (has_b ? 2 : 1); ++q)
-          for (int h = 0; h < kHalves; ++h)
-            tma_load_3d(smem + L::kOffQ + q * L::kQ + h * kSub, &qmap, &bars->q_full, h * 64,
-                        kv * p.G, tok + q * p.tpt);
+      if (is_k) {
+        // query tiles: whole tokens x the G heads of this KV head
+        const bool has_b = w.pad[0] > 0;
+        if (!wait(&bars->q_empty, (qi & 1) ^ 1)) break;
+        if (lane == 0) {
+          const int tok = w.tok0 + w.row0 / p.G;
+          const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
+          mbar_arrive_expect_tx(&bars->q_full, has_b ? 2 * tile_bytes : tile_bytes);
+          for (int q = 0; q < (has_b ? 2 : 1); ++q)
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_3d(smem + L::kOffQ + q * L::kQ + h * kSub, &qmap, &bars->q_full,
+                          h * 64, kv * p.G, tok + q * p.tpt);
+        }
+        ++qi;
       }
-      ++qi;
-      // K/V tiles, 8 pages each; pages past the split read the zero fill
+      // K (or V) tiles of 8 pages; pages past the split read the zero fill. One lane per
+      // page copy: lane = page * kHalves + half (64-element half of the head).
       const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
       int bt_base = -1000, bt_reg = -1;
       bool ok = true;
+      const int pp = lane / kHalves, h = lane % kHalves;
       for (int j = 0; j < nt; ++j) {
         const int first = pb + j * kPagesPerTile;
         if (first - bt_base + kPagesPerTile > 32) {
           bt_base = first;
           bt_reg = first + lane < pe ? __ldg(bt + first + lane) : -1;
         }
-        const uint32_t st = g % kStages;
-        if (!wait(&bars->kv_empty[st], ((g / kStages) & 1) ^ 1)) { ok = false; break; }
-        // one lane per copy: lane = page * 4 + tensor * 2 + half (K/V, 64-element half)
-        constexpr int kCopies = kPagesPerTile * 2 * kHalves;
-        const int pp = lane / (2 * kHalves), tensor = (lane / kHalves) & 1, h = lane % kHalves;
+        const uint32_t st = g % n_stages;
+        uint64_t* empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
+        uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
+        if (!wait(empty, ((g / n_stages) & 1) ^ 1)) { ok = false; break; }
         const int blk = __shfl_sync(0xffffffffu, bt_reg, (first - bt_base + pp) & 31);
-        uint8_t* kdst = smem + L::kOffKV + st * L::kStage;
-        if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[st], L::kStage);
+        uint8_t* dst = smem + (is_k ? L::kOffK : L::kOffV) + st * L::kK;
+        if (lane == 0) mbar_arrive_expect_tx(full, L::kK);
         __syncwarp();
-        if (lane < kCopies) {
+        if (lane < kPagesPerTile * kHalves) {
           int row;
           if (first + pp >= pe) {
             row = p.num_blocks * kBlockSize;  // past the pool: zero fill, no HBM read
@@ -209,91 +227,112 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             row = blk * kBlockSize;
           }
-          tma_load_2d(kdst + tensor * L::kK + h * kSub + pp * (kBlockSize * 128),
-                      tensor ? &vmap : &kmap, &bars->kv_full[st], kv * D + h * 64, row);
+          tma_load_2d(dst + h * kSub + pp * (kBlockSize * 128), is_k ? &kmap : &vmap, full,
+                      kv * D + h * 64, row);
         }
         ++g;
       }
       if (!ok) break;
     }
   } else if (warp == 1) {
-    // ============================ MMA issuer ========================================
-    constexpr uint32_t idS = idesc_f16(kBF16, kRows, kKeys, false);
-    constexpr uint32_t idPV = idesc_f16(kBF16, kRows, D, true);
-    uint32_t g = 0, qi = 0, pc[2] = {0, 0}, act[2] = {0, 0};
-    bool ok = true;
-    for (int it = 0; ok; ++it) {
-      const int idx = next_item(it);
-      if (idx < 0) break;
-      const WorkItem& w = p.tile_items[idx];
-      const int pb = w.page_begin, pe = w.page_end;
-      if (pe <= pb) continue;
-      const bool has_b = w.pad[0] > 0;
-      const int ng = has_b ? 2 : 1;
-      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-      if (!wait(&bars->q_full, qi & 1)) break;
-      const uint32_t g0 = g;
-      // S of query tile `grp` against K tile j
-      auto issue_s = [&](int grp, int j) -> bool {
-        const uint32_t st = (g0 + j) % kStages;
-        if (!wait(&bars->kv_full[st], ((g0 + j) / kStages) & 1)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kbase = sKV + st * L::kStage;
-          const uint32_t qbase = sQ + grp * L::kQ;
+    // ============================ MMA issuer (one thread) ===========================
+    // Issuing one tcgen05.mma occupies the thread for nearly as long as the tensor core
+    // takes to run it (M128 N128 K16), so this loop is kept lean: lane 0 alone, with
+    // descriptors formed as a base plus constant offsets and waits without warp votes.
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(kBF16, kRows, kKeys, false);
+      constexpr uint32_t idPV = idesc_f16(kBF16, kRows, D, true);
+      // bounded single-thread wait; the abort flag is read only on the slow path
+      auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        for (uint32_t i = 0; i < (1u << 24); ++i) {
+          if (*abort_flag) return false;
+          if (mbar_try_wait(bar, parity)) return true;
+        }
+        record_error(p.err, kDevWaitTimeout);
+        *abort_flag = 1;
+        return false;
+      };
+      // descriptor start addresses stay below 2^18 bytes, so offsets added to the 14-bit
+      // start field (address / 16) never carry into the next field
+      const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t qdesc1 = sdesc_sw128(sQ + L::kQ, 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(sV, kSub, 1024);
+      uint32_t g = 0, qi = 0, pc[2] = {0, 0}, act[2] = {0, 0};
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int slot = it % kItemRing;
+        if (!wait1(&bars->item_full[slot], (it / kItemRing) & 1)) break;
+        const int idx = bars->item_idx[slot];
+        mbar_arrive(&bars->item_empty[slot]);
+        if (idx < 0) break;
+        const WorkItem& w = p.tile_items[idx];
+        const int pb = w.page_begin, pe = w.page_end;
+        if (pe <= pb) continue;
+        const bool has_b = w.pad[0] > 0;
+        const int ng = has_b ? 2 : 1;
+        const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
+        if (!wait1(&bars->q_full, qi & 1)) break;
+        const uint32_t g0 = g;
+        // S of query tile `grp` against K tile j
+        auto issue_s = [&](int grp, int j) -> bool {
+          const uint32_t st = (g0 + j) % kKStages;
+          if (!wait1(&bars->k_full[st], ((g0 + j) / kKStages) & 1)) return false;
+          tc_fence_after();
+          const uint64_t a0 = grp ? qdesc1 : qdesc0;
+          const uint64_t b0 = kdesc0 + ((st * L::kK) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(qbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(kbase + (kk / 4) * kSub + (kk % 4) * 32, 16, 1024);
-            umma_f16(tmem + col_s(grp), a, b, idS, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk / 4) * kSub + (kk % 4) * 32) >> 4;
+            umma_f16(tmem + col_s(grp), a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->s_full[grp]);
-          if (j == nt - 1 && grp == ng - 1) umma_commit(&bars->q_empty);  // Q no longer needed
-        }
-        __syncwarp();
-        return true;
-      };
-      // O of query tile `grp` += P V of K/V tile j
-      auto issue_pv = [&](int grp, int j) -> bool {
-        if (!wait(&bars->p_full[grp], pc[grp] & 1)) return false;
-        ++pc[grp];
-        // the previous item's epilogue of this group has read its O
-        if (j == 0 && !wait(&bars->o_free[grp], (act[grp] & 1) ^ 1)) return false;
-        tc_fence_after();
-        const uint32_t st = (g0 + j) % kStages;
-        if (lane == 0) {
-          const uint32_t vbase = sKV + st * L::kStage + L::kK;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t b = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
-            umma_f16_ts(tmem + col_o(grp), tmem + col_s(grp) + kk * 8, b, idPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+          if (grp == ng - 1) {  // last reader of the K stage
+            umma_commit(&bars->k_empty[st]);
+            if (j == nt - 1) umma_commit(&bars->q_empty);  // Q no longer needed
           }
-          if (grp == ng - 1) umma_commit(&bars->kv_empty[st]);  // last reader of the stage
+          return true;
+        };
+        // O of query tile `grp` += P V of K/V tile j
+        auto issue_pv = [&](int grp, int j) -> bool {
+          if (!wait1(&bars->p_full[grp], pc[grp] & 1)) return false;
+          ++pc[grp];
+          // the previous item's epilogue of this group has read its O
+          if (j == 0 && !wait1(&bars->o_free[grp], (act[grp] & 1) ^ 1)) return false;
+          const uint32_t st = (g0 + j) % kVStages;
+          if (!wait1(&bars->v_full[st], ((g0 + j) / kVStages) & 1)) return false;
+          tc_fence_after();
+          const uint64_t b0 = vdesc0 + ((st * L::kK) >> 4);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            umma_f16_ts(tmem + col_o(grp), tmem + col_s(grp) + kk * 8, b0 + ((kk * 2048) >> 4),
+                        idPV, kk > 0 ? 1u : acc0);
+          if (grp == ng - 1) umma_commit(&bars->v_empty[st]);  // last reader of the V stage
+          return true;
+        };
+        for (int q = 0; q < ng && ok; ++q) ok = issue_s(q, 0);
+        // per K/V tile: PV of A, next S of A, PV of B, next S of B. A query tile's next S
+        // overwrites its P in TMEM, so it is issued after that tile's PV (in order).
+        for (int j = 0; j < nt && ok; ++j)
+          for (int q = 0; q < ng && ok; ++q) {
+            ok = issue_pv(q, j);
+            if (ok && j + 1 < nt) ok = issue_s(q, j + 1);
+          }
+        if (!ok) break;
+        for (int q = 0; q < ng; ++q) {
+          umma_commit(&bars->o_done[q]);
+          ++act[q];
         }
-        __syncwarp();
-        return true;
-      };
-      for (int q = 0; q < ng && ok; ++q) ok = issue_s(q, 0);
-      // per K/V tile: PV of A, next S of A, PV of B, next S of B. A query tile's next S
-      // overwrites its P in TMEM, so it is issued after that tile's PV (in order).
-      for (int j = 0; j < nt && ok; ++j)
-        for (int q = 0; q < ng && ok; ++q) {
-          ok = issue_pv(q, j);
-          if (ok && j + 1 < nt) ok = issue_s(q, j + 1);
-        }
-      if (!ok) break;
-      if (lane == 0)
-        for (int q = 0; q < ng; ++q) umma_commit(&bars->o_done[q]);
-      __syncwarp();
-      for (int q = 0; q < ng; ++q) ++act[q];
-      g += nt;
-      ++qi;
+        g += nt;
+        ++qi;
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      umma_commit(&bars->mma_final);
+      mbar_wait(&bars->mma_final, 0, 1u << 22);
     }
-    // every MMA issued by this thread has completed before TMEM is released
-    if (lane == 0) umma_commit(&bars->mma_final);
     __syncwarp();
-    mbar_wait(&bars->mma_final, 0, 1u << 22);
   } else if (warp >= 4) {
     // ============================ softmax groups + epilogue =========================
     const int grp = (warp - 4) >> 2;   // 0: query tile A, 1: query tile B
@@ -396,12 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
           uint32_t pk[32];
           float lq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums
+          // scale and subtract two scores per packed fma; the row sum adds the 16-bit P
+          // values the MMA sees, widened exactly by mixed-precision adds
+          const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
           for (int e = 0; e < 64; e += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(v[e]), sl2, neg_m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), sl2, neg_m));
-            pk[e / 2] = pack2<kBF16>(p0, p1);
-            lq[(e / 2) & 3] += pair_sum<kBF16>(pk[e / 2]);  // the row sum uses the P the MMA sees
+            const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                   sl2x2, nm2);
+            pk[e / 2] = pack2<kBF16>(fast_exp2(x.x), fast_exp2(x.y));
+            const int c = ((e / 2) & 1) * 2;
+            add_halves<kBF16>(lq[c], lq[c + 1], pk[e / 2]);
           }
           l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
           tmem_st16(tS + 32 * h, pk);

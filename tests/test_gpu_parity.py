@@ -103,6 +103,36 @@ def test_verify_rows_many_splits():
     check_workload(wl)
 
 
+def test_batch_larger_than_planner_staging():
+    # more than 4096 sequences: the planner keeps its per-sequence offsets in global memory
+    # (one CTA); a few long decodes split, so the combine's token list is exercised too
+    rng = np.random.default_rng(41)
+    seqs = [(int(L), 1) for L in rng.integers(1, 48, size=5000)]
+    seqs += [(int(L), int(n)) for L, n in zip(rng.integers(3000, 6000, size=6),
+                                              rng.integers(1, 4, size=6))]
+    wl = W.simple_workload("wide", seed=41, dtype="bf16", H_q=12, H_kv=2, D=128, seqs=seqs)
+    rng_rows = np.random.default_rng(42)
+
+    def rows(i, st):
+        qsl = st.query_start_loc
+        r = list(range(int(qsl[-7]), st.T))  # every row of the long sequences
+        return sorted(set(r + _sample_rows(st, 200, rng_rows)))
+
+    check_workload(wl, rows_for_step=rows)
+
+
+def test_planner_grid_sizes():
+    # token and sequence counts around the planner's per-CTA shares, with split decodes
+    for B, seed in ((31, 51), (33, 52), (1025, 53)):
+        rng = np.random.default_rng(seed)
+        seqs = [(int(L), 1) for L in rng.integers(200, 2500, size=B)]
+        seqs[0] = (seqs[0][0], min(seqs[0][0], 700))  # one prefill chunk among them
+        wl = W.simple_workload(f"grid{B}", seed=seed, dtype="f16", H_q=8, H_kv=2, D=64,
+                               seqs=seqs)
+        rr = np.random.default_rng(seed + 100)
+        check_workload(wl, rows_for_step=lambda i, st: _sample_rows(st, 64, rr, extra_rows=200))
+
+
 # ------------------------------------------------------------------------------------
 # edge cases
 # ------------------------------------------------------------------------------------
