@@ -61,7 +61,7 @@ struct TileSmem {
 static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
 
 struct TileBars {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];  // query tiles A and B, each freed after its last S
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
@@ -97,8 +97,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sV = smem_u32(smem + L::kOffV);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->q_empty[q], 1);
+    }
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) tma_prefetch_desc(&qmap);
     }
     const int n_stages = is_k ? kKStages : kVStages;
-    uint32_t g = 0, qi = 0;
+    uint32_t g = 0, qa = 0, qb = 0;
     for (int it = 0;; ++it) {
       int idx = 0;
       if (is_k) {
@@ -183,19 +185,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int seq = w.seq, kv = w.kv;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       if (is_k) {
-        // query tiles: whole tokens x the G heads of this KV head
+        // query tiles: whole tokens x the G heads of this KV head. Each tile has its own
+        // buffer, refilled as soon as that tile's last S of the previous item has read it.
         const bool has_b = w.pad[0] > 0;
-        if (!wait(&bars->q_empty, (qi & 1) ^ 1)) break;
-        if (lane == 0) {
-          const int tok = w.tok0 + w.row0 / p.G;
-          const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
-          mbar_arrive_expect_tx(&bars->q_full, has_b ? 2 * tile_bytes : tile_bytes);
-          for (int q = 0; q < (has_b ? 2 : 1); ++q)
+        const int tok = w.tok0 + w.row0 / p.G;
+        const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
+        bool qok = true;
+        for (int q = 0; q < (has_b ? 2 : 1); ++q) {
+          if (!wait(&bars->q_empty[q], ((q ? qb : qa) & 1) ^ 1)) {
+            qok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->q_full[q], tile_bytes);
             for (int h = 0; h < kHalves; ++h)
-              tma_load_3d(smem + L::kOffQ + q * L::kQ + h * kSub, &qmap, &bars->q_full,
+              tma_load_3d(smem + L::kOffQ + q * L::kQ + h * kSub, &qmap, &bars->q_full[q],
                           h * 64, kv * p.G, tok + q * p.tpt);
+          }
         }
-        ++qi;
+        if (!qok) break;
+        ++qa;
+        if (has_b) ++qb;
       }
       // K (or V) tiles of 8 pages; pages past the split read the zero fill. One lane per
       // page copy: lane = page * kHalves + half (64-element half of the head).
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc1 = sdesc_sw128(sQ + L::kQ, 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(sV, kSub, 1024);
-      uint32_t g = 0, qi = 0, pc[2] = {0, 0}, act[2] = {0, 0};
+      uint32_t g = 0, qa = 0, qb = 0, pc[2] = {0, 0}, act[2] = {0, 0};
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int slot = it % kItemRing;
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_b = w.pad[0] > 0;
         const int ng = has_b ? 2 : 1;
         const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-        if (!wait1(&bars->q_full, qi & 1)) break;
+        if (!wait1(&bars->q_full[0], qa & 1)) break;
         const uint32_t g0 = g;
         // S of query tile `grp` against K tile j
         auto issue_s = [&](int grp, int j) -> bool {
@@ -288,10 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f16(tmem + col_s(grp), a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->s_full[grp]);
-          if (grp == ng - 1) {  // last reader of the K stage
-            umma_commit(&bars->k_empty[st]);
-            if (j == nt - 1) umma_commit(&bars->q_empty);  // Q no longer needed
-          }
+          if (j == nt - 1) umma_commit(&bars->q_empty[grp]);  // last read of this Q tile
+          if (grp == ng - 1) umma_commit(&bars->k_empty[st]);  // last reader of the K stage
           return true;
         };
         // O of query tile `grp` += P V of K/V tile j
@@ -312,7 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (grp == ng - 1) umma_commit(&bars->v_empty[st]);  // last reader of the V stage
           return true;
         };
-        for (int q = 0; q < ng && ok; ++q) ok = issue_s(q, 0);
+        for (int q = 0; q < ng && ok; ++q) {
+          if (q == 1 && !wait1(&bars->q_full[1], qb & 1)) {
+            ok = false;
+            break;
+          }
+          ok = issue_s(q, 0);
+        }
         // per K/V tile: PV of A, next S of A, PV of B, next S of B. A query tile's next S
         // overwrites its P in TMEM, so it is issued after that tile's PV (in order).
         for (int j = 0; j < nt && ok; ++j)
@@ -326,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++act[q];
         }
         g += nt;
-        ++qi;
+        ++qa;
+        if (ng > 1) ++qb;
       }
       // every MMA issued by this thread has completed before TMEM is released
       umma_commit(&bars->mma_final);
