@@ -266,16 +266,38 @@ class DeviceWorkload:
         pool_bytes = 2 * wl.k_pool.nbytes
         self.flush_buf = (torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=device)
                           if pool_bytes < 2 * L2_BYTES else None)
+        self.graphs = None  # set by capture()
 
     def flush_l2(self):
         if self.flush_buf is not None:
             self.flush_buf.fill_(1)
 
-    def run_one(self, d):
+    def run_one(self, d, eager=False):
         from paged_kv_attention_18_gb300 import binding
+        if self.graphs is not None and not eager:
+            d["graph"].replay()
+            return
         binding.attention_step(d["q"], d["k"], d["v"], self.k_pool, self.v_pool, d["bt"],
                                d["sl"], d["qsl"], self.wl.scale, out=d["out"],
                                workspace=d["ws"], slot_buf=d["slots"])
+
+    def capture(self):
+        """Capture each engine step in its own CUDA graph (after one eager run)."""
+        import torch
+        self.run_eager()
+        torch.cuda.synchronize()
+        for d in self.steps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                self.run_one(d, eager=True)
+            d["graph"] = g
+        self.graphs = True
+        torch.cuda.synchronize()
+
+    def run_eager(self):
+        for d in self.steps:
+            self.flush_l2()
+            self.run_one(d, eager=True)
 
     def run(self):
         for d in self.steps:
@@ -330,7 +352,7 @@ def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
     hook_steps = min(steps, 200)
     binding.profile_begin(hook_steps * len(dw.steps))
     for _ in range(hook_steps):
-        dw.run()
+        dw.run_eager()  # the timing hook sees eager launches only
     torch.cuda.synchronize()
     prof = binding.profile_end()
     # keep the same load running until the clock sampler has seen enough of it
@@ -398,6 +420,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     tokens = sum(w["tokens"] for w in work)
     flops = sum(w["flops"] for w in work)
     dw = DeviceWorkload(wl, device)
+    if args.graph:
+        dw.capture()
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 and not args.no_clocks \
         else None
     ms, prof, hook_steps, clk = time_device(dw, args.steps, args.warmup, world, device, clocks,
@@ -489,7 +513,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
                           f"L2 flushed before every engine step ({4 * L2_BYTES / 1e6:.0f} MB "
                           f"buffer written, outside the timed events): the "
                           f"{2 * wl.k_pool.nbytes / 1e6:.0f} MB KV pool fits in L2"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": ("each engine step replayed from a CUDA graph (captured once)"
+                              if args.graph else "eager launches through the C ABI")},
         "gpu_launches": int(sum(n for _, n in prof.values()) * args.steps // hook_steps),
         "roofline": roofline,
         "mixed_batch": mixed,
@@ -498,6 +524,85 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "clocks": clk,
     }
     return result
+
+
+# ------------------------------------------------------------------------------------
+# other operations on the pool: block copies (copy-on-write, swap out / in)
+# ------------------------------------------------------------------------------------
+def time_events(fn, steps: int, warmup: int) -> float:
+    """Mean ms of fn() over `steps` calls, CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_copy_blocks(args, rank, world, local_rank) -> dict | None:
+    """Copy-on-write of 8192 blocks inside the decode workload's pool (device to device),
+    and a swap of 4096 blocks out to a pinned host pool and back in."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_attention_18_gb300 import binding
+    torch.cuda.set_device(local_rank)
+    peaks, peaks_src = load_peaks()
+    wl = make_workload("qwen15b_decode", rank)
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    k = W.to_device(wl.k_pool, wl.dtype, "cuda")
+    v = W.to_device(wl.v_pool, wl.dtype, "cuda")
+    nb = wl.num_blocks
+    block_bytes = 16 * wl.H_kv * wl.D * 2
+    rng = np.random.default_rng(90 + rank)
+    n_cow = 8192
+    perm = rng.permutation(nb)
+    src = torch.tensor(perm[:n_cow].astype(np.int32), device="cuda")
+    dst = torch.tensor(perm[n_cow:2 * n_cow].astype(np.int32), device="cuda")
+    ms_cow = time_events(lambda: binding.copy_blocks(k, v, k, v, src, dst), args.steps,
+                         args.warmup)
+    cow_bytes = 2 * 2 * n_cow * block_bytes  # read + write, K and V
+    n_swap = 4096
+    hk = torch.empty((n_swap, 16, wl.H_kv, wl.D), dtype=dt).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    host_ids = torch.arange(n_swap, dtype=torch.int32, device="cuda")
+    dev_ids = torch.tensor(rng.choice(nb, n_swap, replace=False).astype(np.int32), device="cuda")
+    swap_steps = max(3, min(args.steps, 50))
+    ms_out = time_events(lambda: binding.copy_blocks(k, v, hk, hv, dev_ids, host_ids),
+                         swap_steps, args.warmup)
+    ms_in = time_events(lambda: binding.copy_blocks(hk, hv, k, v, host_ids, dev_ids),
+                        swap_steps, args.warmup)
+    if binding.device_error() != 0:
+        raise RuntimeError("device error word set during the block-copy benchmark")
+    ms_cow = reduce_max(ms_cow, world)
+    swap_bytes = 2 * n_swap * block_bytes  # K and V moved once over the host link
+    gbs = world * cow_bytes / (ms_cow / 1e3) / 1e9
+    if rank != 0:
+        return None
+    return {
+        "metric": "KV block copy-on-write GB/s (read + write)", "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_cow,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (the decode workload's pool; random block pairs)",
+        "config": {"workload": f"copy {n_cow} blocks of {block_bytes} B (K and V) inside the "
+                               f"{2 * nb * block_bytes / 1e6:.0f} MB decode pool",
+                   "l2": "pool larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / world / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "copy_blocks_kernel", "peak_source": f"{peaks_src} (hbm_gbs)"},
+        "swap": {"blocks": n_swap, "bytes": swap_bytes,
+                 "out_gbs": swap_bytes / (ms_out / 1e3) / 1e9,
+                 "in_gbs": swap_bytes / (ms_in / 1e3) / 1e9,
+                 "note": "device pool <-> pinned host pool in one kernel over the host link "
+                         "(no measured link peak, so no roofline)"},
+        "gpu_launches": args.steps,
+    }
 
 
 # ------------------------------------------------------------------------------------
@@ -551,6 +656,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["step", "copy_blocks"], default="step",
+                    help="step: the attention step (default); copy_blocks: block copies")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture each engine step in a CUDA graph and time its replays")
     ap.add_argument("--no-clocks", action="store_true",
                     help="no nvidia-smi sampling and no extra load after the timed steps")
     args = ap.parse_args(argv)
@@ -574,6 +683,8 @@ def main(argv=None):
         world_eff = 1
     if args.impl == "reference":
         res = run_reference(args, 0 if world_eff == 1 else rank, world)
+    elif args.op == "copy_blocks":
+        res = run_copy_blocks(args, rank, world_eff, local_rank)
     else:
         res = run_ours(args, rank, world_eff, local_rank)
     if res is not None:

@@ -106,6 +106,32 @@ int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
                          int dtype, void* stream);
 
 /*
+ * ps_copy_blocks -- copy whole KV blocks between pools, bit-exact.
+ *
+ * Copy-on-write of a block that several block tables share, before one of them writes
+ * into it (tinyserve "How it works"; "Highlights" table, paged KV-cache row), and the
+ * swap of a preempted sequence's blocks to a pinned host pool and back (PageServe
+ * section 04 "Phase 9 · Preemption"; tinyserve "How it works": swapped KV is lossless).
+ *
+ *   src_k, src_v   [src_num_blocks, 16, H_kv, D] of dtype: the source pools.
+ *   dst_k, dst_v   [dst_num_blocks, 16, H_kv, D] of dtype: the destination pools, updated
+ *                  in place. Source and destination may be the same pools (copy-on-write)
+ *                  or different ones. Each pool may be DEVICE memory or PINNED HOST memory
+ *                  (page-locked and mapped, e.g. cudaHostAlloc): the kernel reads and
+ *                  writes it through unified addressing, so a swap out or in is one call.
+ *   src_ids, dst_ids  int32 [n], device-accessible (device or pinned host memory): for
+ *                  every i, block dst_ids[i] of both destination pools becomes a copy of
+ *                  block src_ids[i] of the source pools (all 16 x H_kv x D values).
+ * The pairs are copied concurrently: destination ids must be distinct and no block may be
+ * both a source and a destination of one call (otherwise the result is unspecified). An
+ * id outside its pool records PS_DEV_BAD_BLOCK_ID and that pair is skipped. n = 0 is a
+ * no-op.
+ */
+int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k,
+                   void* dst_v, int dst_num_blocks, const int32_t* src_ids,
+                   const int32_t* dst_ids, int n, int H_kv, int D, int dtype, void* stream);
+
+/*
  * ps_paged_attention_workspace_size -- bytes of device workspace ps_paged_attention wants
  * for a batch of at most T packed tokens, B sequences and contexts of at most
  * max_seq_len tokens. A smaller workspace (at least the size returned for
@@ -232,8 +258,8 @@ const char* ps_status_string(int status);
  * here, not in the timed calls). ps_profile_end() waits for the recorded events and
  * stops recording. ps_profile_read(kind, &ms, &launches) then gives the summed device
  * time and the launch count of one kind: 0 slot mapping, 1 KV scatter, 2 planner,
- * 3 split attention (decode rows), 4 split combine, 5 tile attention (prefill and verify
- * rows, tcgen05).
+ * 3 split attention (decode and verify rows), 4 split combine, 5 tile attention (prefill
+ * rows, tcgen05), 6 block copy, 7 speculative acceptance, 8 rotary KV scatter.
  */
 int ps_profile_begin(int max_launches_per_kind);
 int ps_profile_end(void);

@@ -5,6 +5,6 @@ may import this package. The CUDA library never imports it, and it imports nothi
 from the library.
 """
 from .paged_kv_oracle import (  # noqa: F401
-    BLOCK_SIZE, attention_step, causal_softmax_attention, decode_bits, gather_context,
+    BLOCK_SIZE, attention_step, causal_softmax_attention, copy_blocks, decode_bits, gather_context,
     kv_head_of, paged_attention, query_positions, reshape_and_cache, slot_mapping, slot_of,
 )

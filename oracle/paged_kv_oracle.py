@@ -110,6 +110,27 @@ def reshape_and_cache(k: np.ndarray, v: np.ndarray, slots: np.ndarray,
 # --------------------------------------------------------------------------- #
 # attention
 # --------------------------------------------------------------------------- #
+# --------------------------------------------------------------------------- #
+# block copies (copy-on-write, swap out / in)
+# --------------------------------------------------------------------------- #
+def copy_blocks(src_pool: np.ndarray, dst_pool: np.ndarray, src_ids, dst_ids) -> np.ndarray:
+    """A copy of dst_pool in which block dst_ids[i] holds block src_ids[i] of src_pool.
+
+    Every pair reads the source as it was before the call. This is the copy-on-write of
+    a block shared by several tables before one of them writes into it (tinyserve "How
+    it works"; "Highlights" table, paged KV-cache row) and the lossless swap of a
+    preempted sequence's blocks to a pinned host pool and back (PageServe section 04
+    "Phase 9 - Preemption"; tinyserve "How it works"). A pair with an id outside its
+    pool is skipped.
+    """
+    src = np.asarray(src_pool)
+    out = np.array(dst_pool, copy=True)
+    for s, d in zip(np.asarray(src_ids).tolist(), np.asarray(dst_ids).tolist()):
+        if 0 <= s < src.shape[0] and 0 <= d < out.shape[0]:
+            out[d] = src[s]
+    return out
+
+
 def kv_head_of(h: int, H_q: int, H_kv: int) -> int:
     """KV head read by query head h: consecutive query heads share one KV head."""
     return h // (H_q // H_kv)

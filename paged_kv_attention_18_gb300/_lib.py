@@ -21,6 +21,8 @@ _p = c_void_p  # every pointer argument is passed as an address
 SIGNATURES = {
     "ps_slot_mapping": (c_int, [_p, c_int, _p, _p, c_int, c_int, c_int, _p, _p]),
     "ps_reshape_and_cache": (c_int, [_p, _p, _p, _p, _p, c_int, c_int, c_int, c_int, c_int, _p]),
+    "ps_copy_blocks": (c_int, [_p, _p, c_int, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
+                               _p]),
     "ps_paged_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "ps_paged_attention": (c_int, [_p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
                                    c_int, c_int, c_float, _p, _p, c_size_t, c_int, _p]),

@@ -19,7 +19,8 @@ BLOCK_SIZE = 16
 
 # kernel kinds of the timing hook
 PROFILE_KINDS = {"slot_mapping": 0, "reshape_and_cache": 1, "plan": 2, "split_attention": 3,
-                 "combine": 4, "tile_attention": 5}
+                 "combine": 4, "tile_attention": 5, "copy_blocks": 6, "spec_accept": 7,
+                 "rope_reshape_and_cache": 8}
 
 
 class PagedServeError(RuntimeError):
@@ -92,6 +93,42 @@ def reshape_and_cache(k, v, slot_mapping_t, k_pool, v_pool, stream=None) -> None
     _check(lib().ps_reshape_and_cache(kp, vp, sp, kpp, vpp, T, H_kv, D, k_pool.shape[0],
                                       DTYPE_CODE[k.dtype], _stream(stream)),
            "ps_reshape_and_cache")
+
+
+def _mem(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
+    """Pointer to a CUDA tensor or a pinned host tensor (device-addressable memory)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if not t.is_contiguous():
+            raise PagedServeError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype and not (isinstance(dtype, tuple) and t.dtype in dtype):
+            raise PagedServeError(f"{name} has dtype {t.dtype}")
+        if ndim is not None and t.dim() != ndim:
+            raise PagedServeError(f"{name} must have {ndim} dimensions")
+        return t.data_ptr()
+    return _dev(t, name, dtype, ndim)
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids, stream=None) -> None:
+    """Copy whole blocks between pools (ps_copy_blocks): block dst_ids[i] of (dst_k, dst_v)
+    becomes block src_ids[i] of (src_k, src_v). Pools are CUDA or pinned host tensors
+    [num_blocks, 16, H_kv, D]; ids are int32 CUDA (or pinned) tensors of equal length."""
+    dt = tuple(DTYPE_CODE)
+    skp = _mem(src_k, "src_k", dt, 4)
+    svp = _mem(src_v, "src_v", src_k.dtype, 4)
+    dkp = _mem(dst_k, "dst_k", src_k.dtype, 4)
+    dvp = _mem(dst_v, "dst_v", src_k.dtype, 4)
+    sip = _mem(src_ids, "src_ids", torch.int32, 1)
+    dip = _mem(dst_ids, "dst_ids", torch.int32, 1)
+    if src_k.shape != src_v.shape or dst_k.shape != dst_v.shape or \
+            tuple(src_k.shape[1:]) != tuple(dst_k.shape[1:]) or src_ids.shape != dst_ids.shape:
+        raise PagedServeError("copy_blocks: inconsistent shapes")
+    _, bs, H_kv, D = src_k.shape
+    if bs != BLOCK_SIZE:
+        raise PagedServeError("copy_blocks: pools must have 16-row blocks")
+    _check(lib().ps_copy_blocks(skp, svp, src_k.shape[0], dkp, dvp, dst_k.shape[0], sip, dip,
+                                src_ids.shape[0], H_kv, D, DTYPE_CODE[src_k.dtype],
+                                _stream(stream)),
+           "ps_copy_blocks")
 
 
 def workspace_size(T: int, B: int, H_q: int, H_kv: int, D: int, max_seq_len: int) -> int:

@@ -60,7 +60,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------------
 // timing hook
 // ---------------------------------------------------------------------------------
-constexpr int kKinds = 6;
+constexpr int kKinds = 9;
 struct Profile {
   bool on = false;
   int cap = 0;
@@ -344,6 +344,26 @@ int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
   return cuda_status(ps::launch_reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, T, H_kv, D,
                                                   num_blocks, ds->err, ds->num_sms, s),
                      "KV scatter kernel");
+}
+
+int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k,
+                   void* dst_v, int dst_num_blocks, const int32_t* src_ids,
+                   const int32_t* dst_ids, int n, int H_kv, int D, int dtype, void* stream) {
+  int rc = check_shapes(H_kv, H_kv, D, dtype);
+  if (rc) return rc;
+  if (n < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PS_ERR_ARG;
+  if (n == 0) return PS_OK;
+  if (!src_k || !src_v || !dst_k || !dst_v || !src_ids || !dst_ids) return PS_ERR_ARG;
+  if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+    return PS_ERR_ALIGN;
+  DeviceState* ds;
+  if ((rc = current_device_state(&ds))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timed tm(6, s);
+  return cuda_status(ps::launch_copy_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v,
+                                            dst_num_blocks, src_ids, dst_ids, n, H_kv, D,
+                                            ds->err, ds->num_sms, s),
+                     "block copy kernel");
 }
 
 size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,

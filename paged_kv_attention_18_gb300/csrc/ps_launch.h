@@ -69,6 +69,13 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
                                      int num_blocks, int* err, int num_sms, cudaStream_t stream,
                                      bool pdl = false);
 
+// Copy n whole blocks (16 rows x H_kv x D, K and V): dst block dst_ids[i] of (dst_k, dst_v)
+// gets src block src_ids[i] of (src_k, src_v). Pools may be device or pinned host memory.
+cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks,
+                               void* dst_k, void* dst_v, int dst_num_blocks,
+                               const int32_t* src_ids, const int32_t* dst_ids, int n, int H_kv,
+                               int D, int* err, int num_sms, cudaStream_t stream);
+
 // Number of resident attention CTAs and warps per CTA the split kernel uses.
 int attention_ctas(int D, int num_sms);
 int attention_warps(int D);

@@ -336,9 +336,59 @@ def pin_fp32_close_to_fp64(o, seed=19):
     assert np.abs(a - b).max() < 1e-5
 
 
+# --------------------------------------------------------------------------- #
+# block copies: copy-on-write and swap (contexts read through tables are unchanged)
+# --------------------------------------------------------------------------- #
+def pin_copy_on_write_keeps_contexts(o, seed=20):
+    """tinyserve's figure: seq A [7, 2] and seq B [7, 5] share block 7. Copying block 7
+    to a free block and pointing B's table at the copy must leave every sequence's
+    context, read through its table, exactly as it was, and change no other block."""
+    rng = np.random.default_rng(seed)
+    nb, H, D = 10, 2, 4
+    pool = f16(rng.standard_normal((nb, BS, H, D)))
+    tables = {"A": [7, 2], "B": [7, 5]}
+    before = {n: o.gather_context(pool, np.array(t), 2 * BS) for n, t in tables.items()}
+    free = 9
+    after_pool = o.copy_blocks(pool, pool, [7], [free])
+    new_tables = {"A": [7, 2], "B": [free, 5]}
+    for n, t in new_tables.items():
+        assert np.array_equal(o.gather_context(after_pool, np.array(t), 2 * BS), before[n]), n
+    others = [b for b in range(nb) if b != free]
+    assert np.array_equal(after_pool[others], pool[others])
+    # several pairs at once, one of them reading block 0, read the pool before the call
+    pairs_src, pairs_dst = [0, 3, 7], [8, 9, 1]
+    out = o.copy_blocks(pool, pool, pairs_src, pairs_dst)
+    for s_, d_ in zip(pairs_src, pairs_dst):
+        assert np.array_equal(out[d_], pool[s_])
+    keep = [b for b in range(nb) if b not in pairs_dst]
+    assert np.array_equal(out[keep], pool[keep])
+
+
+def pin_swap_round_trip(o, seed=21):
+    """A sequence's blocks swapped out to a host pool and back into other blocks: its
+    context through the remapped table is bit-identical (the pages: swapped KV is
+    lossless), and host blocks outside the swap keep their contents."""
+    rng = np.random.default_rng(seed)
+    H, D, L = 2, 8, 70
+    ctx = f16(rng.standard_normal((L, H, D)))
+    table = [4, 0, 11, 6, 2]
+    dev = place_paged(ctx, table, 12, f16(rng.standard_normal((12, BS, H, D))))
+    sentinel = np.full((6, BS, H, D), 0x7BFF, dtype=np.uint16)
+    host_ids = [3, 0, 5, 1, 4]
+    host = o.copy_blocks(dev, sentinel, table, host_ids)
+    assert np.array_equal(host[2], sentinel[2])  # not part of the swap
+    back_ids = [1, 7, 3, 9, 10]
+    dev2 = o.copy_blocks(host, np.zeros_like(dev), host_ids, back_ids)
+    assert np.array_equal(o.gather_context(dev2, np.array(back_ids), L), ctx)
+    # a pair with an id outside its pool is skipped
+    out = o.copy_blocks(dev, sentinel, [12, 0], [0, 6])
+    assert np.array_equal(out, sentinel)
+
+
 ALL_PINS = [
     pin_slots_golden, pin_slots_brute_force, pin_scatter_roundtrip, pin_golden_tiny,
     pin_closed_forms, pin_gqa_mapping, pin_softmax_rows, pin_matches_library_sdpa,
     pin_block_permutation_invariance, pin_prefix_sharing_invariance,
     pin_ragged_equals_per_sequence, pin_fp32_close_to_fp64,
+    pin_copy_on_write_keeps_contexts, pin_swap_round_trip,
 ]

@@ -32,6 +32,9 @@ MUTANTS = [
     ("reshape_and_cache", "vp[s] = v[t]", "vp[s] = k[t]"),
     ("reshape_and_cache", "if s < 0:", "if s <= 0:"),
     ("decode_bits", "<< 16", "<< 15"),
+    ("copy_blocks", "out[d] = src[s]", "out[s] = src[d]"),
+    ("copy_blocks", "out[d] = src[s]", "out[d] = out[s]"),
+    ("copy_blocks", "if 0 <= s < src.shape[0]", "if 0 < s < src.shape[0]"),
 ]
 
 
