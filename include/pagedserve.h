@@ -68,7 +68,8 @@ typedef enum {
   PS_DEV_BAD_SLOT = 2,       /* a slot_mapping entry >= num_blocks * 16                */
   PS_DEV_BAD_SEQUENCE = 3,   /* query count > context, or context beyond the table     */
   PS_DEV_WAIT_TIMEOUT = 4,   /* a kernel's bounded wait ran out (the kernel returned)  */
-  PS_DEV_PLAN_OVERFLOW = 5   /* the work plan did not fit the workspace                */
+  PS_DEV_PLAN_OVERFLOW = 5,  /* the work plan did not fit the workspace                */
+  PS_DEV_BAD_TOKEN = 6       /* a draft token id outside [0, V)                          */
 } ps_device_error;
 
 /*
@@ -130,6 +131,47 @@ int ps_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
 int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k,
                    void* dst_v, int dst_num_blocks, const int32_t* src_ids,
                    const int32_t* dst_ids, int n, int H_kv, int D, int dtype, void* stream);
+
+/*
+ * ps_spec_accept -- speculative-decoding acceptance after the verify pass.
+ *
+ * tinyserve "How it works" (speculative decoding): draft d_i is accepted with probability
+ * min(1, p_i(d_i) / q_i(d_i)); at the first rejection the replacement is drawn from
+ * normalize(max(p_i - q_i, 0)); if all k drafts survive, a bonus token is drawn from the
+ * last target distribution. The greedy rule (temperature 0) accepts a draft while it
+ * equals argmax p_i and emits argmax p_i at the first mismatch, or argmax p_k when all
+ * match. Randomness is an input, and every decision is fixed to a precision, so the tokens
+ * are reproducible:
+ *   - acceptance of draft i: (double)R_i * (double)q_i(d_i) < (double)p_i(d_i) * 2^32,
+ *     each product rounded once in fp64 (q = 1 when draft_probs is null);
+ *   - residual weights w = max(p - q, 0) in fp32 (q the one-hot of the draft token when
+ *     draft_probs is null; w = p for the bonus row), as integers W = trunc(w * 2^40);
+ *   - the sample is the first token v whose running sum W_0 + ... + W_v exceeds
+ *     floor(R_k * Z / 2^32), Z the sum of all W (if Z = 0, the same draw from p itself);
+ *   - argmax ties go to the lowest token.
+ *
+ *   target_probs  float [B, k + 1, V]: p_0 .. p_k of each sequence (the verify rows).
+ *   draft_probs   float [B, k, V]: q_0 .. q_{k-1}, or NULL for a deterministic proposer
+ *                 (n-gram drafts: q is the one-hot of the draft token).
+ *   draft_tokens  int32 [B, k]; an id outside [0, V) records PS_DEV_BAD_TOKEN and counts
+ *                 as rejected, its replacement drawn from p alone.
+ *   random_bits   uint32 [B, k + 1]: R_0 .. R_{k-1} for the acceptance tests, R_k for the
+ *                 final draw; may be NULL when greedy != 0.
+ *   out_tokens    int32 [B, k + 1], written: the accepted drafts, then the replacement or
+ *                 bonus token, then -1.
+ *   num_accepted  int32 [B], written: accepted drafts (0 .. k); num_accepted + 1 tokens
+ *                 are emitted.
+ *   workspace     device scratch of ps_spec_accept_workspace_size(B, k, V) bytes,
+ *                 256-byte aligned.
+ * Probabilities are expected in [0, 1]; other values give unspecified tokens, never a
+ * fault. B = 0 is a no-op; k = 0 draws one token from p_0; k > 31 returns
+ * PS_ERR_UNSUPPORTED.
+ */
+size_t ps_spec_accept_workspace_size(int B, int k, int V);
+int ps_spec_accept(const float* target_probs, const float* draft_probs,
+                   const int32_t* draft_tokens, const uint32_t* random_bits, int B, int k, int V,
+                   int greedy, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /*
  * ps_paged_attention_workspace_size -- bytes of device workspace ps_paged_attention wants

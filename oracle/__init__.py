@@ -8,3 +8,4 @@ from .paged_kv_oracle import (  # noqa: F401
     BLOCK_SIZE, attention_step, causal_softmax_attention, copy_blocks, decode_bits, gather_context,
     kv_head_of, paged_attention, query_positions, reshape_and_cache, slot_mapping, slot_of,
 )
+from .spec_oracle import spec_accept  # noqa: F401,E402

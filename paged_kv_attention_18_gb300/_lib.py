@@ -23,6 +23,9 @@ SIGNATURES = {
     "ps_reshape_and_cache": (c_int, [_p, _p, _p, _p, _p, c_int, c_int, c_int, c_int, c_int, _p]),
     "ps_copy_blocks": (c_int, [_p, _p, c_int, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
                                _p]),
+    "ps_spec_accept_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "ps_spec_accept": (c_int, [_p, _p, _p, _p, c_int, c_int, c_int, c_int, _p, _p, _p, c_size_t,
+                               _p]),
     "ps_paged_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "ps_paged_attention": (c_int, [_p, _p, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
                                    c_int, c_int, c_float, _p, _p, c_size_t, c_int, _p]),

@@ -131,6 +131,42 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids, stream=None) -> No
            "ps_copy_blocks")
 
 
+def spec_accept(target_probs, draft_tokens, random_bits=None, draft_probs=None,
+                greedy: bool = False, workspace=None, stream=None):
+    """Speculative acceptance (ps_spec_accept). target_probs float32 [B, k+1, V];
+    draft_tokens int32 [B, k]; random_bits int32 [B, k+1] holding uint32 words (or None
+    when greedy); draft_probs float32 [B, k, V] or None. Returns (out_tokens [B, k+1],
+    num_accepted [B]) as int32 CUDA tensors."""
+    pp = _dev(target_probs, "target_probs", torch.float32, 3)
+    B, k1, V = target_probs.shape
+    k = k1 - 1
+    if draft_tokens.shape != (B, k):
+        raise PagedServeError("spec_accept: draft_tokens shape")
+    dp = _dev(draft_tokens, "draft_tokens", torch.int32, 2) if k > 0 else None
+    qp = None
+    if draft_probs is not None:
+        if draft_probs.shape != (B, k, V):
+            raise PagedServeError("spec_accept: draft_probs shape")
+        qp = _dev(draft_probs, "draft_probs", torch.float32, 3)
+    rp = None
+    if random_bits is not None:
+        if random_bits.shape != (B, k + 1):
+            raise PagedServeError("spec_accept: random_bits shape")
+        rp = _dev(random_bits, "random_bits", torch.int32, 2)
+    elif not greedy:
+        raise PagedServeError("spec_accept: random_bits required unless greedy")
+    out = torch.empty((B, k + 1), dtype=torch.int32, device=target_probs.device)
+    num = torch.empty((B,), dtype=torch.int32, device=target_probs.device)
+    if workspace is None:
+        n = max(int(lib().ps_spec_accept_workspace_size(B, k, V)), 256)
+        workspace = torch.empty(n, dtype=torch.uint8, device=target_probs.device)
+    wp = _dev(workspace, "workspace", torch.uint8, 1)
+    _check(lib().ps_spec_accept(pp, qp, dp, rp, B, k, V, 1 if greedy else 0, _dev(out, "out"),
+                                _dev(num, "num"), wp, workspace.numel(), _stream(stream)),
+           "ps_spec_accept")
+    return out, num
+
+
 def workspace_size(T: int, B: int, H_q: int, H_kv: int, D: int, max_seq_len: int) -> int:
     return int(lib().ps_paged_attention_workspace_size(T, B, H_q, H_kv, D, max_seq_len))
 

@@ -366,6 +366,54 @@ int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, voi
                      "block copy kernel");
 }
 
+size_t ps_spec_accept_workspace_size(int B, int k, int V) {
+  if (B < 0 || k < 0 || V <= 0) return 0;
+  const size_t c = static_cast<size_t>(ps::spec_chunks(V));
+  const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
+  return ps::up256(static_cast<size_t>(B) * c * 8) + 2 * ps::up256(rows * 4) +
+         ps::up256(static_cast<size_t>(B) * 4);
+}
+
+int ps_spec_accept(const float* target_probs, const float* draft_probs,
+                   const int32_t* draft_tokens, const uint32_t* random_bits, int B, int k, int V,
+                   int greedy, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (B < 0 || k < 0 || V <= 0) return PS_ERR_ARG;
+  if (k > 31) return PS_ERR_UNSUPPORTED;  // one lane per draft decides the acceptance
+  if (B == 0) return PS_OK;
+  if (!target_probs || !out_tokens || !num_accepted) return PS_ERR_ARG;
+  if (k > 0 && !draft_tokens) return PS_ERR_ARG;
+  if (!greedy && !random_bits) return PS_ERR_ARG;
+  const size_t need = ps_spec_accept_workspace_size(B, k, V);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return PS_ERR_WORKSPACE;
+  DeviceState* ds;
+  int rc = current_device_state(&ds);
+  if (rc) return rc;
+  const size_t c = static_cast<size_t>(ps::spec_chunks(V));
+  const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ps::SpecParams a = {};
+  a.p = target_probs;
+  a.q = draft_probs;
+  a.drafts = draft_tokens;
+  a.rnd = random_bits;
+  a.B = B;
+  a.k = k;
+  a.V = V;
+  a.greedy = greedy ? 1 : 0;
+  a.out = out_tokens;
+  a.num = num_accepted;
+  a.wsum = reinterpret_cast<long long*>(ws);
+  a.amax_v = reinterpret_cast<float*>(ws + ps::up256(static_cast<size_t>(B) * c * 8));
+  a.amax_i = reinterpret_cast<int*>(ws + ps::up256(static_cast<size_t>(B) * c * 8) + ps::up256(rows * 4));
+  a.acc = reinterpret_cast<int*>(ws + ps::up256(static_cast<size_t>(B) * c * 8) + 2 * ps::up256(rows * 4));
+  a.err = ds->err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timed tm(7, s);
+  return cuda_status(ps::launch_spec_accept(a, s), "speculative acceptance kernels");
+}
+
 size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
                                          int max_seq_len) {
   if (T < 0 || B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || (D != 64 && D != 128))

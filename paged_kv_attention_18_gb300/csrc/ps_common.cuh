@@ -29,6 +29,7 @@ enum DevError : int {
   kDevBadSequence = 3,    // query count > context, or context beyond the block table
   kDevWaitTimeout = 4,    // an mbarrier wait ran out of iterations
   kDevPlanOverflow = 5,   // the work plan did not fit the workspace
+  kDevBadToken = 6,       // a draft token id outside the vocabulary
 };
 
 // Programmatic dependent launch: let the next kernel on the stream start launching, and

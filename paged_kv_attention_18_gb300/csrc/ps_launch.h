@@ -76,6 +76,25 @@ cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, int src_num
                                const int32_t* src_ids, const int32_t* dst_ids, int n, int H_kv,
                                int D, int* err, int num_sms, cudaStream_t stream);
 
+// Speculative acceptance (rejection rule or greedy) of every sequence's k drafts.
+struct SpecParams {
+  const float* p;          // [B, k + 1, V] target probabilities of the verify rows
+  const float* q;          // [B, k, V] draft probabilities, or null (one-hot drafts)
+  const int32_t* drafts;   // [B, k]
+  const uint32_t* rnd;     // [B, k + 1] random words (rejection rule only)
+  int B, k, V, greedy;
+  int chunks, chunk;       // vocabulary chunks (set by the launcher)
+  int32_t* out;            // [B, k + 1] accepted drafts, the final token, then -1
+  int32_t* num;            // [B] accepted drafts
+  long long* wsum;         // [B, chunks] workspace: fixed-point residual sums
+  float* amax_v;           // [B, k + 1, chunks] workspace: chunk maxima (greedy)
+  int* amax_i;             // [B, k + 1, chunks] workspace: their tokens
+  int* acc;                // [B] workspace: accepted drafts | plain << 8 | invalid << 9
+  int* err;
+};
+int spec_chunks(int V);
+cudaError_t launch_spec_accept(const SpecParams& a, cudaStream_t stream);
+
 // Number of resident attention CTAs and warps per CTA the split kernel uses.
 int attention_ctas(int D, int num_sms);
 int attention_warps(int D);

@@ -1,0 +1,107 @@
+"""Speculative acceptance through the C ABI vs the CPU oracle: the accepted-draft counts
+and every emitted token must be identical (the decisions are fixed to a precision)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_18_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+U32 = 2 ** 32
+
+
+def _softmax(x):
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def make_case(B, k, V, seed, near=0.7, peak=2.0):
+    """Target rows p, draft rows q near p, drafts drawn from q, random words."""
+    rng = np.random.default_rng(seed)
+    lt = rng.standard_normal((B, k + 1, V)).astype(np.float32) * peak
+    p = _softmax(lt)
+    q = _softmax(lt[:, :k] * near + rng.standard_normal((B, k, V)).astype(np.float32))
+    cq = np.cumsum(q.astype(np.float64), axis=-1)
+    u = rng.random((B, k, 1))
+    drafts = np.minimum((cq <= u).sum(axis=-1), V - 1).astype(np.int32)
+    rnd = rng.integers(0, U32, size=(B, k + 1), dtype=np.uint64).astype(np.uint32)
+    return p, q, drafts, rnd
+
+
+def run(p, drafts, rnd, q=None, greedy=False):
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    r = None if rnd is None else dev(rnd.view(np.int32))
+    out, num = binding.spec_accept(dev(p), dev(drafts), r, None if q is None else dev(q),
+                                   greedy=greedy)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), num.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,k,V", [(64, 4, 1000), (37, 3, 3001), (20, 4, 8197), (9, 1, 50000)])
+@pytest.mark.parametrize("mode", ["draft_model", "ngram", "greedy"])
+def test_matches_oracle(B, k, V, mode):
+    p, q, drafts, rnd = make_case(B, k, V, seed=B + k + V, peak=6.0 if mode == "ngram" else 2.0)
+    if mode == "ngram":
+        # a deterministic proposer: half of the drafts on the target's most likely token
+        am = p.argmax(axis=-1)[:, :k]
+        pick = np.random.default_rng(V).random((B, k)) < 0.5
+        drafts = np.where(pick, am, drafts).astype(np.int32)
+    if mode == "greedy":
+        # plant argmax-equal drafts for part of the batch so acceptance runs vary
+        am = p.argmax(axis=-1)[:, :k]
+        drafts = np.where(np.arange(B)[:, None] % 3 == 0, am, drafts).astype(np.int32)
+        got = run(p, drafts, None, greedy=True)
+        ref = oracle.spec_accept(p, drafts, greedy=True)
+    else:
+        qq = q if mode == "draft_model" else None
+        got = run(p, drafts, rnd, qq)
+        ref = oracle.spec_accept(p, drafts, rnd, qq)
+    assert binding.device_error() == 0
+    np.testing.assert_array_equal(got[1], ref[1])
+    np.testing.assert_array_equal(got[0], ref[0])
+    if mode != "greedy":
+        assert 0 < ref[1].mean() < k  # both accepting and rejecting paths ran
+
+
+def test_full_vocabulary_batch():
+    # 132 sequences x (4 drafts + bonus) over a 151936-token vocabulary
+    B, k, V = 132, 4, 151936
+    p, q, drafts, rnd = make_case(B, k, V, seed=5, near=0.9)
+    got = run(p, drafts, rnd, q)
+    ref = oracle.spec_accept(p, drafts, rnd, q)
+    assert binding.device_error() == 0
+    np.testing.assert_array_equal(got[1], ref[1])
+    np.testing.assert_array_equal(got[0], ref[0])
+
+
+def test_edges():
+    # k = 0: one draw from p_0
+    p, q, drafts, rnd = make_case(16, 0, 777, seed=8)
+    got = run(p, np.zeros((16, 0), np.int32), rnd)
+    ref = oracle.spec_accept(p, np.zeros((16, 0), np.int32), rnd)
+    np.testing.assert_array_equal(got[0], ref[0])
+    assert (got[1] == 0).all()
+    # an invalid draft id: error code, counted as rejected, replacement drawn from p
+    p, q, drafts, rnd = make_case(8, 3, 500, seed=9)
+    drafts[3, 1] = 500
+    drafts[5, 0] = -2
+    rnd[:, :3] = 0  # every valid draft accepted
+    got = run(p, drafts, rnd, q)
+    assert binding.device_error() == 6  # PS_DEV_BAD_TOKEN
+    ref = oracle.spec_accept(p, drafts, rnd, q)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+    # no residual mass (every positive difference below 2^-40): the draw falls back to p
+    V = 64
+    p = np.full((4, 2, V), 1.0 / V, np.float32)
+    p[:, 0, 5] = 0.0
+    q = p[:, :1].copy()
+    q[:, 0, 0] += np.float32(2.0 ** -27)   # q(d) > p(d): the draft can be rejected
+    p[:, 0, 5] = np.float32(2.0 ** -45)    # the only positive residual, below 2^-40
+    drafts = np.zeros((4, 1), np.int32)
+    rnd = np.array([[U32 - 1, r] for r in (0, 2 ** 30, 2 ** 31, U32 - 1)], np.uint64).astype(np.uint32)
+    got = run(p, drafts, rnd, q)
+    ref = oracle.spec_accept(p, drafts, rnd, q)
+    assert (ref[1] == 0).all()
+    np.testing.assert_array_equal(got[0], ref[0])

@@ -3,7 +3,13 @@ import numpy as np
 import pytest
 
 import oracle
-from tests import pins
+import oracle.spec_oracle
+from tests import pins, spec_pins
+
+
+@pytest.mark.parametrize("pin", spec_pins.SPEC_PINS, ids=lambda p: p.__name__)
+def test_spec_pin(pin):
+    pin(oracle.spec_oracle)
 
 
 @pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)

@@ -11,7 +11,8 @@ import textwrap
 import pytest
 
 import oracle.paged_kv_oracle as O
-from tests import pins
+import oracle.spec_oracle as S
+from tests import pins, spec_pins
 
 MUTANTS = [
     ("slot_of", "* BLOCK_SIZE + pos % BLOCK_SIZE", "* (BLOCK_SIZE - 1) + pos % BLOCK_SIZE"),
@@ -38,10 +39,24 @@ MUTANTS = [
 ]
 
 
-def _mutated(name, old, new):
-    src = textwrap.dedent(inspect.getsource(getattr(O, name)))
+SPEC_MUTANTS = [
+    ("accepts", "float(R) * float(np.float32(qv)) < float(np.float32(pv)) * 4294967296.0",
+     "float(R) * float(np.float32(pv)) < float(np.float32(qv)) * 4294967296.0"),
+    ("spec_accept", "np.maximum(p[b, a] - qr, np.float32(0))",
+     "np.maximum(qr - p[b, a], np.float32(0))"),
+    ("spec_accept", "                w = p[b, a]\n", "                w = p[b, 0]\n"),
+    ("spec_accept", "qv = 1.0 if q is None else q[b, i, d]", "qv = 1.0"),
+    ("spec_accept", "if not accepts(int(rnd[b, i]), p[b, i, d], qv):",
+     "if accepts(int(rnd[b, i]), p[b, i, d], qv):"),
+    ("spec_accept", "int(np.argmax(p[b, a]))", "int(np.argmin(p[b, a]))"),
+    ("draw", "t = (int(R) * Z) >> 32", "t = (int(R) * Z) >> 33"),
+]
+
+
+def _mutated(name, old, new, mod=O):
+    src = textwrap.dedent(inspect.getsource(getattr(mod, name)))
     assert src.count(old) == 1, (name, old)
-    ns = dict(vars(O))
+    ns = dict(vars(mod))
     exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
     return ns[name]
 
@@ -53,6 +68,18 @@ def test_mutant_is_caught(monkeypatch, name, old, new):
     for pin in pins.ALL_PINS:
         try:
             pin(O)
+        except Exception as e:  # an assertion or a crash both count as caught
+            failed.append((pin.__name__, type(e).__name__))
+    assert failed, f"no pin caught the mutant {name}: {old!r} -> {new!r}"
+
+
+@pytest.mark.parametrize("name,old,new", SPEC_MUTANTS, ids=[f"{m[0]}:{m[2]}" for m in SPEC_MUTANTS])
+def test_spec_mutant_is_caught(monkeypatch, name, old, new):
+    monkeypatch.setattr(S, name, _mutated(name, old, new, S))
+    failed = []
+    for pin in spec_pins.SPEC_PINS:
+        try:
+            pin(S)
         except Exception as e:  # an assertion or a crash both count as caught
             failed.append((pin.__name__, type(e).__name__))
     assert failed, f"no pin caught the mutant {name}: {old!r} -> {new!r}"
