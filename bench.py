@@ -623,6 +623,49 @@ def run_copy_blocks(args, rank, world, local_rank) -> dict | None:
     }
 
 
+def run_rope_cache(args, rank, world, local_rank) -> dict | None:
+    """Rotary embedding of q (in place) and k, fused with the KV scatter, for 32768 new
+    tokens at Qwen2.5-1.5B attention shapes (12/2 heads, D 128, bf16, theta 10^6)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_attention_18_gb300 import binding
+    torch.cuda.set_device(local_rank)
+    peaks, peaks_src = load_peaks()
+    T, H_q, H_kv, D, nb = 32768, 12, 2, 128, 2304
+    dev = torch.device("cuda", local_rank)
+    g = torch.Generator(dev).manual_seed(97 + rank)
+    q = torch.randn((T, H_q, D), device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn((T, H_kv, D), device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn((T, H_kv, D), device=dev, generator=g).to(torch.bfloat16)
+    kp = torch.zeros((nb, 16, H_kv, D), device=dev, dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    rng = np.random.default_rng(97 + rank)
+    pos = torch.tensor(rng.integers(0, 32768, T).astype(np.int32), device=dev)
+    slots = torch.tensor(rng.permutation(nb * 16)[:T].astype(np.int32), device=dev)
+    ms = reduce_max(time_events(lambda: binding.rope_reshape_and_cache(q, k, v, pos, slots, kp, vp, 1e6),
+                                args.steps, args.warmup, per_graph=10), world)
+    if binding.device_error() != 0:
+        raise RuntimeError("device error word set during the rotary scatter benchmark")
+    nbytes = T * (2 * H_q + 4 * H_kv) * D * 2 + 2 * T * 4  # q in and out, k, v in, pool rows out
+    gbs = world * nbytes / (ms / 1e3) / 1e9
+    if rank != 0:
+        return None
+    return {
+        "metric": "rotary KV scatter GB/s (q rotated in place, k rotated into the pool)",
+        "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (N(0,1) values, random slots)",
+        "config": {"workload": f"T={T} tokens, {H_q}/{H_kv} heads, D {D}, theta 1e6",
+                   "bytes_per_call": nbytes, "l2": f"{nbytes / 1e6:.0f} MB per call, larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / world / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "rope_reshape_and_cache_kernel",
+                     "peak_source": f"{peaks_src} (hbm_gbs)"},
+        "gpu_launches": args.steps,
+    }
+
+
 def run_spec_accept(args, rank, world, local_rank) -> dict | None:
     """Acceptance of 4 drafts for 132 sequences over a 151936-token vocabulary: the
     rejection rule with draft-model probabilities (the headline), with one-hot n-gram
@@ -733,9 +776,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["step", "copy_blocks", "spec_accept"], default="step",
+    ap.add_argument("--op", choices=["step", "copy_blocks", "spec_accept", "rope_cache"],
+                    default="step",
                     help="step: the attention step (default); copy_blocks: block copies; "
-                         "spec_accept: speculative acceptance")
+                         "spec_accept: speculative acceptance; rope_cache: rotary KV scatter")
     ap.add_argument("--graph", action="store_true",
                     help="capture each engine step in a CUDA graph and time its replays")
     ap.add_argument("--no-clocks", action="store_true",
@@ -765,6 +809,8 @@ def main(argv=None):
         res = run_copy_blocks(args, rank, world_eff, local_rank)
     elif args.op == "spec_accept":
         res = run_spec_accept(args, rank, world_eff, local_rank)
+    elif args.op == "rope_cache":
+        res = run_rope_cache(args, rank, world_eff, local_rank)
     else:
         res = run_ours(args, rank, world_eff, local_rank)
     if res is not None:

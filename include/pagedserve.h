@@ -133,6 +133,33 @@ int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, voi
                    const int32_t* dst_ids, int n, int H_kv, int D, int dtype, void* stream);
 
 /*
+ * ps_rope_reshape_and_cache -- rotary position embedding fused with the KV scatter.
+ *
+ * Every new token's query and key are rotated by its position before the key is cached
+ * (tinyserve "Highlights" table, forward-pass row: rotary embeddings in the Qwen2
+ * decoder; PageServe section 01: explicit position ids per packed token). Rotate-half
+ * form, for each head and frequency i < D/2, with a = positions[t] * rope_theta^(-2i/D):
+ *     x'[i]       = x[i] cos(a) - x[i + D/2] sin(a)
+ *     x'[i + D/2] = x[i + D/2] cos(a) + x[i] sin(a)
+ * The angle is formed and reduced in fp64, its cosine and sine taken in fp32, and each
+ * output rounded once to dtype: within one unit in the last place of the exact value
+ * plus 2^-20 (|x[i]| + |x[i + D/2]|), the fp32 cosine's share.
+ *
+ *   q             [T, H_q, D] of dtype, rotated IN PLACE.
+ *   k, v          [T, H_kv, D] of dtype (k is not modified).
+ *   positions     int32 [T]: position of each token.
+ *   slot_mapping  int32 [T]: as for ps_reshape_and_cache; the rotated key row and the V
+ *                 row go to the slot (a negative slot skips the token's K/V, a slot past
+ *                 the pool records PS_DEV_BAD_SLOT; q is rotated either way).
+ *   k_pool, v_pool [num_blocks, 16, H_kv, D] of dtype, updated in place.
+ *   rope_theta    the rotary base (> 1), e.g. 1e6 for Qwen2.5 models.
+ */
+int ps_rope_reshape_and_cache(void* q, const void* k, const void* v, const int32_t* positions,
+                              const int32_t* slot_mapping, void* k_pool, void* v_pool, int T,
+                              int H_q, int H_kv, int D, int num_blocks, float rope_theta,
+                              int dtype, void* stream);
+
+/*
  * ps_spec_accept -- speculative-decoding acceptance after the verify pass.
  *
  * tinyserve "How it works" (speculative decoding): draft d_i is accepted with probability

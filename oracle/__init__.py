@@ -6,6 +6,7 @@ from the library.
 """
 from .paged_kv_oracle import (  # noqa: F401
     BLOCK_SIZE, attention_step, causal_softmax_attention, copy_blocks, decode_bits, gather_context,
-    kv_head_of, paged_attention, query_positions, reshape_and_cache, slot_mapping, slot_of,
+    kv_head_of, paged_attention, query_positions, reshape_and_cache, rope, rope_reshape_and_cache,
+    slot_mapping, slot_of,
 )
 from .spec_oracle import spec_accept  # noqa: F401,E402

@@ -108,9 +108,6 @@ def reshape_and_cache(k: np.ndarray, v: np.ndarray, slots: np.ndarray,
 
 
 # --------------------------------------------------------------------------- #
-# attention
-# --------------------------------------------------------------------------- #
-# --------------------------------------------------------------------------- #
 # block copies (copy-on-write, swap out / in)
 # --------------------------------------------------------------------------- #
 def copy_blocks(src_pool: np.ndarray, dst_pool: np.ndarray, src_ids, dst_ids) -> np.ndarray:
@@ -131,6 +128,41 @@ def copy_blocks(src_pool: np.ndarray, dst_pool: np.ndarray, src_ids, dst_ids) ->
     return out
 
 
+# --------------------------------------------------------------------------- #
+# rotary position embedding (fused with the scatter in the library)
+# --------------------------------------------------------------------------- #
+def rope(x_bits: np.ndarray, positions, theta: float, dtype: str) -> np.ndarray:
+    """Rotary embedding of x [T, H, D] (16-bit bit patterns) by each token's position,
+    exact in float64: for frequency i < D/2, with a = pos * theta^(-2i/D),
+    x'[i] = x[i] cos a - x[i + D/2] sin a and x'[i + D/2] = x[i + D/2] cos a + x[i] sin a.
+
+    The Qwen2 decoder's rotary embeddings (tinyserve "Highlights" table, forward-pass
+    row) applied at the explicit position ids of the packed batch (PageServe section 01);
+    the pairing of element i with i + D/2 (rotate-half) is the plainest reading of a
+    Qwen2-style rotary embedding, which the pages name without a formula."""
+    x = decode_bits(x_bits, dtype)
+    D = x.shape[-1]
+    half = D // 2
+    inv_freq = float(theta) ** (-(2.0 * np.arange(half)) / D)
+    a = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
+    c, s = np.cos(a)[:, None, :], np.sin(a)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rope_reshape_and_cache(q, k, v, positions, slots, k_pool, v_pool, theta, dtype):
+    """The fused step: (rotated q, rotated k, v pool after the scatter) in float64 for q
+    and k; the K pool rows at the slots hold the rotated keys rounded to the 16-bit type,
+    which the caller compares within the rounding; the V pool is exact bits."""
+    q_rot = rope(q, positions, theta, dtype)
+    k_rot = rope(k, positions, theta, dtype)
+    _, v_out = reshape_and_cache(k, v, slots, k_pool, v_pool)
+    return q_rot, k_rot, v_out
+
+
+# --------------------------------------------------------------------------- #
+# attention
+# --------------------------------------------------------------------------- #
 def kv_head_of(h: int, H_q: int, H_kv: int) -> int:
     """KV head read by query head h: consecutive query heads share one KV head."""
     return h // (H_q // H_kv)

@@ -23,6 +23,8 @@ SIGNATURES = {
     "ps_reshape_and_cache": (c_int, [_p, _p, _p, _p, _p, c_int, c_int, c_int, c_int, c_int, _p]),
     "ps_copy_blocks": (c_int, [_p, _p, c_int, _p, _p, c_int, _p, _p, c_int, c_int, c_int, c_int,
                                _p]),
+    "ps_rope_reshape_and_cache": (c_int, [_p, _p, _p, _p, _p, _p, _p, c_int, c_int, c_int, c_int,
+                                          c_int, c_float, c_int, _p]),
     "ps_spec_accept_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "ps_spec_accept": (c_int, [_p, _p, _p, _p, c_int, c_int, c_int, c_int, _p, _p, _p, c_size_t,
                                _p]),

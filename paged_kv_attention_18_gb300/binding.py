@@ -131,6 +131,30 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids, stream=None) -> No
            "ps_copy_blocks")
 
 
+def rope_reshape_and_cache(q, k, v, positions, slot_mapping_t, k_pool, v_pool,
+                           rope_theta: float, stream=None) -> None:
+    """Rotate q [T, H_q, D] in place and k [T, H_kv, D] into the pools at the slots by each
+    token's position, copying v too (ps_rope_reshape_and_cache)."""
+    dt = tuple(DTYPE_CODE)
+    qp = _dev(q, "q", dt, 3)
+    kp = _dev(k, "k", q.dtype, 3)
+    vp = _dev(v, "v", q.dtype, 3)
+    pp = _dev(positions, "positions", torch.int32, 1)
+    sp = _dev(slot_mapping_t, "slot_mapping", torch.int32, 1)
+    kpp = _dev(k_pool, "k_pool", q.dtype, 4)
+    vpp = _dev(v_pool, "v_pool", q.dtype, 4)
+    T, H_q, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (T, H_kv, D) or v.shape != k.shape or positions.shape[0] != T or \
+            slot_mapping_t.shape[0] != T or tuple(k_pool.shape[1:]) != (BLOCK_SIZE, H_kv, D) \
+            or k_pool.shape != v_pool.shape:
+        raise PagedServeError("rope_reshape_and_cache: inconsistent shapes")
+    _check(lib().ps_rope_reshape_and_cache(qp, kp, vp, pp, sp, kpp, vpp, T, H_q, H_kv, D,
+                                           k_pool.shape[0], float(rope_theta),
+                                           DTYPE_CODE[q.dtype], _stream(stream)),
+           "ps_rope_reshape_and_cache")
+
+
 def spec_accept(target_probs, draft_tokens, random_bits=None, draft_probs=None,
                 greedy: bool = False, workspace=None, stream=None):
     """Speculative acceptance (ps_spec_accept). target_probs float32 [B, k+1, V];

@@ -4,6 +4,7 @@
 
 #include <cstdio>
 
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -364,6 +365,31 @@ int ps_copy_blocks(const void* src_k, const void* src_v, int src_num_blocks, voi
                                             dst_num_blocks, src_ids, dst_ids, n, H_kv, D,
                                             ds->err, ds->num_sms, s),
                      "block copy kernel");
+}
+
+int ps_rope_reshape_and_cache(void* q, const void* k, const void* v, const int32_t* positions,
+                              const int32_t* slot_mapping, void* k_pool, void* v_pool, int T,
+                              int H_q, int H_kv, int D, int num_blocks, float rope_theta,
+                              int dtype, void* stream) {
+  int rc = check_shapes(H_q, H_kv, D, dtype);
+  if (rc) return rc;
+  if (T < 0 || num_blocks <= 0 || !(rope_theta > 1.f) || !std::isfinite(rope_theta))
+    return PS_ERR_ARG;
+  if (static_cast<int64_t>(num_blocks) * PS_BLOCK_SIZE > INT32_MAX) return PS_ERR_ARG;
+  if (T == 0) return PS_OK;
+  if (!q || !k || !v || !positions || !slot_mapping || !k_pool || !v_pool) return PS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_pool) ||
+      !aligned16(v_pool))
+    return PS_ERR_ALIGN;
+  DeviceState* ds;
+  if ((rc = current_device_state(&ds))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timed tm(8, s);
+  return cuda_status(ps::launch_rope_reshape_and_cache(q, k, v, positions, slot_mapping, k_pool,
+                                                       v_pool, T, H_q, H_kv, D, num_blocks,
+                                                       rope_theta, dtype == PS_BF16, ds->err,
+                                                       ds->num_sms, s),
+                     "rotary KV scatter kernel");
 }
 
 size_t ps_spec_accept_workspace_size(int B, int k, int V) {

@@ -76,6 +76,14 @@ cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, int src_num
                                const int32_t* src_ids, const int32_t* dst_ids, int n, int H_kv,
                                int D, int* err, int num_sms, cudaStream_t stream);
 
+// Rotary embedding of q (in place) and k (into the pool at each token's slot) by position,
+// with the V rows copied to their slots.
+cudaError_t launch_rope_reshape_and_cache(void* q, const void* k, const void* v,
+                                          const int32_t* pos, const int32_t* slots,
+                                          void* k_pool, void* v_pool, int T, int H_q, int H_kv,
+                                          int D, int num_blocks, float theta, bool bf16,
+                                          int* err, int num_sms, cudaStream_t stream);
+
 // Speculative acceptance (rejection rule or greedy) of every sequence's k drafts.
 struct SpecParams {
   const float* p;          // [B, k + 1, V] target probabilities of the verify rows

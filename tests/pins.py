@@ -385,10 +385,54 @@ def pin_swap_round_trip(o, seed=21):
     assert np.array_equal(out, sentinel)
 
 
+# --------------------------------------------------------------------------- #
+# rotary embedding: identity at position 0, rotation (norm), relative positions, hand
+# cases with the frequencies written out
+# --------------------------------------------------------------------------- #
+def _bf16_bits(x):
+    from paged_kv_attention_18_gb300 import workloads as W
+    return W.round_to_bits(np.asarray(x, np.float32), "bf16")
+
+
+def pin_rope_identity_and_norm(o, seed=22):
+    rng = np.random.default_rng(seed)
+    x = _bf16_bits(rng.standard_normal((5, 3, 16)))
+    xv = o.decode_bits(x, "bf16")
+    r0 = o.rope(x, np.zeros(5, np.int32), 1e4, "bf16")
+    assert np.array_equal(r0, xv)  # cos 0 = 1, sin 0 = 0
+    r = o.rope(x, np.array([1, 7, 100, 4095, 32767]), 1e6, "bf16")
+    assert np.allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(xv, axis=-1), rtol=1e-12)
+
+
+def pin_rope_relative_position(o, seed=23):
+    """<rope(q, m), rope(k, n)> depends on m - n only: RoPE's defining property."""
+    rng = np.random.default_rng(seed)
+    q = _bf16_bits(rng.standard_normal((1, 1, 32)))
+    k = _bf16_bits(rng.standard_normal((1, 1, 32)))
+    for m, n, shift in ((5, 2, 11), (40, 39, 1000), (3, 17, 250)):
+        d0 = float(np.sum(o.rope(q, [m], 1e4, "bf16") * o.rope(k, [n], 1e4, "bf16")))
+        d1 = float(np.sum(o.rope(q, [m + shift], 1e4, "bf16") * o.rope(k, [n + shift], 1e4, "bf16")))
+        assert abs(d0 - d1) < 1e-9, (m, n, shift, d0, d1)
+
+
+def pin_rope_hand_cases(o):
+    """D = 4, theta = 10^4: frequencies 1 and 10^-2; element i pairs with i + 2."""
+    e0 = _bf16_bits([[[1, 0, 0, 0]]])
+    e1 = _bf16_bits([[[0, 1, 0, 0]]])
+    r0 = o.rope(e0, [3], 1e4, "bf16")[0, 0]
+    r1 = o.rope(e1, [3], 1e4, "bf16")[0, 0]
+    assert np.allclose(r0, [math.cos(3), 0, math.sin(3), 0], atol=1e-15)
+    assert np.allclose(r1, [0, math.cos(0.03), 0, math.sin(0.03)], atol=1e-15)
+    e2 = _bf16_bits([[[0, 0, 1, 0]]])  # the second half rotates the other way round
+    r2 = o.rope(e2, [3], 1e4, "bf16")[0, 0]
+    assert np.allclose(r2, [-math.sin(3), 0, math.cos(3), 0], atol=1e-15)
+
+
 ALL_PINS = [
     pin_slots_golden, pin_slots_brute_force, pin_scatter_roundtrip, pin_golden_tiny,
     pin_closed_forms, pin_gqa_mapping, pin_softmax_rows, pin_matches_library_sdpa,
     pin_block_permutation_invariance, pin_prefix_sharing_invariance,
     pin_ragged_equals_per_sequence, pin_fp32_close_to_fp64,
     pin_copy_on_write_keeps_contexts, pin_swap_round_trip,
+    pin_rope_identity_and_norm, pin_rope_relative_position, pin_rope_hand_cases,
 ]

@@ -36,6 +36,11 @@ MUTANTS = [
     ("copy_blocks", "out[d] = src[s]", "out[s] = src[d]"),
     ("copy_blocks", "out[d] = src[s]", "out[d] = out[s]"),
     ("copy_blocks", "if 0 <= s < src.shape[0]", "if 0 < s < src.shape[0]"),
+    ("rope", "[x1 * c - x2 * s, x2 * c + x1 * s]", "[x1 * c + x2 * s, x2 * c - x1 * s]"),
+    ("rope", "(-(2.0 * np.arange(half)) / D)", "(-(1.0 * np.arange(half)) / D)"),
+    ("rope", "c, s = np.cos(a)[:, None, :], np.sin(a)[:, None, :]",
+     "s, c = np.cos(a)[:, None, :], np.sin(a)[:, None, :]"),
+    ("rope", "x1, x2 = x[..., :half], x[..., half:]", "x1, x2 = x[..., 0::2], x[..., 1::2]"),
 ]
 
 
