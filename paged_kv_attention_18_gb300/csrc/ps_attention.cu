@@ -849,8 +849,11 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
   const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 32;
   // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
-  plan_kernel<<<ctas, 1024, smem, stream>>>(p, concurrency, tile_ctas);
-  return cudaGetLastError();
+  // programmatic dependent launch: the planner's CTAs may start while the previous kernel
+  // on the stream (say, the last step's combine) finishes; they wait for it before reading
+  // or writing anything
+  return launch_kernel(plan_kernel, dim3(ctas), dim3(1024), static_cast<size_t>(smem), stream,
+                       true, p, concurrency, tile_ctas);
 }
 
 template <bool kBF16, int D>
