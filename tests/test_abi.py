@@ -106,3 +106,49 @@ def test_profile_read_rejects(lib):
     ms, n = ctypes.c_float(), ctypes.c_int()
     assert lib.ps_profile_read(9, ctypes.addressof(ms), ctypes.addressof(n)) == -1
     assert lib.ps_profile_begin(0) == -1
+
+
+def test_copy_blocks_rejects(lib):
+    f = lib.ps_copy_blocks
+    args = lambda **kw: [kw.get(n, d) for n, d in (  # noqa: E731
+        ("sk", FAKE), ("sv", FAKE), ("snb", 8), ("dk", FAKE), ("dv", FAKE), ("dnb", 8),
+        ("si", FAKE), ("di", FAKE), ("n", 4), ("hkv", 2), ("d", 64), ("dt", 1), ("s", None))]
+    assert f(*args(d=96)) == -2              # head_dim
+    assert f(*args(dt=7)) == -2              # dtype
+    assert f(*args(n=-1)) == -1              # count
+    assert f(*args(snb=0)) == -1             # source pool size
+    assert f(*args(sk=FAKE + 2)) == -3       # alignment
+    assert f(*args(si=None)) == -1           # ids
+    assert f(*args(sk=None, sv=None, dk=None, dv=None, si=None, di=None, n=0)) == 0  # no-op
+
+
+def test_rope_reshape_and_cache_rejects(lib):
+    f = lib.ps_rope_reshape_and_cache
+    args = lambda **kw: [kw.get(n, d) for n, d in (  # noqa: E731
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("pos", FAKE), ("slots", FAKE), ("kp", FAKE),
+        ("vp", FAKE), ("T", 4), ("hq", 12), ("hkv", 2), ("d", 128), ("nb", 8),
+        ("theta", ctypes.c_float(1e6)), ("dt", 1), ("s", None))]
+    assert f(*args(d=96)) == -2                          # head_dim
+    assert f(*args(hq=5)) == -2                          # H_q % H_kv
+    assert f(*args(theta=ctypes.c_float(0.5))) == -1     # rotary base
+    assert f(*args(T=-1)) == -1                          # count
+    assert f(*args(q=FAKE + 4)) == -3                    # alignment
+    assert f(*args(pos=None)) == -1                      # positions
+    assert f(*args(q=None, k=None, v=None, pos=None, slots=None, kp=None, vp=None, T=0)) == 0
+
+
+def test_spec_accept_rejects(lib):
+    f = lib.ps_spec_accept
+    need = lib.ps_spec_accept_workspace_size(4, 4, 1000)
+    assert need > 0 and lib.ps_spec_accept_workspace_size(-1, 4, 1000) == 0
+    args = lambda **kw: [kw.get(n, d) for n, d in (  # noqa: E731
+        ("p", FAKE), ("q", None), ("dr", FAKE), ("r", FAKE), ("B", 4), ("k", 4), ("V", 1000),
+        ("g", 0), ("out", FAKE), ("num", FAKE), ("ws", FAKE), ("wsb", need), ("s", None))]
+    assert f(*args(B=-1)) == -1              # batch
+    assert f(*args(V=0)) == -1               # vocabulary
+    assert f(*args(k=32)) == -2              # one lane per draft: k <= 31
+    assert f(*args(r=None)) == -1            # random words needed by the rejection rule
+    assert f(*args(dr=None)) == -1           # drafts needed when k > 0
+    assert f(*args(ws=FAKE + 16)) == -4      # workspace alignment (256 bytes)
+    assert f(*args(wsb=need - 1)) == -4      # workspace size
+    assert f(*args(p=None, dr=None, r=None, out=None, num=None, ws=None, B=0)) == 0
