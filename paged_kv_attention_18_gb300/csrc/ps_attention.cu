@@ -801,19 +801,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += ws * v.x;
-        acc[1] += ws * v.y;
-        acc[2] += ws * v.z;
-        acc[3] += ws * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += ws * v.x;
-        acc[1] += ws * v.y;
+    // four partials' loads in flight per round
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+      float ws[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u;
+        ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < ns) {
+          const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
+          if constexpr (kPer == 4) {
+            v[u] = *reinterpret_cast<const float4*>(src);
+          } else {
+            const float2 v2 = *reinterpret_cast<const float2*>(src);
+            v[u] = make_float4(v2.x, v2.y, 0.f, 0.f);
+          }
+        } else {
+          ws[u] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[0] += ws[u] * v[u].x;
+        acc[1] += ws[u] * v[u].y;
+        if constexpr (kPer == 4) {
+          acc[2] += ws[u] * v[u].z;
+          acc[3] += ws[u] * v[u].w;
+        }
       }
     }
     const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
