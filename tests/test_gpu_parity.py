@@ -77,6 +77,7 @@ def test_spec_verify_long_full_size():
 SWEEP = [
     ("f16", 64, 4, 2), ("bf16", 64, 14, 2), ("f16", 128, 12, 2), ("bf16", 128, 12, 2),
     ("bf16", 128, 8, 8), ("f16", 64, 16, 1), ("bf16", 128, 32, 4), ("f16", 128, 6, 3),
+    ("bf16", 128, 32, 1),  # 32 query heads per KV head: every row on the split kernel
 ]
 
 
