@@ -319,14 +319,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   const bool planned = tot.x > 0 || tot.y > 0;
 
   // tokens: splits holding the rows, first partial entry, the combine's token list and the
-  // slot of the token's new K/V (block_table[pos / 16] * 16 + pos % 16). Four tokens per
-  // round so their block-table reads are in flight together.
+  // slot of the token's new K/V (block_table[pos / 16] * 16 + pos % 16). The tokens are
+  // dealt to the CTAs in blocks of nth, round robin, and each thread takes four per round so
+  // their block-table reads are in flight together.
   constexpr int kTokUnroll = 4;
-  for (int base = blockIdx.x * kTokUnroll * nth; base < p.T; base += gridDim.x * kTokUnroll * nth) {
+  const int tok_stride = gridDim.x * nth;
+  for (int base = blockIdx.x * nth; base < p.T; base += kTokUnroll * tok_stride) {
     int bb[kTokUnroll], blk[kTokUnroll];
 #pragma unroll
     for (int u = 0; u < kTokUnroll; ++u) {
-      const int t = base + u * nth + tid;
+      const int t = base + u * tok_stride + tid;
       bb[u] = -1;
       blk[u] = -1;
       if (t < p.T) {
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     }
 #pragma unroll
     for (int u = 0; u < kTokUnroll; ++u) {
-      const int t = base + u * nth + tid;
+      const int t = base + u * tok_stride + tid;
       if (t >= p.T) continue;
       const int b = bb[u];
       const SeqInfo s = seq_info(p, qsl, lens, b);
