@@ -47,8 +47,12 @@ TRAFFIC_FILES = {
     ("split_attention", "qwen15b_decode"): "split_attention_qwen15b_decode_traffic.json",
     ("tile_attention", "long_prefill"): "tile_attention_long_prefill_traffic.json",
 }
+# the source text each kernel is built from: a whole file, or (file, first line, line that
+# ends the region) for a kernel that shares its file with others
 KERNEL_SOURCES = {
-    "split_attention": ["paged_kv_attention_18_gb300/csrc/ps_attention.cu",
+    "split_attention": [("paged_kv_attention_18_gb300/csrc/ps_attention.cu",
+                         "// split kernel: one warp = one work item at a time",
+                         "// combine: one warp per (token, head) whose rows were split"),
                         "paged_kv_attention_18_gb300/csrc/ps_common.cuh"],
     "tile_attention": ["paged_kv_attention_18_gb300/csrc/ps_tile.cu",
                        "paged_kv_attention_18_gb300/csrc/ps_tc05.cuh",
@@ -99,9 +103,14 @@ def load_peaks() -> tuple[dict, str]:
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES[kernel]:
+    for src in KERNEL_SOURCES[kernel]:
+        rel, first, end = (src, None, None) if isinstance(src, str) else src
         with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+            text = f.read()
+        if first is not None:
+            a = text.index(first.encode())
+            text = text[a:text.index(end.encode(), a)]
+        h.update(text)
     return h.hexdigest()
 
 
