@@ -64,7 +64,7 @@ struct TileBars {
   uint64_t q_full[2], q_empty[2];  // query tiles A and B, each freed after its last S
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t mma_final;
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   int item_idx[kItemRing];
@@ -113,7 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[g], 1);
       mbar_init(&bars->p_full[g], 4);
       mbar_init(&bars->o_done[g], 1);
-      mbar_init(&bars->o_free[g], 4);
     }
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < kItemRing; ++s) {
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc1 = sdesc_sw128(sQ + L::kQ, 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(sV, kSub, 1024);
-      uint32_t g = 0, qa = 0, qb = 0, pc[2] = {0, 0}, act[2] = {0, 0};
+      uint32_t g = 0, qa = 0, qb = 0, pc[2] = {0, 0};
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int slot = it % kItemRing;
@@ -285,11 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
         if (!wait1(&bars->q_full[0], qa & 1)) break;
         const uint32_t g0 = g;
-        // S of query tile `grp` against K tile j
+        // S of query tile `grp` against K tile j. Only the item's first K tile is waited
+        // for here; P of query tile A for tile j - 1 implies K tile j (see the softmax).
         auto issue_s = [&](int grp, int j) -> bool {
           const uint32_t st = (g0 + j) % kKStages;
-          if (!wait1(&bars->k_full[st], ((g0 + j) / kKStages) & 1)) return false;
-          tc_fence_after();
+          if (j == 0 && grp == 0) {
+            if (!wait1(&bars->k_full[st], ((g0 + j) / kKStages) & 1)) return false;
+            tc_fence_after();
+          }
           const uint64_t a0 = grp ? qdesc1 : qdesc0;
           const uint64_t b0 = kdesc0 + ((st * L::kK) >> 4);
 #pragma unroll
@@ -302,14 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (grp == ng - 1) umma_commit(&bars->k_empty[st]);  // last reader of the K stage
           return true;
         };
-        // O of query tile `grp` += P V of K/V tile j
+        // O of query tile `grp` += P V of K/V tile j. P is the only wait: the softmax
+        // warps arrive on it after their epilogue of the previous item has read O, and
+        // query tile A's after V tile j (and K tile j + 1) have landed.
         auto issue_pv = [&](int grp, int j) -> bool {
           if (!wait1(&bars->p_full[grp], pc[grp] & 1)) return false;
           ++pc[grp];
-          // the previous item's epilogue of this group has read its O
-          if (j == 0 && !wait1(&bars->o_free[grp], (act[grp] & 1) ^ 1)) return false;
           const uint32_t st = (g0 + j) % kVStages;
-          if (!wait1(&bars->v_full[st], ((g0 + j) / kVStages) & 1)) return false;
           tc_fence_after();
           const uint64_t b0 = vdesc0 + ((st * L::kK) >> 4);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
@@ -335,10 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && j + 1 < nt) ok = issue_s(q, j + 1);
           }
         if (!ok) break;
-        for (int q = 0; q < ng; ++q) {
-          umma_commit(&bars->o_done[q]);
-          ++act[q];
-        }
+        for (int q = 0; q < ng; ++q) umma_commit(&bars->o_done[q]);
         g += nt;
         ++qa;
         if (ng > 1) ++qb;
@@ -356,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t tS = trow + col_s(grp), tO = trow + col_o(grp);
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, act = 0;
+    uint32_t sc = 0, act = 0, gt = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
@@ -364,9 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
+      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
+      const uint32_t g0 = gt;  // K/V tiles of the items before this one (as the producers count)
+      gt += nt;
       const int nrows = grp == 0 ? w.nrows : w.pad[0];
       if (nrows == 0) continue;  // no query tile B in this item
-      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       // this thread's query row
       const bool valid = r < nrows;
       const int R = w.row0 + grp * p.tpt * p.G + r;  // packed row within the sequence
@@ -466,6 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tS + 32 * h + 16, pk + 16);
         }
         m_next = m_tile > m_ref + kRescaleLog2 ? m_tile : m_ref;
+        // One warp of query tile A waits for V tile j and K tile j + 1 before its P goes
+        // out, so the MMA thread needs no wait of its own on them.
+        if (grp == 0 && quarter == 0) {
+          const uint32_t gv = g0 + j, gk = g0 + j + 1;
+          if (!wait(&bars->v_full[gv % kVStages], (gv / kVStages) & 1)) { ok = false; break; }
+          if (j + 1 < nt && !wait(&bars->k_full[gk % kKStages], (gk / kKStages) & 1)) {
+            ok = false;
+            break;
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -506,9 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c == 0) p.part_lse[pidx] = m_ref + __log2f(l);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_free[grp]);
       ++act;
     }
   }
