@@ -242,6 +242,32 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
+// a + b on two fp32 lanes in one packed instruction.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// acc.x += low 16-bit value of the pair, acc.y += high one, both exactly widened. A bf16
+// value is the upper half of an fp32 one, so widening is a shift or a mask, and the two
+// sums take one packed add.
+template <bool kBF16>
+__device__ __forceinline__ void add_pair_exact(float2& acc, uint32_t packed) {
+  if constexpr (kBF16) {
+    acc = fadd2(acc, make_float2(__uint_as_float(packed << 16),
+                                 __uint_as_float(packed & 0xffff0000u)));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y) : "r"(packed));
+  }
+}
+
 // s0 += low 16-bit value of the pair, s1 += high one: mixed-precision adds (a 16-bit
 // operand into an fp32 sum, exact widening), so no unpacking instructions are needed.
 template <bool kBF16>

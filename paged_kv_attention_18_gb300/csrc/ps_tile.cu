@@ -111,13 +111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&bars->s_full[g], 1);
-      mbar_init(&bars->p_full[g], 4);
+      mbar_init(&bars->p_full[g], g == 0 ? 5 : 4);  // tile A's: + the K/V watcher
       mbar_init(&bars->o_done[g], 1);
     }
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], 10);  // V producer, MMA warp, the 8 softmax warps
+      mbar_init(&bars->item_empty[s], 11);  // V producer, MMA, K/V watcher, 8 softmax warps
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait1(&bars->q_full[0], qa & 1)) break;
         const uint32_t g0 = g;
         // S of query tile `grp` against K tile j. Only the item's first K tile is waited
-        // for here; P of query tile A for tile j - 1 implies K tile j (see the softmax).
+        // for here; P of query tile A for tile j - 1 implies K tile j (the K/V watcher).
         auto issue_s = [&](int grp, int j) -> bool {
           const uint32_t st = (g0 + j) % kKStages;
           if (j == 0 && grp == 0) {
@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // O of query tile `grp` += P V of K/V tile j. P is the only wait: the softmax
         // warps arrive on it after their epilogue of the previous item has read O, and
-        // query tile A's after V tile j (and K tile j + 1) have landed.
+        // the K/V watcher adds its arrival to query tile A's once V tile j (and K tile
+        // j + 1) have landed.
         auto issue_pv = [&](int grp, int j) -> bool {
           if (!wait1(&bars->p_full[grp], pc[grp] & 1)) return false;
           ++pc[grp];
@@ -346,15 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bars->mma_final, 0, 1u << 22);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ============================ softmax groups + epilogue =========================
-    const int grp = (warp - 4) >> 2;   // 0: query tile A, 1: query tile B
-    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
-    const int r = quarter * 32 + lane;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = trow + col_s(grp), tO = trow + col_o(grp);
-    const float sl2 = p.scale_log2;
-    uint32_t sc = 0, act = 0, gt = 0;
+  } else if (warp == 3) {
+    // ============================ K/V watcher ==================================
+    // P of query tile A also stands for V tile j and K tile j + 1 having landed: this
+    // warp waits for them and adds its arrival to that P barrier, then waits for the
+    // barrier's phase to complete so that it never runs a tile ahead. The MMA thread
+    // then waits on P alone, and the softmax warps carry no extra waits.
+    uint32_t gt = 0, pc = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
@@ -363,8 +362,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-      const uint32_t g0 = gt;  // K/V tiles of the items before this one (as the producers count)
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t gv = gt + j, gk = gv + 1;
+        ok = wait(&bars->v_full[gv % kVStages], (gv / kVStages) & 1) &&
+             (j + 1 >= nt || wait(&bars->k_full[gk % kKStages], (gk / kKStages) & 1));
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(&bars->p_full[0]);
+        ok = wait(&bars->p_full[0], pc & 1);
+        ++pc;
+      }
       gt += nt;
+    }
+  } else if (warp >= 4) {
+    // ============================ softmax groups + epilogue =========================
+    const int grp = (warp - 4) >> 2;   // 0: query tile A, 1: query tile B
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = trow + col_s(grp), tO = trow + col_o(grp);
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, act = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int idx = next_item(it);
+      if (idx < 0) break;
+      const WorkItem& w = p.tile_items[idx];
+      const int pb = w.page_begin, pe = w.page_end;
+      if (pe <= pb) continue;
+      const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       const int nrows = grp == 0 ? w.nrows : w.pad[0];
       if (nrows == 0) continue;  // no query tile B in this item
       // this thread's query row
@@ -449,33 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
           uint32_t pk[32];
-          float lq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums
+          float2 lq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // four sums
           // scale and subtract two scores per packed fma; the row sum adds the 16-bit P
-          // values the MMA sees, widened exactly by mixed-precision adds
+          // values the MMA sees, widened exactly
           const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
           for (int e = 0; e < 64; e += 2) {
             const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
                                    sl2x2, nm2);
             pk[e / 2] = pack2<kBF16>(fast_exp2(x.x), fast_exp2(x.y));
-            const int c = ((e / 2) & 1) * 2;
-            add_halves<kBF16>(lq[c], lq[c + 1], pk[e / 2]);
+            add_pair_exact<kBF16>(lq[(e / 2) & 1], pk[e / 2]);
           }
-          l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+          l += (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
           tmem_st16(tS + 32 * h, pk);
           tmem_st16(tS + 32 * h + 16, pk + 16);
         }
         m_next = m_tile > m_ref + kRescaleLog2 ? m_tile : m_ref;
-        // One warp of query tile A waits for V tile j and K tile j + 1 before its P goes
-        // out, so the MMA thread needs no wait of its own on them.
-        if (grp == 0 && quarter == 0) {
-          const uint32_t gv = g0 + j, gk = g0 + j + 1;
-          if (!wait(&bars->v_full[gv % kVStages], (gv / kVStages) & 1)) { ok = false; break; }
-          if (j + 1 < nt && !wait(&bars->k_full[gk % kKStages], (gk / kKStages) & 1)) {
-            ok = false;
-            break;
-          }
-        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
