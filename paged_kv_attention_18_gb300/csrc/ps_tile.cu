@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = w.kv * p.G + R - qtok * p.G;
       const int pos = valid ? w.ctx_len - w.n_query + qtok : -1;
       const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
+      // the row's split count and partial base, fetched now so that the epilogue's
+      // stores do not wait on them
+      const int ns_t = valid ? __ldg(p.tok_ns + tok) : 0;
+      const int tok_part = valid && ns_t > 1 ? __ldg(p.tok_base + tok) : 0;
       // m_ref: the reference max (log2 units) that P, O and l are currently taken against;
       // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
       float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
@@ -499,35 +503,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: O / l of this group's rows to the output, or to the split partials
       if (!wait(&bars->o_done[grp], act & 1)) break;
       tc_fence_after();
-      int ns_t = 0;
-      if (valid) ns_t = __ldg(p.tok_ns + tok);
       const bool write = valid && w.split < ns_t && l > 0.f;
       const float inv = write ? 1.f / l : 0.f;
+      if (__all_sync(0xffffffffu, !write || ns_t == 1)) {
+        // Direct output. Each lane holds 64 columns (128 bytes) of its row per step; an
+        // 8 x 8 transpose of 16-byte segments inside each group of eight lanes lets every
+        // store instruction write four whole 128-byte rows (eight lanes per row) instead
+        // of touching 32 rows at once.
+        const int64_t row_off = write ? (static_cast<int64_t>(tok) * p.H_q + head) * D : -1;
+        const int g8 = lane & ~7, b = lane & 7;
+        uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32, v);
-        tmem_ld_wait();
-        if (!write) continue;
-        if (ns_t == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                (static_cast<int64_t>(tok) * p.H_q + head) * D +
-                                                c * 32);
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          uint32_t v[64];
+          tmem_ld32(tO + c2 * 64, v);
+          tmem_ld32(tO + c2 * 64 + 32, v + 32);
+          tmem_ld_wait();
+          uint4 x[8];  // x[s]: segment s (columns 8s..8s+7) of this lane's row
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(
-                pack2<kBF16>(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
-        } else {
-          const int64_t pidx = __ldg(p.tok_base + tok) + w.split * p.H_q + head;
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c * 32);
+          for (int sg = 0; sg < 8; ++sg)
+            x[sg] = make_uint4(
+                pack2<kBF16>(__uint_as_float(v[8 * sg + 0]) * inv, __uint_as_float(v[8 * sg + 1]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * sg + 2]) * inv, __uint_as_float(v[8 * sg + 3]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * sg + 4]) * inv, __uint_as_float(v[8 * sg + 5]) * inv),
+                pack2<kBF16>(__uint_as_float(v[8 * sg + 6]) * inv, __uint_as_float(v[8 * sg + 7]) * inv));
+          // butterfly transpose: afterwards x[k] is segment b of the row of lane g8 + k
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
-          if (c == 0) p.part_lse[pidx] = m_ref + __log2f(l);
+          for (int m = 4; m >= 1; m >>= 1) {
+            const bool hi = (b & m) != 0;
+#pragma unroll
+            for (int sg = 0; sg < 8; ++sg) {
+              if (sg & m) continue;
+              const uint4 send = hi ? x[sg] : x[sg | m];
+              uint4 recv;
+              recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+              recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+              recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+              recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+              if (hi) x[sg] = recv;
+              else x[sg | m] = recv;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int64_t ro = __shfl_sync(0xffffffffu, row_off, g8 + k);
+            if (ro >= 0) reinterpret_cast<uint4*>(out + ro + c2 * 64)[b] = x[k];
+          }
+        }
+      } else {
+        // split partials (fp32), one row per lane
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          uint32_t v[64];
+          tmem_ld32(tO + c2 * 64, v);
+          tmem_ld32(tO + c2 * 64 + 32, v + 32);
+          tmem_ld_wait();
+          if (!write) continue;
+          if (ns_t == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                  (static_cast<int64_t>(tok) * p.H_q + head) * D +
+                                                  c2 * 64);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_uint4(
+                  pack2<kBF16>(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                  pack2<kBF16>(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                  pack2<kBF16>(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                  pack2<kBF16>(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+          } else {
+            const int64_t pidx = static_cast<int64_t>(tok_part) + w.split * p.H_q + head;
+            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c2 * 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                   __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+            if (c2 == 0) p.part_lse[pidx] = m_ref + __log2f(l);
+          }
         }
       }
       ++act;
