@@ -268,20 +268,6 @@ __device__ __forceinline__ void add_pair_exact(float2& acc, uint32_t packed) {
   }
 }
 
-// s0 += low 16-bit value of the pair, s1 += high one: mixed-precision adds (a 16-bit
-// operand into an fp32 sum, exact widening), so no unpacking instructions are needed.
-template <bool kBF16>
-__device__ __forceinline__ void add_halves(float& s0, float& s1, uint32_t packed) {
-  if constexpr (kBF16)
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-        : "+f"(s0), "+f"(s1) : "r"(packed));
-  else
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
-        : "+f"(s0), "+f"(s1) : "r"(packed));
-}
-
 // Both 16-bit halves of a packed pair multiplied by a, rounded back.
 template <bool kBF16>
 __device__ __forceinline__ uint32_t scale_pair(uint32_t packed, float a) {
