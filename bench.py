@@ -372,8 +372,11 @@ def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
     return reduce_max(ms, world, device), prof, hook_steps, clk
 
 
-def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device):
-    """Same steps from pinned host buffers through ps_attention_step_host."""
+def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
+             eager: bool = False):
+    """Same steps from pinned host buffers: each engine step replays its
+    ps_attention_step_host graph (copies in, the step, copy out), or with ``eager`` calls
+    ps_attention_step_host itself; the stream is synchronised after every engine step."""
     import torch
     from paged_kv_attention_18_gb300 import binding
     wl = dw.wl
@@ -393,13 +396,21 @@ def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device):
         h["staging"] = torch.empty(n, dtype=torch.uint8, device=device)
         h2d += sum(h[k].numel() * h[k].element_size() for k in ("q", "k", "v", "bt", "sl", "qsl"))
         d2h += h["out"].numel() * h["out"].element_size()
+        if not eager:
+            h["graph"] = binding.HostStepGraph(h["q"], h["k"], h["v"], h["bt"], h["sl"], h["qsl"],
+                                               h["out"], dw.k_pool, dw.v_pool, wl.scale,
+                                               h["staging"])
         hosts.append(h)
     stream = torch.cuda.current_stream()
 
     def one():
         for h in hosts:
-            binding.attention_step_host(h["q"], h["k"], h["v"], h["bt"], h["sl"], h["qsl"],
-                                        h["out"], dw.k_pool, dw.v_pool, wl.scale, h["staging"])
+            if eager:
+                binding.attention_step_host(h["q"], h["k"], h["v"], h["bt"], h["sl"], h["qsl"],
+                                            h["out"], dw.k_pool, dw.v_pool, wl.scale,
+                                            h["staging"])
+            else:
+                h["graph"].launch()
             stream.synchronize()  # the caller reads the step's output
 
     for _ in range(warmup):
@@ -409,6 +420,9 @@ def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device):
     for _ in range(steps):
         one()
     sec = reduce_max(time.perf_counter() - t0, world, device)
+    for h in hosts:
+        if "graph" in h:
+            h["graph"].close()
     return sec, h2d, d2h
 
 
@@ -494,12 +508,16 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 200))
-        e2e_s, h2d, d2h = time_e2e(dw, e2e_steps, 3, world, device)
+        e2e_s, h2d, d2h = time_e2e(dw, e2e_steps, 3, world, device, eager=args.e2e_eager)
         e2e_value = (world * step_bytes * e2e_steps / e2e_s / 1e9 if unit == "GB/s"
                      else world * tokens * e2e_steps / e2e_s)
         e2e = {"value": e2e_value, "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "api": "ps_attention_step_host (pinned host buffers, stream sync per step)"}
+               "api": ("ps_attention_step_host (pinned host buffers, stream sync per step)"
+                       if args.e2e_eager else
+                       "ps_attention_step_host_graph_create once per engine step, then "
+                       "ps_graph_launch each step: the copies in from pinned host buffers, the "
+                       "step and the copy out, stream sync per step")}
 
     if rank != 0:
         return None
@@ -785,6 +803,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="time the end-to-end leg with plain ps_attention_step_host calls "
+                         "instead of its recorded graph")
     ap.add_argument("--op", choices=["step", "copy_blocks", "spec_accept", "rope_cache"],
                     default="step",
                     help="step: the attention step (default); copy_blocks: block copies; "

@@ -297,6 +297,38 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
  */
 size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq, int H_q,
                                            int H_kv, int D, int max_seq_len);
+
+/*
+ * ps_attention_step_host_graph_create -- ps_attention_step_host recorded once into a CUDA
+ * graph, so that a serving loop pays one graph launch per step instead of the copies' and
+ * kernels' launch costs (PageServe, "Next steps": CUDA graphs for decode, against Python
+ * and launch overhead at small batch sizes).
+ *
+ *   Arguments as ps_attention_step_host, without the stream; `graph` receives an opaque
+ *   handle. Nothing runs at creation: the pools are not touched.
+ *   Each ps_graph_launch(graph, stream) copies the CURRENT contents of the host buffers q,
+ *   k, v, block_tables, seq_lens, query_start_loc to the device, runs the step and copies
+ *   the output to `out`, as one call of ps_attention_step_host with the same arguments
+ *   would. Shapes (T, B, max_blocks_per_seq, heads, D, num_blocks) are fixed at creation;
+ *   the contents (lengths, block tables, tokens) may change between launches.
+ *   Ownership: the caller keeps every buffer alive, in place and (for the host ones)
+ *   page-locked while the graph exists; ps_graph_destroy releases the graph.
+ * Errors: those of ps_attention_step_host's argument checks; PS_ERR_CUDA if the capture or
+ * instantiation fails (for example, host buffers that are not page-locked). The handle is
+ * set only on success.
+ */
+int ps_attention_step_host_graph_create(const void* q, const void* k, const void* v,
+                                        const int32_t* block_tables, const int32_t* seq_lens,
+                                        const int32_t* query_start_loc, void* out,
+                                        void* k_pool, void* v_pool, int max_blocks_per_seq,
+                                        int B, int T, int H_q, int H_kv, int D, int num_blocks,
+                                        float scale, void* staging, size_t staging_bytes,
+                                        int dtype, void** graph);
+/* Launch a graph from ps_attention_step_host_graph_create on `stream` (asynchronous; the
+ * output is valid once the stream has completed). PS_ERR_ARG for a null handle. */
+int ps_graph_launch(void* graph, void* stream);
+/* Release a graph (after its last launch has completed). PS_ERR_ARG for a null handle. */
+int ps_graph_destroy(void* graph);
 int ps_attention_step_host(const void* q, const void* k, const void* v,
                            const int32_t* block_tables, const int32_t* seq_lens,
                            const int32_t* query_start_loc, void* out, void* k_pool,

@@ -40,6 +40,11 @@ SIGNATURES = {
     "ps_attention_step_host": (c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, c_int, c_int, c_int,
                                        c_int, c_int, c_int, c_int, c_float, _p, c_size_t, c_int,
                                        _p]),
+    "ps_attention_step_host_graph_create": (c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, c_int,
+                                                    c_int, c_int, c_int, c_int, c_int, c_int,
+                                                    c_float, _p, c_size_t, c_int, _p]),
+    "ps_graph_launch": (c_int, [_p, _p]),
+    "ps_graph_destroy": (c_int, [_p]),
     "ps_get_device_error": (c_int, [_p]),
     "ps_status_string": (c_char_p, [c_int]),
     "ps_last_error_message": (c_char_p, []),

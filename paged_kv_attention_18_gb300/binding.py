@@ -287,14 +287,9 @@ def staging_size(T: int, B: int, max_blocks: int, H_q: int, H_kv: int, D: int,
                                                          max_seq_len))
 
 
-def attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
-                        scale: float, staging, stream=None) -> None:
-    """One step from host tensors (ps_attention_step_host); ``out`` is a host tensor.
-
-    q/k/v/block_tables/seq_lens/query_start_loc/out live in host memory (pin them for
-    asynchronous copies); k_pool/v_pool and staging live on the device. The call returns
-    once everything is enqueued: synchronise the stream before reading ``out``.
-    """
+def _host_step_args(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                    scale, staging) -> tuple:
+    """Checked arguments of ps_attention_step_host, up to (not including) the stream."""
     for name, t in (("q", q), ("k", k), ("v", v), ("block_tables", block_tables),
                     ("seq_lens", seq_lens), ("query_start_loc", query_start_loc), ("out", out)):
         if t.is_cuda or not t.is_contiguous():
@@ -311,9 +306,58 @@ def attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k
     T, H_q, D = q.shape
     NB, _, H_kv, _ = k_pool.shape
     B, maxblk = block_tables.shape
-    _check(lib().ps_attention_step_host(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                        block_tables.data_ptr(), seq_lens.data_ptr(),
-                                        query_start_loc.data_ptr(), out.data_ptr(), kpp, vpp,
-                                        maxblk, B, T, H_q, H_kv, D, NB, float(scale), sp,
-                                        staging.numel(), DTYPE_CODE[q.dtype], _stream(stream)),
-           "ps_attention_step_host")
+    return (q.data_ptr(), k.data_ptr(), v.data_ptr(), block_tables.data_ptr(),
+            seq_lens.data_ptr(), query_start_loc.data_ptr(), out.data_ptr(), kpp, vpp, maxblk, B,
+            T, H_q, H_kv, D, NB, float(scale), sp, staging.numel(), DTYPE_CODE[q.dtype])
+
+
+def attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                        scale: float, staging, stream=None) -> None:
+    """One step from host tensors (ps_attention_step_host); ``out`` is a host tensor.
+
+    q/k/v/block_tables/seq_lens/query_start_loc/out live in host memory (pin them for
+    asynchronous copies); k_pool/v_pool and staging live on the device. The call returns
+    once everything is enqueued: synchronise the stream before reading ``out``.
+    """
+    args = _host_step_args(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool,
+                           v_pool, scale, staging)
+    _check(lib().ps_attention_step_host(*args, _stream(stream)), "ps_attention_step_host")
+
+
+class HostStepGraph:
+    """ps_attention_step_host recorded once in a CUDA graph (ps_attention_step_host_graph_create).
+
+    Every launch() copies the current contents of the host tensors to the device, runs the
+    step and copies the output back into ``out``: write a step's inputs into the same
+    tensors, launch, synchronise the stream, read ``out``. Shapes are fixed at creation;
+    the host tensors must be pinned. The object keeps every tensor alive until close().
+    """
+
+    def __init__(self, q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                 scale: float, staging):
+        args = _host_step_args(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool,
+                               v_pool, scale, staging)
+        handle = ctypes.c_void_p()
+        _check(lib().ps_attention_step_host_graph_create(*args, ctypes.addressof(handle)),
+               "ps_attention_step_host_graph_create")
+        self._handle = handle.value
+        self._keep = (q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                      staging)
+
+    def launch(self, stream=None) -> None:
+        if not self._handle:
+            raise PagedServeError("graph is closed")
+        _check(lib().ps_graph_launch(self._handle, _stream(stream)), "ps_graph_launch")
+
+    def close(self) -> None:
+        """Release the graph; its last launch must have completed."""
+        if self._handle:
+            lib().ps_graph_destroy(self._handle)
+            self._handle = None
+            self._keep = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "pagedserve.h"
@@ -627,6 +628,77 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
   if (cudaMemcpyAsync(out, st + l.out, static_cast<size_t>(T) * H_q * D * 2,
                       cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return PS_ERR_CUDA;
+  return PS_OK;
+}
+
+// One host step in a CUDA graph: the copies in, the step's kernels and the copy out are
+// captured from a private stream and instantiated once; each launch replays them with the
+// host buffers' contents at that time.
+struct HostStepGraph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+int ps_attention_step_host_graph_create(const void* q, const void* k, const void* v,
+                                        const int32_t* block_tables, const int32_t* seq_lens,
+                                        const int32_t* query_start_loc, void* out,
+                                        void* k_pool, void* v_pool, int max_blocks_per_seq,
+                                        int B, int T, int H_q, int H_kv, int D, int num_blocks,
+                                        float scale, void* staging, size_t staging_bytes,
+                                        int dtype, void** graph) {
+  if (!graph) return PS_ERR_ARG;
+  // device state (SM count, error word, tensor-map encoder) is resolved before capture
+  DeviceState* ds;
+  int rc = current_device_state(&ds);
+  if (rc) return rc;
+  cudaStream_t cs;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "graph stream");
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "graph capture");
+  }
+  rc = ps_attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool,
+                              v_pool, max_blocks_per_seq, B, T, H_q, H_kv, D, num_blocks, scale,
+                              staging, staging_bytes, dtype, cs);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(cs, &g);  // ends the capture whatever the step returned
+  cudaStreamDestroy(cs);
+  if (rc || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();  // clear the last-error state a failed capture leaves behind
+    return rc ? rc : cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown, "graph capture");
+  }
+  cudaGraphExec_t x;
+  e = cudaGraphInstantiate(&x, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(e, "graph instantiate");
+  }
+  auto* h = new (std::nothrow) HostStepGraph{g, x};
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return cuda_fail(cudaErrorMemoryAllocation, "graph handle");
+  }
+  *graph = h;
+  return PS_OK;
+}
+
+int ps_graph_launch(void* graph, void* stream) {
+  if (!graph) return PS_ERR_ARG;
+  const cudaError_t e =
+      cudaGraphLaunch(static_cast<HostStepGraph*>(graph)->exec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PS_OK : cuda_fail(e, "graph launch");
+}
+
+int ps_graph_destroy(void* graph) {
+  if (!graph) return PS_ERR_ARG;
+  auto* h = static_cast<HostStepGraph*>(graph);
+  cudaGraphExecDestroy(h->exec);
+  cudaGraphDestroy(h->graph);
+  delete h;
   return PS_OK;
 }
 

@@ -152,3 +152,13 @@ def test_spec_accept_rejects(lib):
     assert f(*args(ws=FAKE + 16)) == -4      # workspace alignment (256 bytes)
     assert f(*args(wsb=need - 1)) == -4      # workspace size
     assert f(*args(p=None, dr=None, r=None, out=None, num=None, ws=None, B=0)) == 0
+
+
+def test_graph_calls_reject_null_handles(lib):
+    assert lib.ps_graph_launch(None, None) == -1
+    assert lib.ps_graph_destroy(None) == -1
+    # no place for the handle: rejected before any CUDA call
+    f = lib.ps_attention_step_host_graph_create
+    rc = f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 3, 12, 2, 128, 64,
+           ctypes.c_float(0.1), FAKE, 1 << 30, 1, None)
+    assert rc == -1

@@ -68,3 +68,49 @@ def test_step_replayed_from_cuda_graph(name):
                                  st.query_start_loc, wl.scale, dt, acc=np.float32)
     err = np.abs(out.float().cpu().numpy() - ref).max()
     assert err <= TOL[dt], err
+
+
+def test_host_step_graph_follows_host_buffers():
+    # ps_attention_step_host recorded in a graph: every launch copies the host buffers'
+    # current contents in and the output out, so new tokens written into the same pinned
+    # tensors between launches must show up in the pools and the output
+    wl = W.named("qwen05b_mixed")
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    dt = wl.dtype
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dt]
+
+    def pin(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
+        return (t.view(dtype) if dtype is not None else t).pin_memory()
+
+    q, k, v = pin(st.q, tdt), pin(st.k, tdt), pin(st.v, tdt)
+    bt, sl, qs = pin(st.block_tables), pin(st.seq_lens), pin(st.query_start_loc)
+    out = torch.empty(q.shape, dtype=tdt).pin_memory()
+    n = binding.staging_size(st.T, st.B, st.max_blocks_per_seq, wl.H_q, wl.H_kv, wl.D,
+                             int(st.seq_lens.max()))
+    staging = torch.empty(n, dtype=torch.uint8, device="cuda")
+    g = binding.HostStepGraph(q, k, v, bt, sl, qs, out, pools.k, pools.v, wl.scale, staging)
+    try:
+        assert np.array_equal(host_bits(pools.k), wl.k_pool)  # creation runs nothing
+        slots_ref = oracle.slot_mapping(st.block_tables, st.seq_lens, st.query_start_loc)
+        kref, vref = wl.k_pool, wl.v_pool
+        rng = np.random.default_rng(78)
+        for launch in range(2):
+            if launch:
+                for t, a in ((q, st.q), (k, st.k), (v, st.v)):
+                    new = W.round_to_bits(rng.standard_normal(a.shape, dtype=np.float32), dt)
+                    t.copy_(torch.from_numpy(new.view(np.int16)).view(tdt))
+            qh, kh, vh = (t.view(torch.int16).numpy().view(np.uint16).copy() for t in (q, k, v))
+            g.launch()
+            torch.cuda.synchronize()
+            assert binding.device_error() == 0
+            kref, vref = oracle.reshape_and_cache(kh, vh, slots_ref, kref, vref)
+            assert np.array_equal(host_bits(pools.k), kref)
+            assert np.array_equal(host_bits(pools.v), vref)
+            ref = oracle.paged_attention(qh, kref, vref, st.block_tables, st.seq_lens,
+                                         st.query_start_loc, wl.scale, dt, acc=np.float32)
+            err = np.abs(out.float().numpy() - ref).max()
+            assert err <= TOL[dt], (launch, err)
+    finally:
+        g.close()
