@@ -220,7 +220,7 @@ __device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& i
 // sequences' items, so no CTA waits on another. The per-sequence metadata is staged in
 // shared memory when the batch is small enough (kPlanSmemSeqs sequences).
 constexpr int kPlanSmemSeqs = 4096;
-constexpr int kPlanSmemArrays = 6;  // qsl, lens and four offset arrays, B + 1 ints each
+constexpr int kPlanSmemArrays = 7;  // qsl, lens and five offset arrays, B + 1 ints each
 constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
@@ -318,6 +318,39 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   __syncthreads();
   const bool planned = tot.x > 0 || tot.y > 0;
 
+  // Tile items go out longest first as far as the sequences allow. A sequence's rank-r
+  // items are its r-th longest pair of query tiles (for every KV head and split). For the
+  // ranks every tile sequence has (r < rc) the items go rank by rank across the
+  // sequences; the ranks beyond follow sequence by sequence, each longest first. That
+  // needs the prefix of the items per rank (off_w), staged in shared memory; larger
+  // batches keep rc = 0.
+  __shared__ int s_rc;
+  int rc = 0;
+  int* off_w = in_smem ? off_s + (p.B + 1) : nullptr;
+  if (planned && tot.y > 0 && in_smem) {
+    if (tid == 0) s_rc = 1 << 30;
+    __syncthreads();
+    int run_w = 0;
+    for (int base = 0; base < p.B; base += nth) {
+      const int b = base + tid;
+      int wb = 0;
+      if (b < p.B) {
+        const SeqInfo s = seq_info(p, qsl, lens, b);
+        if (s.valid && s.tile) {
+          wb = seq_splits(s, pps_d, pps_t) * p.H_kv;
+          atomicMin(&s_rc, (s.qtiles + 1) / 2);
+        }
+      }
+      int4 t4;
+      const int4 ex = block_exscan4(make_int4(wb, 0, 0, 0), sh4, t4);
+      if (b < p.B) off_w[b] = run_w + ex.x;
+      run_w += t4.x;
+    }
+    if (tid == 0) off_w[p.B] = run_w;
+    __syncthreads();
+    rc = s_rc;
+  }
+
   // tokens: splits holding the rows, first partial entry, the combine's token list and the
   // slot of the token's new K/V (block_table[pos / 16] * 16 + pos % 16). The tokens are
   // dealt to the CTAs in blocks of nth, round robin, and each thread takes four per round so
@@ -374,7 +407,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
 
   // work items, one warp per sequence: split-kernel items with the group index fastest
   // (rows sharing pages run back to back); tile-kernel items as pairs of consecutive query
-  // tiles (A, B), the last (longest) pair of a sequence first
+  // tiles (A, B), placed in the rank order above
   const int lane = tid & 31, nw = nth >> 5;
   const int gw = blockIdx.x * nw + (tid >> 5);
   for (int b = planned ? gw : p.B; b < p.B; b += gridDim.x * nw) {
@@ -407,10 +440,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       }
     } else {
       const int npairs = (s.qtiles + 1) / 2;
-      const int cnt = npairs * ns * p.H_kv, first = off_t[b];
+      const int wb = ns * p.H_kv, cnt = npairs * wb, first = off_t[b];
+      const int width = rc > 0 ? off_w[p.B] : 0, ow = rc > 0 ? off_w[b] : 0;
       for (int local = lane; local < cnt; local += 32) {
-        const int j = npairs - 1 - local % npairs;
-        const int rest = local / npairs;
+        const int r = local % npairs;  // rank: 0 is the longest pair
+        const int j = npairs - 1 - r;
+        const int rest = local / npairs;  // split * H_kv + KV head
+        const int pos = r < rc ? r * width + ow + rest
+                               : rc * width + (first - rc * ow) + (r - rc) * wb + rest;
         const int kv = rest % p.H_kv;
         const int sp = rest / p.H_kv;
         const int qa = 2 * j * p.tpt, qb = qa + p.tpt;  // first query of tiles A and B
@@ -431,7 +468,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
         it.tok0 = s.tok0;
         it.pad[0] = nb * p.G;
         it.pad[1] = it.pad[2] = it.pad[3] = it.pad[4] = 0;
-        store_item(p.tile_items + first + local, it);
+        store_item(p.tile_items + pos, it);
       }
     }
   }

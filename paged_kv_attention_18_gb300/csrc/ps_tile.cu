@@ -73,6 +73,18 @@ struct TileBars {
 };
 static_assert(sizeof(TileBars) <= 512, "barrier block");
 
+// An item fits this launch: a sequence and KV head of the batch, a page range inside the
+// block table, and query rows inside the packed batch. Every role checks each item the
+// same way and skips one that does not fit, so no role reads or writes outside its
+// buffers on a plan it cannot use.
+__device__ __forceinline__ bool tile_item_ok(const WorkItem& w, const AttnParams& p) {
+  if (w.seq < 0 || w.seq >= p.B || w.kv < 0 || w.kv >= p.H_kv) return false;
+  if (w.page_begin < 0 || w.page_end > p.max_blocks) return false;
+  if (w.tok0 < 0 || w.row0 < 0 || w.nrows <= 0 || w.pad[0] < 0) return false;
+  const int last_row = w.row0 + (w.pad[0] > 0 ? p.tpt * p.G + w.pad[0] : w.nrows) - 1;
+  return w.tok0 + last_row / p.G < p.T;
+}
+
 }  // namespace
 
 template <bool kBF16, int D>
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
-      if (pe <= pb) continue;
+      if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int seq = w.seq, kv = w.kv;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       if (is_k) {
@@ -278,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx < 0) break;
         const WorkItem& w = p.tile_items[idx];
         const int pb = w.page_begin, pe = w.page_end;
+        if (!tile_item_ok(w, p)) {
+          record_error(p.err, kDevPlanOverflow);  // a plan this launch cannot use
+          continue;
+        }
         if (pe <= pb) continue;
         const bool has_b = w.pad[0] > 0;
         const int ng = has_b ? 2 : 1;
@@ -360,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
-      if (pe <= pb) continue;
+      if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       for (int j = 0; j < nt && ok; ++j) {
         const uint32_t gv = gt + j, gk = gv + 1;
@@ -388,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       const WorkItem& w = p.tile_items[idx];
       const int pb = w.page_begin, pe = w.page_end;
-      if (pe <= pb) continue;
+      if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
       const int nrows = grp == 0 ? w.nrows : w.pad[0];
       if (nrows == 0) continue;  // no query tile B in this item
