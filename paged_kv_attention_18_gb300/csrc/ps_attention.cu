@@ -220,7 +220,8 @@ __device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& i
 // sequences' items, so no CTA waits on another. The per-sequence metadata is staged in
 // shared memory when the batch is small enough (kPlanSmemSeqs sequences).
 constexpr int kPlanSmemSeqs = 4096;
-constexpr int kPlanSmemArrays = 7;  // qsl, lens and five offset arrays, B + 1 ints each
+constexpr int kPlanSmemArrays = 9;  // qsl, lens, five offset arrays, two tile lists; B + 1 ints each
+constexpr int kPlanRankSeqs = 512;  // tile sequences up to which every rank goes rank by rank
 constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
@@ -318,37 +319,51 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   __syncthreads();
   const bool planned = tot.x > 0 || tot.y > 0;
 
-  // Tile items go out longest first as far as the sequences allow. A sequence's rank-r
-  // items are its r-th longest pair of query tiles (for every KV head and split). For the
-  // ranks every tile sequence has (r < rc) the items go rank by rank across the
-  // sequences; the ranks beyond follow sequence by sequence, each longest first. That
-  // needs the prefix of the items per rank (off_w), staged in shared memory; larger
-  // batches keep rc = 0.
+  // Tile items go out longest first. A sequence's rank-r items are its r-th longest pair
+  // of query tiles (for every KV head and split); the items go rank by rank, and within a
+  // rank sequence by sequence. Rank r starts after C(r) = sum over tile sequences of
+  // width * min(pairs, r) items, and sequence b's block within it after the widths of the
+  // earlier sequences that have a rank r. For the ranks every tile sequence has (r < rc)
+  // that is r * (total width) + off_w[b]; beyond them it is summed over a compact list of
+  // the tile sequences (when there are at most kPlanRankSeqs of them; otherwise those ranks
+  // follow sequence by sequence). Batches not staged in shared memory keep rc = 0 and the
+  // sequence order.
   __shared__ int s_rc;
-  int rc = 0;
-  int* off_w = in_smem ? off_s + (p.B + 1) : nullptr;
+  int rc = 0, n_tile = 0;
+  int* off_w = in_smem ? off_s + (p.B + 1) : nullptr;   // width prefix (KV heads x splits)
+  int* tl_np = in_smem ? off_w + (p.B + 1) : nullptr;   // compact list: pairs of each
+  int* tl_w = in_smem ? tl_np + (p.B + 1) : nullptr;    // tile sequence, and its width
   if (planned && tot.y > 0 && in_smem) {
     if (tid == 0) s_rc = 1 << 30;
     __syncthreads();
-    int run_w = 0;
+    int run_w = 0, run_n = 0;
     for (int base = 0; base < p.B; base += nth) {
       const int b = base + tid;
-      int wb = 0;
+      int wb = 0, npb = 0;
       if (b < p.B) {
         const SeqInfo s = seq_info(p, qsl, lens, b);
         if (s.valid && s.tile) {
           wb = seq_splits(s, pps_d, pps_t) * p.H_kv;
-          atomicMin(&s_rc, (s.qtiles + 1) / 2);
+          npb = (s.qtiles + 1) / 2;
+          atomicMin(&s_rc, npb);
         }
       }
       int4 t4;
-      const int4 ex = block_exscan4(make_int4(wb, 0, 0, 0), sh4, t4);
-      if (b < p.B) off_w[b] = run_w + ex.x;
+      const int4 ex = block_exscan4(make_int4(wb, wb > 0 ? 1 : 0, 0, 0), sh4, t4);
+      if (b < p.B) {
+        off_w[b] = run_w + ex.x;
+        if (wb > 0) {
+          tl_np[run_n + ex.y] = npb;
+          tl_w[run_n + ex.y] = wb;
+        }
+      }
       run_w += t4.x;
+      run_n += t4.y;
     }
     if (tid == 0) off_w[p.B] = run_w;
     __syncthreads();
     rc = s_rc;
+    n_tile = run_n;
   }
 
   // tokens: splits holding the rows, first partial entry, the combine's token list and the
@@ -442,12 +457,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       const int npairs = (s.qtiles + 1) / 2;
       const int wb = ns * p.H_kv, cnt = npairs * wb, first = off_t[b];
       const int width = rc > 0 ? off_w[p.B] : 0, ow = rc > 0 ? off_w[b] : 0;
+      const bool by_rank = rc > 0 && n_tile <= kPlanRankSeqs;
       for (int local = lane; local < cnt; local += 32) {
         const int r = local % npairs;  // rank: 0 is the longest pair
         const int j = npairs - 1 - r;
         const int rest = local / npairs;  // split * H_kv + KV head
-        const int pos = r < rc ? r * width + ow + rest
-                               : rc * width + (first - rc * ow) + (r - rc) * wb + rest;
+        int pos;
+        if (r < rc) {
+          pos = r * width + ow + rest;
+        } else if (by_rank) {
+          // C(r) over every tile sequence, plus the earlier sequences that have rank r;
+          // the compact list keeps batch order, so "earlier" is a prefix of width ow
+          int c = 0, before = 0, seen_w = 0;
+          for (int k = 0; k < n_tile; ++k) {
+            const int nk = tl_np[k], wk = tl_w[k];
+            c += wk * min(nk, r);
+            if (seen_w < ow && nk > r) before += wk;
+            seen_w += wk;
+          }
+          pos = c + before + rest;
+        } else {
+          pos = rc * width + (first - rc * ow) + (r - rc) * wb + rest;
+        }
         const int kv = rest % p.H_kv;
         const int sp = rest / p.H_kv;
         const int qa = 2 * j * p.tpt, qb = qa + p.tpt;  // first query of tiles A and B
