@@ -18,6 +18,7 @@ the SM clocks seen during the timed region.
 from __future__ import annotations
 
 import os
+import re
 
 # the CPU oracle runs single-threaded (reported as cores = 1)
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -101,6 +102,14 @@ def load_peaks() -> tuple[dict, str]:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_only(text: bytes) -> bytes:
+    """Source text without comments and blank lines: editing a comment leaves the kernel,
+    and so its committed counters, as they were."""
+    text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    return b"\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for src in KERNEL_SOURCES[kernel]:
@@ -110,7 +119,7 @@ def kernel_source_hash(kernel: str) -> str:
         if first is not None:
             a = text.index(first.encode())
             text = text[a:text.index(end.encode(), a)]
-        h.update(text)
+        h.update(code_only(text))
     return h.hexdigest()
 
 

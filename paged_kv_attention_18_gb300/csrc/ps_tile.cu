@@ -12,15 +12,21 @@
 // j <= p: PageServe section 01; tinyserve "How it works") and grouped-query attention
 // (tinyserve "Highlights" table).
 //
-// Warp roles (384 threads): warp 0 hands out work items and loads Q and K (three K stages,
-// freed as soon as both S products have read them); warp 2 loads V (two stages); the page
-// copies of a tile are spread over the lanes, one TMA copy per lane. Warp 1 owns TMEM and
-// one of its threads issues the MMAs (warp 3 idle). Warps 4..7 (query tile A) and 8..11
-// (query tile B) are two softmax groups, one TMEM lane (one query row) per thread (a warp
-// reaches the 32 TMEM lanes of its warp index mod 4). While one group computes its
-// exponentials the tensor core works on the other group's products. P is written back
-// over S in TMEM and read from there by the PV product. O is rescaled lazily, only when a
-// row's running max grows by more than 2^8.
+// Warp roles (384 threads):
+//   warp 0     hands out work items (longest first, as the planner lists them) and loads
+//              Q and K: three K stages, each freed once both S products have read it;
+//   warp 2     loads V (two stages); a tile's page copies are spread over the lanes, one
+//              TMA copy per lane;
+//   warp 1     owns TMEM; one of its threads issues every MMA and, per tile and query
+//              tile, waits on nothing but P;
+//   warp 3     watches K and V: it adds its arrival to query tile A's P barrier once V
+//              tile j and K tile j + 1 have landed, so P also stands for them;
+//   warps 4..7 and 8..11  the softmax groups of query tiles A and B, one TMEM lane (one
+//              query row) per thread; a warp reaches the 32 TMEM lanes of its warp index
+//              mod 4. While one group computes its exponentials the tensor core works on
+//              the other group's products. P is written back over S in TMEM and read from
+//              there by the PV product. O is rescaled lazily, only when a row's running
+//              max grows by more than 2^8. The same warps write the item's output.
 #include "ps_common.cuh"
 #include "ps_launch.h"
 #include "ps_tc05.cuh"
