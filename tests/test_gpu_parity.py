@@ -111,15 +111,29 @@ def test_batch_larger_than_planner_staging():
     seqs = [(int(L), 1) for L in rng.integers(1, 48, size=5000)]
     seqs += [(int(L), int(n)) for L, n in zip(rng.integers(3000, 6000, size=6),
                                               rng.integers(1, 4, size=6))]
+    # three prefill chunks: tile items planned without the staged rank tables
+    seqs += [(300, 40), (900, 100), (2000, 250)]
     wl = W.simple_workload("wide", seed=41, dtype="bf16", H_q=12, H_kv=2, D=128, seqs=seqs)
     rng_rows = np.random.default_rng(42)
 
     def rows(i, st):
         qsl = st.query_start_loc
-        r = list(range(int(qsl[-7]), st.T))  # every row of the long sequences
+        r = list(range(int(qsl[-10]), st.T))  # every row of the long sequences and chunks
         return sorted(set(r + _sample_rows(st, 200, rng_rows)))
 
     check_workload(wl, rows_for_step=rows)
+
+
+def test_many_prefill_chunks():
+    # more than 512 prefill chunks of different lengths: the tile items of the ranks past
+    # the shortest chunk's are placed sequence by sequence instead of rank by rank
+    rng = np.random.default_rng(61)
+    seqs = [(int(L), int(n)) for L, n in zip(rng.integers(120, 400, size=600),
+                                             rng.integers(11, 60, size=600))]
+    seqs += [(int(L), 1) for L in rng.integers(500, 3000, size=20)]  # decodes among them
+    wl = W.simple_workload("chunks", seed=61, dtype="f16", H_q=12, H_kv=2, D=64, seqs=seqs)
+    rr = np.random.default_rng(62)
+    check_workload(wl, rows_for_step=lambda i, st: _sample_rows(st, 80, rr, extra_rows=300))
 
 
 def test_planner_grid_sizes():
