@@ -311,11 +311,13 @@ size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq,
  *   the output to `out`, as one call of ps_attention_step_host with the same arguments
  *   would. Shapes (T, B, max_blocks_per_seq, heads, D, num_blocks) are fixed at creation;
  *   the contents (lengths, block tables, tokens) may change between launches.
- *   Ownership: the caller keeps every buffer alive, in place and (for the host ones)
- *   page-locked while the graph exists; ps_graph_destroy releases the graph.
- * Errors: those of ps_attention_step_host's argument checks; PS_ERR_CUDA if the capture or
- * instantiation fails (for example, host buffers that are not page-locked). The handle is
- * set only on success.
+ *   The host buffers must be page-locked (cudaHostAlloc, cudaHostRegister); a host pointer
+ *   that is not is rejected with PS_ERR_ARG before anything is recorded.
+ *   Ownership: the caller keeps every buffer alive, in place and page-locked while the
+ *   graph exists; ps_graph_destroy releases the graph.
+ * Errors: PS_ERR_ARG for a null `graph` or a host buffer that is not page-locked; those of
+ * ps_attention_step_host's argument checks; PS_ERR_CUDA if the capture or instantiation
+ * fails. The handle is set only on success.
  */
 int ps_attention_step_host_graph_create(const void* q, const void* k, const void* v,
                                         const int32_t* block_tables, const int32_t* seq_lens,

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <initializer_list>
 #include <new>
 #include <vector>
 
@@ -651,6 +652,20 @@ int ps_attention_step_host_graph_create(const void* q, const void* k, const void
   DeviceState* ds;
   int rc = current_device_state(&ds);
   if (rc) return rc;
+  // every host buffer the graph copies from or to must be page-locked (null ones are left
+  // to the step's own argument checks)
+  for (const void* h : {q, k, v, static_cast<const void*>(block_tables),
+                        static_cast<const void*>(seq_lens),
+                        static_cast<const void*>(query_start_loc),
+                        static_cast<const void*>(out)}) {
+    if (!h) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+      cudaGetLastError();
+      return PS_ERR_ARG;
+    }
+    if (a.type != cudaMemoryTypeHost) return PS_ERR_ARG;
+  }
   cudaStream_t cs;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "graph stream");

@@ -114,3 +114,59 @@ def test_host_step_graph_follows_host_buffers():
             assert err <= TOL[dt], (launch, err)
     finally:
         g.close()
+
+
+def _host_step_tensors(wl, st, pinned=True):
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+    def host(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
+        t = (t.view(dtype) if dtype is not None else t).clone()
+        return t.pin_memory() if pinned else t
+
+    q, k, v = host(st.q, tdt), host(st.k, tdt), host(st.v, tdt)
+    bt, sl, qs = host(st.block_tables), host(st.seq_lens), host(st.query_start_loc)
+    out = torch.empty(q.shape, dtype=tdt)
+    out = out.pin_memory() if pinned else out
+    n = binding.staging_size(st.T, st.B, st.max_blocks_per_seq, wl.H_q, wl.H_kv, wl.D,
+                             max(1, int(st.seq_lens.max())))
+    return q, k, v, bt, sl, qs, out, torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def test_host_step_graph_empty_batch():
+    # no query tokens: the recorded graph is empty and launching it does nothing
+    wl = W.simple_workload("z", seed=4, dtype="f16", H_q=4, H_kv=2, D=64,
+                           seqs=[(10, 0), (33, 0)])
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    q, k, v, bt, sl, qs, out, staging = _host_step_tensors(wl, st)
+    g = binding.HostStepGraph(q, k, v, bt, sl, qs, out, pools.k, pools.v, wl.scale, staging)
+    g.launch()
+    torch.cuda.synchronize()
+    g.close()
+    assert binding.device_error() == 0
+    assert np.array_equal(host_bits(pools.k), wl.k_pool)
+
+
+def test_host_step_graph_rejects_pageable_buffers():
+    # the graph copies from and to page-locked host memory only: pageable buffers are
+    # rejected before anything is recorded, and a graph over pinned buffers still works
+    wl = W.named("tiny_decode")
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    args = _host_step_tensors(wl, st, pinned=False)
+    with pytest.raises(binding.PagedServeError):
+        binding.HostStepGraph(*args[:7], pools.k, pools.v, wl.scale, args[7])
+    assert np.array_equal(host_bits(pools.k), wl.k_pool)
+    args = _host_step_tensors(wl, st, pinned=True)
+    g = binding.HostStepGraph(*args[:7], pools.k, pools.v, wl.scale, args[7])
+    g.launch()
+    torch.cuda.synchronize()
+    g.close()
+    assert binding.device_error() == 0
+    out = args[6]
+    slots_ref = oracle.slot_mapping(st.block_tables, st.seq_lens, st.query_start_loc)
+    kref, vref = oracle.reshape_and_cache(st.k, st.v, slots_ref, wl.k_pool, wl.v_pool)
+    ref = oracle.paged_attention(st.q, kref, vref, st.block_tables, st.seq_lens,
+                                 st.query_start_loc, wl.scale, wl.dtype, acc=np.float32)
+    assert np.abs(out.float().numpy() - ref).max() <= TOL[wl.dtype]
