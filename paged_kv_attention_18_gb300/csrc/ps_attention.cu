@@ -372,11 +372,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // their block-table reads are in flight together.
   constexpr int kTokUnroll = 4;
   const int tok_stride = gridDim.x * nth;
+  // the token pass starts from the block's upper half: with few tokens it then runs on
+  // other warps than the item pass below, which deals sequences to the low warps first
+  const int ttid = (tid + nth / 2) % nth;
   for (int base = blockIdx.x * nth; base < p.T; base += kTokUnroll * tok_stride) {
     int bb[kTokUnroll], blk[kTokUnroll];
 #pragma unroll
     for (int u = 0; u < kTokUnroll; ++u) {
-      const int t = base + u * tok_stride + tid;
+      const int t = base + u * tok_stride + ttid;
       bb[u] = -1;
       blk[u] = -1;
       if (t < p.T) {
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     }
 #pragma unroll
     for (int u = 0; u < kTokUnroll; ++u) {
-      const int t = base + u * tok_stride + tid;
+      const int t = base + u * tok_stride + ttid;
       if (t >= p.T) continue;
       const int b = bb[u];
       const SeqInfo s = seq_info(p, qsl, lens, b);
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // (rows sharing pages run back to back); tile-kernel items as pairs of consecutive query
   // tiles (A, B), placed in the rank order above
   const int lane = tid & 31, nw = nth >> 5;
-  const int gw = blockIdx.x * nw + (tid >> 5);
+  const int gw = (tid >> 5) * gridDim.x + blockIdx.x;  // sequences dealt across the CTAs
   for (int b = planned ? gw : p.B; b < p.B; b += gridDim.x * nw) {
     const SeqInfo s = seq_info(p, qsl, lens, b);
     if (!s.valid || s.groups == 0) continue;
@@ -931,8 +934,9 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  // enough CTAs that the token and item passes are short; each repeats the batch scan
-  const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 32;
+  // enough CTAs that the token and item passes are short (a CTA's warps share its SM's
+  // issue slots, and emitting a sequence's items is division-heavy); each repeats the scan
+  const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 8;
   // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
   // programmatic dependent launch: the planner's CTAs may start while the previous kernel
