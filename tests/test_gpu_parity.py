@@ -137,7 +137,8 @@ def test_many_prefill_chunks():
 
 
 def test_planner_grid_sizes():
-    # token and sequence counts around the planner's per-CTA shares, with split decodes
+    # batches that give the planner different grid sizes (a CTA per 8 sequences and per 1024
+    # tokens, at most 64), with split decodes and a prefill chunk
     for B, seed in ((31, 51), (33, 52), (1025, 53)):
         rng = np.random.default_rng(seed)
         seqs = [(int(L), 1) for L in rng.integers(200, 2500, size=B)]
