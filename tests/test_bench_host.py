@@ -64,3 +64,27 @@ def test_subset_keeps_values_and_relabels_blocks():
     for i, b in enumerate([2, 0]):
         for j in range(-(-int(st.seq_lens[b]) // 16)):
             assert np.array_equal(sub.k_pool[sst.block_tables[i, j]], wl.k_pool[st.block_tables[b, j]])
+
+
+def test_traffic_records_follow_code_not_comments():
+    # a kernel's committed DRAM counters are keyed to its code: comments and blank lines
+    # may change, any code change drops the record
+    src = b"""// header
+__global__ void k(int* p) {  // trailing note
+  /* block
+     comment */
+  p[0] = 1;
+
+}
+"""
+    commented = src.replace(b"// header", b"// a new header, longer").replace(b"\n\n}", b"\n}")
+    edited = src.replace(b"p[0] = 1;", b"p[0] = 2;")
+    assert bench.code_only(src) == bench.code_only(commented)
+    assert bench.code_only(src) != bench.code_only(edited)
+    assert b"//" not in bench.code_only(src) and b"/*" not in bench.code_only(src)
+    # and the committed records match the current sources
+    import json
+    for (kernel, workload), name in bench.TRAFFIC_FILES.items():
+        with open(os.path.join(bench.ROOT, "profiles", name)) as f:
+            rec = json.load(f)
+        assert rec["source_sha256"] == bench.kernel_source_hash(kernel), name
