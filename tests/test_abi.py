@@ -4,7 +4,6 @@ import ctypes
 import os
 import re
 
-import pytest
 
 from paged_kv_attention_18_gb300 import _lib
 
