@@ -4,7 +4,6 @@ import ctypes
 import os
 import re
 
-
 from paged_kv_attention_18_gb300 import _lib
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pagedserve.h")
