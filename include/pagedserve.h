@@ -310,7 +310,9 @@ size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq,
  *   k, v, block_tables, seq_lens, query_start_loc to the device, runs the step and copies
  *   the output to `out`, as one call of ps_attention_step_host with the same arguments
  *   would. Shapes (T, B, max_blocks_per_seq, heads, D, num_blocks) are fixed at creation;
- *   the contents (lengths, block tables, tokens) may change between launches.
+ *   the contents (lengths, block tables, tokens) may change between launches, with lengths
+ *   within the max_seq_len `staging` was sized for (longer ones get fewer splits, and
+ *   PS_DEV_PLAN_OVERFLOW if even those do not fit).
  *   The host buffers must be page-locked (cudaHostAlloc, cudaHostRegister); a host pointer
  *   that is not is rejected with PS_ERR_ARG before anything is recorded.
  *   Ownership: the caller keeps every buffer alive, in place and page-locked while the
