@@ -648,10 +648,15 @@ int ps_attention_step_host_graph_create(const void* q, const void* k, const void
                                         float scale, void* staging, size_t staging_bytes,
                                         int dtype, void** graph) {
   if (!graph) return PS_ERR_ARG;
+  // argument errors are reported before anything is resolved or recorded
+  int rc = check_shapes(H_q, H_kv, D, dtype);
+  if (rc) return rc;
+  if ((rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
+                        num_blocks)))
+    return rc;
   // device state (SM count, error word, tensor-map encoder) is resolved before capture
   DeviceState* ds;
-  int rc = current_device_state(&ds);
-  if (rc) return rc;
+  if ((rc = current_device_state(&ds))) return rc;
   // every host buffer the graph copies from or to must be page-locked (null ones are left
   // to the step's own argument checks)
   for (const void* h : {q, k, v, static_cast<const void*>(block_tables),

@@ -160,3 +160,11 @@ def test_graph_calls_reject_null_handles(lib):
     rc = f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 3, 12, 2, 128, 64,
            ctypes.c_float(0.1), FAKE, 1 << 30, 1, None)
     assert rc == -1
+    # shape errors come back before any device work or recording
+    handle = ctypes.c_void_p()
+    rc = f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 3, 12, 2, 72, 64,
+           ctypes.c_float(0.1), FAKE, 1 << 30, 1, ctypes.addressof(handle))
+    assert rc == -2 and handle.value is None  # D = 72 unsupported; no handle
+    rc = f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 3, 12, 5, 128, 64,
+           ctypes.c_float(0.1), FAKE, 1 << 30, 1, ctypes.addressof(handle))
+    assert rc == -2 and handle.value is None  # 12 query heads over 5 KV heads
