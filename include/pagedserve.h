@@ -205,6 +205,8 @@ int ps_spec_accept(const float* target_probs, const float* draft_probs,
  * for a batch of at most T packed tokens, B sequences and contexts of at most
  * max_seq_len tokens. A smaller workspace (at least the size returned for
  * max_seq_len = 0) still works; the attention then splits long contexts into fewer parts.
+ * Returns 0 for invalid sizes or head counts, and for a batch whose plan could not be
+ * indexed with 32-bit integers (such a batch is rejected by ps_paged_attention too).
  */
 size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
                                          int max_seq_len);

@@ -165,29 +165,33 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 size_t workspace_fixed_bytes(int T, int B, int H_q, int H_kv, bool headroom, int* cap_items,
                              int* cap_tile) {
-  const int64_t G = H_q / H_kv;
-  const int tpt = tile_tokens(static_cast<int>(G));
-  const int64_t split_seqs = B < T ? B : T;
-  int64_t ci = static_cast<int64_t>(H_kv) * ((static_cast<int64_t>(T) * G + 15) / 16 + B);
-  int64_t ct = tpt > 0 ? static_cast<int64_t>(H_kv) * ((T + tpt - 1) / tpt + B) : 1;
+  // every count is taken in 64 bits, so sizes near INT_MAX cannot wrap; a plan whose
+  // lists would not be indexable with int gives SIZE_MAX (larger than any workspace)
+  const int64_t T64 = T, B64 = B, G = H_q / H_kv;
+  const int64_t tpt = tile_tokens(static_cast<int>(G));
+  const int64_t split_seqs = B64 < T64 ? B64 : T64;
+  int64_t ci = H_kv * ((T64 * G + 15) / 16 + B64);
+  int64_t ct = tpt > 0 ? H_kv * ((T64 + tpt - 1) / tpt + B64) : 1;
   if (headroom) {
-    ci += static_cast<int64_t>(H_kv) * split_seqs * kSplitGroupLimit * (kMaxSplits - 1);
-    if (tpt > 0) ct += static_cast<int64_t>(H_kv) * split_seqs * kTileSplitQTiles * (kMaxSplits - 1);
+    ci += H_kv * split_seqs * kSplitGroupLimit * (kMaxSplits - 1);
+    if (tpt > 0) ct += H_kv * split_seqs * kTileSplitQTiles * (kMaxSplits - 1);
   }
   if (ci < 1) ci = 1;
   if (ct < 1) ct = 1;
+  if (ci > INT32_MAX || ct > INT32_MAX || T64 < 0 || B64 < 0) return SIZE_MAX;
   if (cap_items) *cap_items = static_cast<int>(ci);
   if (cap_tile) *cap_tile = static_cast<int>(ct);
+  const size_t per_seq = static_cast<size_t>(B64 + 1) * 4, per_tok = static_cast<size_t>(T64) * 4;
   size_t o = 256;                                                   // header
   o = up256(o + static_cast<size_t>(ci) * sizeof(WorkItem));        // split items
-  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off
+  o = up256(o + per_seq);                                           // seq_off
   o = up256(o + static_cast<size_t>(ct) * sizeof(WorkItem));        // tile items
-  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_t
-  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_ns
-  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_base
-  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_p
-  o = up256(o + static_cast<size_t>(B + 1) * 4);                    // seq_off_s
-  o = up256(o + static_cast<size_t>(T) * 4);                        // tok_list
+  o = up256(o + per_seq);                                           // seq_off_t
+  o = up256(o + per_tok);                                           // tok_ns
+  o = up256(o + per_tok);                                           // tok_base
+  o = up256(o + per_seq);                                           // seq_off_p
+  o = up256(o + per_seq);                                           // seq_off_s
+  o = up256(o + per_tok);                                           // tok_list
   return o;
 }
 
@@ -447,6 +451,7 @@ size_t ps_paged_attention_workspace_size(int T, int B, int H_q, int H_kv, int D,
   if (T < 0 || B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || (D != 64 && D != 128))
     return 0;
   const size_t fixed = ps::workspace_fixed_bytes(T, B, H_q, H_kv, true, nullptr, nullptr);
+  if (fixed == SIZE_MAX) return 0;  // no workspace can hold the plan
   int64_t splits = (static_cast<int64_t>(max_seq_len) + ps::kBlockSize * ps::kMinSplitPages - 1) /
                    (ps::kBlockSize * ps::kMinSplitPages);
   if (splits > ps::kMaxSplits) splits = ps::kMaxSplits;

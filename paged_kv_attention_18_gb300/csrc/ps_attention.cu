@@ -8,7 +8,8 @@
 //     out[r, h] = softmax_j<=p( q[r, h] . K_b[j, h / G] * scale ) . V_b[j, h / G]
 // with K_b[j] read from the pool row block_table[b][j / 16] * 16 + j % 16.
 //
-// Design (GB300): a one-CTA planner turns the batch into work items on the device
+// Design (GB300): a multi-CTA planner (up to 64 CTAs, each repeating the per-sequence
+// scan) turns the batch into work items on the device
 // (16 packed rows = query tokens x GQA heads of one KV head, over one split of the
 // context); a persistent split kernel lets every warp fetch items from an atomic
 // counter and stream the item's K/V pages through its own ring of TMA-filled shared

@@ -40,6 +40,18 @@ def test_workspace_size(lib):
     assert 0 < small < big
     assert lib.ps_paged_attention_workspace_size(4, 4, 5, 2, 64, 100) == 0  # H_q % H_kv
     assert lib.ps_paged_attention_workspace_size(4, 4, 4, 2, 96, 100) == 0  # head_dim
+    big = 2 ** 31 - 1  # sizes are taken in 64 bits: no wrapped (small) size comes back
+    assert lib.ps_paged_attention_workspace_size(big, big, 12, 2, 128, 0) == 0
+
+
+def test_batch_sizes_near_int_max_are_rejected_before_device_work(lib):
+    big = 2 ** 31 - 1
+    rc = lib.ps_paged_attention(FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, big, big, 12, 2, 128,
+                                64, ctypes.c_float(0.1), FAKE, FAKE, 1 << 40, 1, None)
+    assert rc == -4  # PS_ERR_WORKSPACE: the plan's lists cannot be laid out
+    rc = lib.ps_paged_attention_noalloc(FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, big, big, 12,
+                                        2, 128, 64, ctypes.c_float(0.1), FAKE, 1, None)
+    assert rc == -4
 
 
 FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced by these calls

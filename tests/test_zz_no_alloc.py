@@ -4,8 +4,9 @@ Some callers are given only their input and output buffers and may not create de
 memory (a plug-in whose host framework owns all device memory, a loop that must not
 call cudaMalloc/cudaFree because they can synchronise the device). The no-allocation
 entry point keeps its scratch in a fixed array inside the library. These tests call it
-through the C ABI on two calls in a row and check each result against the ordinary
-entry point (which takes a caller-allocated workspace) within the parity tolerance.
+through the C ABI on two calls in a row and check each result against the CPU oracle
+within the parity bound, and against the ordinary entry point (which takes a
+caller-allocated workspace) within the same bound.
 """
 import ctypes
 
@@ -13,8 +14,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_attention_18_gb300 import _lib, binding
 from paged_kv_attention_18_gb300 import workloads as W
+from tests.gpu_util import bound_check
 
 pytestmark = pytest.mark.gpu
 
@@ -30,20 +33,28 @@ def _noalloc(lib, st, wl, q, kp, vp, bt, sl, qs, out):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def _compare_one(lib, wl):
+def _compare_one(lib, wl, rows=None):
+    """One no-allocation call against the oracle (on `rows`, or every row) and against
+    the workspace entry point."""
     st = wl.steps[0]
     dev = lambda a, dt=None: W.to_device(a, dt)  # noqa: E731
     q, kp, vp = dev(st.q, wl.dtype), dev(wl.k_pool, wl.dtype), dev(wl.v_pool, wl.dtype)
     bt, sl, qs = dev(st.block_tables), dev(st.seq_lens), dev(st.query_start_loc)
-    ref = binding.paged_attention(q, kp, vp, bt, sl, qs, wl.scale)  # caller workspace
     out = torch.full_like(q, float("nan"))
     rc = _noalloc(lib, st, wl, q, kp, vp, bt, sl, qs, out)
     assert rc == 0, lib.ps_status_string(rc)
     torch.cuda.synchronize()
-    assert binding.device_error() == 0
-    got, want = out.float().cpu().numpy(), ref.float().cpu().numpy()
+    assert binding.device_error() == 0  # no plan overflow, no bad index
+    got = out.float().cpu().numpy()
+    ref = oracle.paged_attention(st.q, wl.k_pool, wl.v_pool, st.block_tables, st.seq_lens,
+                                 st.query_start_loc, wl.scale, wl.dtype, acc=np.float32,
+                                 rows=rows)
+    sel = slice(None) if rows is None else np.asarray(rows, dtype=np.int64)
+    bound_check(got[sel], ref[sel], wl.dtype)
+    ws_out = binding.paged_attention(q, kp, vp, bt, sl, qs, wl.scale).float().cpu().numpy()
+    torch.cuda.synchronize()
     assert np.isfinite(got).all()
-    assert np.abs(got - want).max() <= TOL[wl.dtype]
+    assert np.abs(got - ws_out).max() <= TOL[wl.dtype]
 
 
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
@@ -57,6 +68,26 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
                                seqs=[(90, 1), (512, 256), (33, 2)])
     _compare_one(lib, first)
     _compare_one(lib, second)
+
+
+def test_noalloc_batch_whose_split_room_does_not_fit():
+    # 4096 one-token decodes: the work lists with room for splitting long contexts would
+    # take about 65 MB, more than the fixed scratch, so the call lays out the unsplit lists
+    # (under 1 MB). Half the sequences are long enough that the planner first splits them
+    # in two, which overflows those lists; it must coarsen the splits until the plan fits,
+    # and record no plan overflow.
+    rng = np.random.default_rng(71)
+    short = [(int(L), 1) for L in rng.integers(1, 17, size=2000)]
+    long_ = [(int(L), 1) for L in rng.integers(600, 901, size=2096)]
+    order = rng.permutation(len(short) + len(long_))
+    seqs = [(short + long_)[i] for i in order]
+    users = [i for i, (L, _) in enumerate(seqs) if L >= 600]
+    wl = W.simple_workload("noalloc-wide", seed=71, dtype="f16", H_q=12, H_kv=2, D=64,
+                           seqs=seqs, shared_prefix_blocks=37, prefix_users=users)
+    lib = _lib.load()
+    st = wl.steps[0]
+    rows = sorted(rng.choice(st.T, size=300, replace=False).tolist())
+    _compare_one(lib, wl, rows=rows)
 
 
 def test_noalloc_rejects_a_batch_beyond_its_fixed_scratch():
