@@ -2,14 +2,23 @@
 """Benchmark of one paged-KV attention step on GB300.
 
 A step is the whole hot path over one packed batch: slot mapping, KV scatter and
-paged attention (planner, split kernel, split combine), through the C ABI.
+paged attention (planner, split kernel, tile kernel, split combine), through the C ABI.
 
-Default workload: Qwen2.5-1.5B attention shapes, 256 decodes with contexts
-U[512, 4096] (12/2 heads, head_dim 128, bf16). ``value`` is the step's algorithmic HBM
-bytes / device time (GB/s, whole job). The line also carries the mixed-batch tokens/s
-of the prefix-cached chunked-prefill workload, the roofline of the dominant kernel,
-the end-to-end figure through the host-buffer entry point, the CPU-oracle baseline and
-the SM clocks seen during the timed region.
+With no --workload, the run covers the five workloads the attention step is specified
+on, each timed on its own:
+
+    tiny_decode            4 decodes, 4/2 heads, D 64, f16
+    qwen05b_mixed          8 decodes + 2 prefill chunks of 256, 14/2 heads, D 64, f16
+    qwen15b_decode         256 decodes, contexts U[512, 4096], 12/2 heads, D 128, bf16
+    prefix_chunked_prefill 64 prompts sharing a cached 1024-token prefix, chunked under an
+                           8192-token budget with 32 decodes (4 engine steps), bf16
+    spec_verify_long       132 sequences x 5 verify tokens, contexts up to 32768, bf16
+
+``value`` is the decode workload's (qwen15b_decode) algorithmic HBM bytes / device time
+(GB/s, whole job). ``workloads`` holds, for every workload, its GB/s, TFLOP/s and
+tokens/s, the roofline of its dominant kernel and the CPU oracle's rate on the host
+cores. The line also carries the end-to-end decode figure through the host-buffer entry
+point and the SM clocks seen during the timed regions.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -217,11 +226,36 @@ def barrier(world: int):
 # ------------------------------------------------------------------------------------
 # CPU oracle timing (baseline and reference arm)
 # ------------------------------------------------------------------------------------
-def oracle_seconds(wl: W.Workload, st: W.Step, seqs: list[int]) -> tuple[float, int]:
+def cpu_info() -> dict:
+    """The host CPU: core count, model name (or, on Arm, implementer and part) and the
+    BLAS threads each oracle process uses."""
+    model = None
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k.lower() == "model name" and not model:
+                    model = v
+                elif k in ("CPU implementer", "CPU part") and k not in fields:
+                    fields[k] = v
+    except OSError:
+        pass
+    if not model:
+        import platform
+        model = platform.machine() + (" (" + ", ".join(f"{k} {v}" for k, v in fields.items())
+                                      + ")" if fields else "")
+    return {"cpu_count": os.cpu_count() or 1, "model": model,
+            "blas_threads_per_process": int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))}
+
+
+def oracle_seconds(wl: W.Workload, st: W.Step, seqs: list[int]) -> tuple[float, int, int]:
     """Time the oracle (slot mapping, scatter, attention) on a subset of sequences.
 
     The subset keeps only the pool blocks its sequences use, so the oracle's copy of the
-    pool in its scatter scales with the sample. Returns (seconds, algorithmic bytes)."""
+    pool in its scatter scales with the sample. Returns (seconds, algorithmic bytes,
+    tokens)."""
     import oracle
     sub, sst = W.subset(wl, st, seqs)
     t0 = time.perf_counter()
@@ -230,20 +264,144 @@ def oracle_seconds(wl: W.Workload, st: W.Step, seqs: list[int]) -> tuple[float, 
     return dt, step_work(sub, sst)["step_bytes"], sst.T
 
 
-def cpu_baseline(wl, st, unit: str = "GB/s", budget_s: float = 12.0) -> dict:
-    """Oracle throughput on the same workload, whole steps repeated for ~budget_s."""
-    seqs = list(range(st.B))
-    total_t, total_b, total_tok, reps = 0.0, 0, 0, 0
-    while total_t < budget_s and reps < 50:
-        dt, nb, nt = oracle_seconds(wl, st, seqs)
-        total_t += dt
-        total_b += nb
-        total_tok += nt
-        reps += 1
-    value = total_b / total_t / 1e9 if unit == "GB/s" else total_tok / total_t
-    return {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-            "sample": f"the whole step ({st.B} sequences, {st.T} tokens) x {reps}, "
-                      f"{total_t:.1f} s of single-thread CPU"}
+_SAMPLE_ARRAYS = ("k_pool", "v_pool", "q", "k", "v", "block_tables", "seq_lens",
+                  "query_start_loc", "seq_ids")
+
+
+def save_sample(wl: W.Workload, st: W.Step, seqs: list[int], path: str) -> None:
+    """The sample's sequences of one step, with only the pool blocks they use, written as
+    .npy files under `path` for the oracle worker processes to map read-only."""
+    sub, sst = W.subset(wl, st, seqs)
+    os.makedirs(path, exist_ok=True)
+    for name in _SAMPLE_ARRAYS:
+        np.save(os.path.join(path, name + ".npy"), getattr(sub if "pool" in name else sst, name))
+    with open(os.path.join(path, "meta.json"), "w") as f:
+        json.dump({"name": sub.name, "dtype": sub.dtype, "H_q": sub.H_q, "H_kv": sub.H_kv,
+                   "D": sub.D, "num_blocks": sub.num_blocks}, f)
+
+
+_SAMPLES: dict = {}
+
+
+def _oracle_chunk(task) -> tuple[int, int]:
+    """Worker process: run the oracle on sequences `seqs` of the sample stored at `path`
+    (with no sequences, only map the sample and wait `pause` seconds, so that a round of
+    such tasks reaches every worker). Returns (algorithmic bytes, tokens) of the chunk."""
+    path, seqs, pause = task
+    if not path:
+        return 0, 0
+    if path not in _SAMPLES:
+        with open(os.path.join(path, "meta.json")) as f:
+            m = json.load(f)
+        a = {n: np.load(os.path.join(path, n + ".npy"), mmap_mode="r") for n in _SAMPLE_ARRAYS}
+        wl = W.Workload(name=m["name"], dtype=m["dtype"], H_q=m["H_q"], H_kv=m["H_kv"], D=m["D"],
+                        num_blocks=m["num_blocks"], k_pool=a["k_pool"], v_pool=a["v_pool"])
+        st = W.Step(q=a["q"], k=a["k"], v=a["v"], block_tables=np.array(a["block_tables"]),
+                    seq_lens=np.array(a["seq_lens"]),
+                    query_start_loc=np.array(a["query_start_loc"]), seq_ids=np.array(a["seq_ids"]))
+        _SAMPLES.clear()
+        _SAMPLES[path] = (wl, st)
+    if not seqs:
+        time.sleep(pause)
+        return 0, 0
+    wl, st = _SAMPLES[path]
+    _, nb, nt = oracle_seconds(wl, st, list(seqs))
+    return nb, nt
+
+
+class OraclePool:
+    """One oracle process per host core (spawned, so no process is forked from one that
+    has used the GPU), each with single-threaded BLAS."""
+
+    def __init__(self, n: int | None = None):
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        self.n = n or (os.cpu_count() or 1)
+        self.ex = ProcessPoolExecutor(self.n, mp_context=mp.get_context("spawn"))
+        list(self.ex.map(_oracle_chunk, [("", [], 0.0)] * self.n))  # start every worker
+
+    def prepare(self, path: str) -> None:
+        """Every worker maps the sample (untimed): each of 2n pausing tasks holds its
+        worker, so the round reaches all of them."""
+        list(self.ex.map(_oracle_chunk, [(path, [], 0.3)] * (2 * self.n)))
+
+    def run(self, path: str, chunks: list[list[int]]) -> tuple[float, int, int]:
+        """Wall seconds, bytes and tokens of the oracle over `chunks` in parallel (after
+        prepare(path))."""
+        t0 = time.perf_counter()
+        res = list(self.ex.map(_oracle_chunk, [(path, c, 0.0) for c in chunks]))
+        return time.perf_counter() - t0, sum(r[0] for r in res), sum(r[1] for r in res)
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def _rate(nbytes: int, tokens: int, sec: float, unit: str) -> float:
+    return nbytes / sec / 1e9 if unit == "GB/s" else tokens / sec
+
+
+def sample_sequences(wl: W.Workload, st: W.Step, budget_s: float, seed: int = 0) -> list[int]:
+    """A seeded random order of step 0's sequences, cut to about budget_s of single-core
+    oracle time (measured on a probe of the first few)."""
+    order = [int(b) for b in np.random.default_rng(seed).permutation(st.B)]
+    probe = order[:min(4, st.B)]
+    dt, _, _ = oracle_seconds(wl, st, probe)
+    per_seq = max(dt / max(1, len(probe)), 1e-5)
+    n = int(max(1, min(st.B, budget_s / per_seq)))
+    return sorted(order[:n])
+
+
+def cpu_baseline(wl: W.Workload, unit: str, pool: OraclePool | None, budget_s: float = 3.0,
+                 tmpdir: str | None = None) -> dict:
+    """The oracle's rate on the same workload (its first engine step): on one core over a
+    sample of about budget_s, and on every core (one process per core) over a sample
+    about cores times larger, split by sequence. Rates are algorithmic bytes (or tokens)
+    of the sample / time, in the workload's unit."""
+    st = wl.steps[0]
+    info = cpu_info()
+    min_s = min(1.0, budget_s)  # a sample that runs shorter is repeated up to this time
+    one = sample_sequences(wl, st, budget_s)
+    dt1, nb1, nt1, reps = 0.0, 0, 0, 0
+    while dt1 < min_s:
+        dt, nb, nt = oracle_seconds(wl, st, one)
+        dt1, nb1, nt1, reps = dt1 + dt, nb1 + nb, nt1 + nt, reps + 1
+    single = {"value": _rate(nb1, nt1, dt1, unit), "unit": unit, "cores": 1, "kind": "oracle",
+              "sample": f"{len(one)} of {st.B} sequences of engine step 0 "
+                        f"({nt1 // reps} tokens) x {reps}, {dt1:.1f} s on one core"}
+    if pool is None:
+        single["cpu"] = info
+        return single
+    # every core: a sample of about cores x budget_s of single-core time (capped at the
+    # whole step), split into chunks of about equal oracle work
+    seqs = sample_sequences(wl, st, budget_s * pool.n, seed=1)
+    n_b = np.diff(st.query_start_loc).astype(np.int64)
+    cost = {b: int(st.seq_lens[b]) * max(1, int(n_b[b])) for b in seqs}  # oracle work ~ L * n
+    chunks: list[list[int]] = [[] for _ in range(pool.n)]
+    loads = [0] * pool.n
+    for b in sorted(seqs, key=lambda x: -cost[x]):
+        i = loads.index(min(loads))
+        chunks[i].append(b)
+        loads[i] += cost[b]
+    path = tempfile.mkdtemp(prefix="oracle_sample_", dir=tmpdir)
+    try:
+        save_sample(wl, st, seqs, path)
+        # sequence ids inside the saved sample are its positions
+        pos = {b: i for i, b in enumerate(seqs)}
+        chunks = [[pos[b] for b in c] for c in chunks if c]
+        pool.prepare(path)
+        dta, nba, nta, reps = 0.0, 0, 0, 0
+        while dta < min_s:
+            dt, nb, nt = pool.run(path, chunks)
+            dta, nba, nta, reps = dta + dt, nba + nb, nta + nt, reps + 1
+    finally:
+        import shutil
+        shutil.rmtree(path, ignore_errors=True)
+    return {"value": _rate(nba, nta, dta, unit), "unit": unit, "cores": len(chunks),
+            "kind": "oracle",
+            "sample": f"{len(seqs)} of {st.B} sequences of engine step 0 ({nta // reps} "
+                      f"tokens) x {reps}, split over {len(chunks)} single-threaded oracle "
+                      f"processes (of {pool.n} host cores), {dta:.1f} s wall",
+            "single_core": single, "cpu": info}
 
 
 # ------------------------------------------------------------------------------------
@@ -323,27 +481,22 @@ class DeviceWorkload:
             self.run_one(d)
 
 
-def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
-                clocks: ClockSampler | None, min_load_s: float = 1.5):
+def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device):
     """Time `steps` steps with CUDA events (max over ranks), then time each kernel.
 
     The per-kernel times come from a second pass over the same steps with the library's
     timing hook (CUDA events around every launch). The hook is kept out of the first pass
     because an event between two launches would undo their programmatic dependent launch.
-    Returns (ms for the timed steps, {kernel: (ms, launches)} per hook step, hook steps,
-    clock record).
+    Returns (ms for the timed steps, {kernel: (ms, launches)} per hook step, hook steps).
     """
     import torch
     from paged_kv_attention_18_gb300 import binding
-    if clocks:
-        clocks.start()
     for _ in range(warmup):
         dw.run()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    t_wall = time.perf_counter()
     if dw.flush_buf is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -373,12 +526,7 @@ def time_device(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
         dw.run_eager()  # the timing hook sees eager launches only
     torch.cuda.synchronize()
     prof = binding.profile_end()
-    # keep the same load running until the clock sampler has seen enough of it
-    while time.perf_counter() - t_wall < min_load_s:
-        dw.run()
-        torch.cuda.synchronize()
-    clk = clocks.stop() if clocks else None
-    return reduce_max(ms, world, device), prof, hook_steps, clk
+    return reduce_max(ms, world, device), prof, hook_steps
 
 
 def time_e2e(dw: DeviceWorkload, steps: int, warmup: int, world: int, device,
@@ -467,138 +615,202 @@ def time_flushed(dw: DeviceWorkload, steps: int, world: int, device) -> float:
         dw.flush_buf = None
 
 
-def run_ours(args, rank, world, local_rank) -> dict | None:
-    import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    from paged_kv_attention_18_gb300 import binding
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    peaks, peaks_src = load_peaks()
+# the five workloads the step is specified on; the decode one gives the headline value
+ALL_WORKLOADS = ["tiny_decode", "qwen05b_mixed", "qwen15b_decode", "prefix_chunked_prefill",
+                 "spec_verify_long"]
+HEADLINE = "qwen15b_decode"
+# each workload's own unit: HBM GB/s where every row is a decode or verify row (the
+# split kernel streams the context), tokens/s where prefill chunks are mixed in
+UNITS = {"tiny_decode": "GB/s", "qwen05b_mixed": "tokens/s", "qwen15b_decode": "GB/s",
+         "prefix_chunked_prefill": "tokens/s", "spec_verify_long": "GB/s",
+         "long_prefill": "tokens/s"}
 
-    wl = make_workload(args.workload, rank, args.batch)
+
+def roofline_of(prof: dict, work: list[dict], name: str, peaks: dict, peaks_src: str,
+                hook_steps: int) -> dict:
+    """Roofline of the step's dominant attention kernel (split or tile, by summed time),
+    from the library hook's per-launch CUDA-event times on the launching stream."""
+    kernel_ms = {k: t for k, (t, n) in prof.items() if n > 0}
+    nsteps = len(work)
+    attn = {k: kernel_ms.get(k, 0.0) for k in ("split_attention", "tile_attention")}
+    dom = max(attn, key=attn.get)
+    dom_ms, dom_n = prof[dom]
+    avg_s = dom_ms / 1e3 / max(1, dom_n)
+    share = dom_ms / (sum(kernel_ms.values()) or 1)
+    if dom == "tile_attention":
+        flops_launch = sum(w["tile_flops"] for w in work) / nsteps
+        peak = peaks["bf16_tflops"]
+        achieved = flops_launch / avg_s / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+             "frac": achieved / peak,
+             "traffic": committed_traffic("tile_attention", name, flops_launch),
+             "kernel": "tile_attention_kernel (tcgen05)",
+             "algorithmic_per_launch": {"flops": flops_launch},
+             "peak_source": f"{peaks_src} bf16_tflops (burst: the kernel runs well under a "
+                            "millisecond per launch; fp16 runs at the bf16 rate)"}
+    else:
+        bytes_launch = sum(w["split_bytes"] for w in work) / nsteps
+        achieved = bytes_launch / avg_s / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": achieved / peaks["hbm_gbs"],
+             "traffic": committed_traffic("split_attention", name,
+                                          sum(w["split_kv_bytes"] for w in work) / nsteps),
+             "kernel": "split_attention_kernel",
+             "algorithmic_per_launch": {"bytes": bytes_launch},
+             "peak_source": f"{peaks_src} hbm_gbs"}
+    r["kernel_share_of_step"] = share
+    r["per_kernel_ms_per_step"] = {k: t / max(1, prof[k][1]) * nsteps for k, t in kernel_ms.items()}
+    r["timing"] = (f"kernel times from a second pass of {hook_steps} steps with CUDA events "
+                   "around every launch (library timing hook)")
+    return r
+
+
+def measure_workload(name: str, wl: W.Workload, args, world: int, device, peaks: dict,
+                     peaks_src: str, keep: bool = False):
+    """Device timing of one workload: the step rate, its GB/s, TFLOP/s and tokens/s, the
+    L2-flushed companion for a workload larger than L2, and the dominant kernel's
+    roofline. Returns (entry, the resident workload if `keep`)."""
+    import torch
+    from paged_kv_attention_18_gb300 import binding
     work = [step_work(wl, st) for st in wl.steps]
     step_bytes = sum(w["step_bytes"] for w in work)
-    attn_bytes = sum(w["attn_bytes"] for w in work)
-    kv_bytes = sum(w["kv_bytes"] for w in work)
     tokens = sum(w["tokens"] for w in work)
     flops = sum(w["flops"] for w in work)
     dw = DeviceWorkload(wl, device)
     if args.graph:
         dw.capture()
-    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 and not args.no_clocks \
-        else None
-    ms, prof, hook_steps, clk = time_device(dw, args.steps, args.warmup, world, device, clocks,
-                                            min_load_s=0.0 if args.no_clocks else 1.5)
+    ms, prof, hook_steps = time_device(dw, args.steps, args.warmup, world, device)
     if binding.device_error() != 0:
-        raise RuntimeError("device error word set during the benchmark")
+        raise RuntimeError(f"device error word set during the {name} benchmark")
+    sec = ms / 1e3
+    unit = UNITS[name]
+    gbs = world * step_bytes * args.steps / sec / 1e9
+    tok_s = world * tokens * args.steps / sec
     flushed = None
     if dw.flush_buf is None and not args.no_flushed:
         fsteps = max(3, min(args.steps, 100))
         fms = time_flushed(dw, fsteps, world, device)
-        fval = (world * step_bytes / (fms / 1e3) / 1e9 if args.workload == "qwen15b_decode"
-                else world * tokens / (fms / 1e3))
-        flushed = {"value": fval, "ms_per_step": fms, "steps": fsteps,
+        flushed = {"value": (world * step_bytes / (fms / 1e3) / 1e9 if unit == "GB/s"
+                             else world * tokens / (fms / 1e3)),
+                   "ms_per_step": fms, "steps": fsteps,
                    "note": "the same steps with the L2 written over (516 MB) before every "
                            "engine step, outside CUDA events around each step"}
-    sec = ms / 1e3
-    if args.workload == "qwen15b_decode":
-        value, unit = world * step_bytes * args.steps / sec / 1e9, "GB/s"
-    else:
-        value, unit = world * tokens * args.steps / sec, "tokens/s"
+    st0 = wl.steps[0]
+    entry = {
+        "workload": wl.name, "description": wl.description, "dtype": wl.dtype,
+        "value": gbs if unit == "GB/s" else tok_s, "unit": unit,
+        "ms_per_step": ms / args.steps, "steps": args.steps,
+        "engine_steps_per_step": len(wl.steps),
+        "gbs": gbs, "tflops": world * flops * args.steps / sec / 1e12, "tokens_per_s": tok_s,
+        "B": [st.B for st in wl.steps] if len(wl.steps) > 1 else st0.B,
+        "T_per_step": tokens, "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D,
+        "block_size": 16, "num_blocks": wl.num_blocks,
+        "kv_bytes_per_step": sum(w["kv_bytes"] for w in work),
+        "algorithmic_bytes_per_step": step_bytes, "flops_per_step": flops,
+        "l2": (f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 1e6:.0f} MB KV pool, "
+               f"{sum(w['kv_bytes'] for w in work) / 1e6:.0f} MB of it read per step, vs "
+               f"{L2_BYTES / 1e6:.0f} MB L2); no flush" if dw.flush_buf is None else
+               f"L2 flushed before every engine step ({4 * L2_BYTES / 1e6:.0f} MB buffer "
+               f"written, outside the timed events): the {2 * wl.k_pool.nbytes / 1e6:.0f} MB "
+               "KV pool fits in L2"),
+        "l2_flushed": flushed,
+        "gpu_launches": int(sum(n for _, n in prof.values()) * args.steps // hook_steps),
+        "roofline": roofline_of(prof, work, name, peaks, peaks_src, hook_steps),
+    }
+    if not keep:
+        del dw
+        torch.cuda.empty_cache()
+        return entry, None
+    return entry, dw
 
-    # dominant kernel (largest share of the summed kernel time), timed per launch by the
-    # library hook on the launching stream
-    kernel_ms = {k: t for k, (t, n) in prof.items() if n > 0}
-    dom = max(kernel_ms, key=kernel_ms.get)
-    dom_ms, dom_n = prof[dom]
-    avg_s = dom_ms / 1e3 / max(1, dom_n)
-    nsteps = len(wl.steps)
-    share = dom_ms / (sum(kernel_ms.values()) or 1)
-    if dom == "tile_attention":
-        flops_launch = sum(w["tile_flops"] for w in work) / nsteps
-        peak = peaks["bf16_tflops_sustained"]
-        achieved = flops_launch / avg_s / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak,
-                    "traffic": committed_traffic("tile_attention", args.workload, flops_launch),
-                    "kernel": "tile_attention_kernel (tcgen05)",
-                    "peak_source": f"{peaks_src} (bf16_tflops_sustained; fp16 runs at the bf16 "
-                                   "rate)",
-                    "kernel_share_of_step": share}
-    else:
-        bytes_launch = sum(w["split_bytes"] for w in work) / nsteps
-        achieved = bytes_launch / avg_s / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": committed_traffic("split_attention", args.workload,
-                                                 sum(w["split_kv_bytes"] for w in work) / nsteps),
-                    "kernel": "split_attention_kernel", "peak_source": f"{peaks_src} (hbm_gbs)",
-                    "kernel_share_of_step": share}
-    roofline["per_kernel_ms_per_step"] = {k: t / max(1, prof[k][1]) * nsteps
-                                          for k, t in kernel_ms.items()}
-    roofline["timing"] = (f"kernel times from a second pass of {hook_steps} steps with CUDA "
-                          "events around every launch (library timing hook)")
 
-    # mixed batch: prefix-cached chunked prefill packed with decodes
-    mixed = None
-    if args.workload == "qwen15b_decode" and not args.no_mixed:
-        wm = make_workload("prefix_chunked_prefill", rank)
-        dm = DeviceWorkload(wm, device)
-        msteps = max(3, min(args.steps, 20))
-        mms, _, _, _ = time_device(dm, msteps, min(args.warmup, 3), world, device, None,
-                                   min_load_s=0.0)
-        mtok = sum(st.T for st in wm.steps)
-        mflops = sum(step_work(wm, st)["flops"] for st in wm.steps)
-        mixed = {"workload": wm.name, "value": world * mtok * msteps / (mms / 1e3),
-                 "unit": "tokens/s", "steps": msteps, "engine_steps_per_step": len(wm.steps),
-                 "tflops": world * mflops * msteps / (mms / 1e3) / 1e12}
-        del dm
+def run_ours(args, rank, world, local_rank) -> dict | None:
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    peaks, peaks_src = load_peaks()
+    names = [args.workload] if args.workload else list(ALL_WORKLOADS)
+    head = args.workload or HEADLINE
+    # the headline workload last, so that it stays resident for the end-to-end leg
+    names = [n for n in names if n != head] + [head]
+    wls = {n: make_workload(n, rank, args.batch) for n in names}
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 and not args.no_clocks \
+        else None
+    if clocks:
+        clocks.start()
+    t_load = time.perf_counter()
+    entries, head_dw = {}, None
+    for n in names:
+        entries[n], dw = measure_workload(n, wls[n], args, world, device, peaks, peaks_src,
+                                          keep=(n == head))
+        if n == head:
+            head_dw = dw
+    # keep the same load running until the clock sampler has seen enough of it
+    while clocks and time.perf_counter() - t_load < 1.5:
+        head_dw.run()
+        torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
 
+    hd = entries[head]
     e2e = None
     if not args.no_e2e:
+        wl = wls[head]
         e2e_steps = max(3, min(args.steps, 200))
-        e2e_s, h2d, d2h = time_e2e(dw, e2e_steps, 3, world, device, eager=args.e2e_eager)
-        e2e_value = (world * step_bytes * e2e_steps / e2e_s / 1e9 if unit == "GB/s"
-                     else world * tokens * e2e_steps / e2e_s)
-        e2e = {"value": e2e_value, "unit": unit,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+        e2e_s, h2d, d2h = time_e2e(head_dw, e2e_steps, 3, world, device, eager=args.e2e_eager)
+        nbytes = hd["algorithmic_bytes_per_step"]
+        e2e = {"value": (world * nbytes * e2e_steps / e2e_s / 1e9 if hd["unit"] == "GB/s"
+                         else world * hd["T_per_step"] * e2e_steps / e2e_s),
+               "unit": hd["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps,
                "api": ("ps_attention_step_host (pinned host buffers, stream sync per step)"
                        if args.e2e_eager else
                        "ps_attention_step_host_graph_create once per engine step, then "
                        "ps_graph_launch each step: the copies in from pinned host buffers, the "
                        "step and the copy out, stream sync per step")}
+        del wl
+    del head_dw
+    torch.cuda.empty_cache()
 
     if rank != 0:
         return None
-    base = None if args.no_cpu_baseline else cpu_baseline(wl, wl.steps[0], unit)
-    st0 = wl.steps[0]
+    # the CPU oracle on the host cores, after all GPU work (its worker processes are
+    # spawned, never forked from this process)
+    if not args.no_cpu_baseline:
+        pool = OraclePool() if (os.cpu_count() or 1) > 1 else None
+        try:
+            for n in names:
+                entries[n]["cpu_baseline"] = cpu_baseline(wls[n], UNITS[n], pool)
+        finally:
+            if pool:
+                pool.close()
     result = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "metric": METRIC, "value": hd["value"], "unit": hd["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": hd["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": hd["dtype"],
         "data": "synthetic (seeded N(0,1) values, random block permutation)",
-        "config": {"workload": wl.name, "description": wl.description, "B": st0.B,
-                   "T": tokens, "H_q": wl.H_q, "H_kv": wl.H_kv, "head_dim": wl.D,
-                   "block_size": 16, "num_blocks": wl.num_blocks,
-                   "kv_bytes_per_step": kv_bytes, "algorithmic_bytes_per_step": step_bytes,
-                   "flops_per_step": flops,
-                   "tflops": world * flops * args.steps / sec / 1e12,
-                   "l2": (f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 1e6:.0f} MB KV pool, "
-                          f"{kv_bytes / 1e6:.0f} MB of it read per step, vs "
-                          f"{L2_BYTES / 1e6:.0f} MB L2); no flush" if dw.flush_buf is None else
-                          f"L2 flushed before every engine step ({4 * L2_BYTES / 1e6:.0f} MB "
-                          f"buffer written, outside the timed events): the "
-                          f"{2 * wl.k_pool.nbytes / 1e6:.0f} MB KV pool fits in L2"),
-                   "l2_flushed": flushed,
+        "config": {"workload": hd["workload"], "description": hd["description"],
+                   "B": hd["B"], "T": hd["T_per_step"], "H_q": hd["H_q"], "H_kv": hd["H_kv"],
+                   "head_dim": hd["head_dim"], "block_size": 16,
+                   "num_blocks": hd["num_blocks"], "kv_bytes_per_step": hd["kv_bytes_per_step"],
+                   "algorithmic_bytes_per_step": hd["algorithmic_bytes_per_step"],
+                   "flops_per_step": hd["flops_per_step"], "tflops": hd["tflops"],
+                   "l2": hd["l2"], "l2_flushed": hd["l2_flushed"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": ("each engine step replayed from a CUDA graph (captured once)"
                               if args.graph else "eager launches through the C ABI")},
-        "gpu_launches": int(sum(n for _, n in prof.values()) * args.steps // hook_steps),
-        "roofline": roofline,
-        "mixed_batch": mixed,
+        "gpu_launches": hd["gpu_launches"],
+        "roofline": hd["roofline"],
+        "workloads": {n: entries[n] for n in ALL_WORKLOADS if n in entries} if len(names) > 1
+        else None,
+        "mixed_batch": ({"workload": entries["prefix_chunked_prefill"]["workload"],
+                         "value": entries["prefix_chunked_prefill"]["tokens_per_s"],
+                         "unit": "tokens/s",
+                         "tflops": entries["prefix_chunked_prefill"]["tflops"]}
+                        if "prefix_chunked_prefill" in entries else None),
         "e2e": e2e,
-        "cpu_baseline": base,
+        "cpu_baseline": hd.get("cpu_baseline"),
         "clocks": clk,
     }
     return result
@@ -807,36 +1019,56 @@ def run_spec_accept(args, rank, world, local_rank) -> dict | None:
 # reference arm: the CPU oracle as it stands
 # ------------------------------------------------------------------------------------
 def run_reference(args, rank, world) -> dict | None:
+    """The CPU oracle as it stands, on the host cores (one single-threaded process per
+    core), on the headline workload and unit; each step is one pass over a bounded sample
+    of its sequences, sized so that warm-up and steps take about two minutes."""
     if rank != 0:
         return None
-    wl = make_workload(args.workload, 0, args.batch)
+    name = args.workload or HEADLINE
+    unit = UNITS[name]
+    wl = make_workload(name, 0, args.batch)
     st = wl.steps[0]
-    # a bounded sample per step so that warm-up + steps stay within ~2 minutes
-    probe = list(range(min(4, st.B)))
-    probe_t, _, _ = oracle_seconds(wl, st, probe)
-    per_seq = probe_t / max(1, len(probe))
+    pool = OraclePool() if (os.cpu_count() or 1) > 1 else None
+    ncores = pool.n if pool else 1
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(st.B, per_step_budget / max(per_seq, 1e-5))))
-    seqs = list(range(n))
-    for _ in range(args.warmup):
-        oracle_seconds(wl, st, seqs)
+    seqs = sample_sequences(wl, st, per_step_budget * ncores)
+    path = tempfile.mkdtemp(prefix="oracle_ref_")
     total_t, total_b, total_tok = 0.0, 0, 0
-    for _ in range(args.steps):
-        dt, nb, nt = oracle_seconds(wl, st, seqs)
-        total_t += dt
-        total_b += nb
-        total_tok += nt
-    unit = "GB/s" if args.workload == "qwen15b_decode" else "tokens/s"
-    value = total_b / total_t / 1e9 if unit == "GB/s" else total_tok / total_t
-    sample = f"{n} of {st.B} sequences of step 0 per step, single-thread CPU oracle"
+    try:
+        if pool:
+            save_sample(wl, st, seqs, path)
+            n_b = np.diff(st.query_start_loc).astype(np.int64)
+            order = sorted(range(len(seqs)),
+                           key=lambda i: -int(st.seq_lens[seqs[i]]) * max(1, int(n_b[seqs[i]])))
+            chunks = [order[c::ncores] for c in range(ncores)]
+            chunks = [c for c in chunks if c]
+            pool.prepare(path)
+            run = lambda: pool.run(path, chunks)  # noqa: E731
+        else:
+            run = lambda: oracle_seconds(wl, st, seqs)  # noqa: E731
+        for _ in range(args.warmup):
+            run()
+        for _ in range(args.steps):
+            dt, nb, nt = run()
+            total_t += dt
+            total_b += nb
+            total_tok += nt
+    finally:
+        import shutil
+        shutil.rmtree(path, ignore_errors=True)
+        if pool:
+            pool.close()
+    value = _rate(total_b, total_tok, total_t, unit)
+    sample = (f"{len(seqs)} of {st.B} sequences of engine step 0 per step, over {ncores} "
+              "single-threaded CPU oracle processes")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded N(0,1) values, random block permutation)",
             "config": {"workload": wl.name, "description": wl.description},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": ncores, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_info()},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -847,12 +1079,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen15b_decode", choices=sorted(W.NAMED))
+    ap.add_argument("--workload", default=None, choices=sorted(W.NAMED),
+                    help="time this workload alone (default: the five specified workloads, "
+                         "with the decode workload as the headline)")
     ap.add_argument("--batch", type=int, default=None,
                     help="decode batch size for qwen15b_decode (default 256); for small "
                          "profiling cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flushed", action="store_true",
                     help="skip the L2-flushed companion timing of a workload larger than L2")
