@@ -248,30 +248,36 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   int rc = current_device(&num_sms, &err);
   if (rc) return rc;
   p.err = err;
+  // Only a sequence with more than 16 * kTileMinGroups packed rows (n * G) reaches the
+  // tile kernel, and n <= T: for a smaller batch the tile kernel is not launched at all.
+  const bool tiles = p.tpt > 0 && static_cast<int64_t>(p.T) * p.G > 16 * kTileMinGroups;
   CUtensorMap kmap, vmap, qmap;
   if ((rc = make_pool_map(&kmap, k_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
-  if (p.tpt > 0 && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
-  const int concurrency = attention_ctas(p.D, num_sms) * attention_warps(p.D);
+  if (tiles && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
+  const int split_grid = split_ctas(p, num_sms);
+  const int concurrency = split_grid * attention_warps(p.D);
   cudaError_t e;
-  {
-    Timed tm(2, s);
-    if ((e = launch_plan(p, concurrency, num_sms, s)) != cudaSuccess)
-      return cuda_fail(e, "plan kernel");
-  }
+  // With the step's K/V to cache, the scatter goes first and the planner runs beside it;
+  // every later launch is chained with programmatic dependent launch.
   if (scatter) {
     Timed tm(1, s);
-    if ((e = launch_reshape_and_cache(scatter->k, scatter->v, p.slots, k_pool, v_pool, p.T,
-                                      p.H_kv, p.D, p.num_blocks, err, num_sms, s, true)) !=
-        cudaSuccess)
+    if ((e = launch_step_scatter(scatter->k, scatter->v, p.block_tables, p.max_blocks, p.seq_lens,
+                                 p.qsl, p.B, p.T, p.H_kv, p.D, p.num_blocks, p.slots, k_pool,
+                                 v_pool, err, num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "KV scatter kernel");
   }
   {
+    Timed tm(2, s);
+    if ((e = launch_plan(p, concurrency, num_sms, scatter != nullptr, s)) != cudaSuccess)
+      return cuda_fail(e, "plan kernel");
+  }
+  {
     Timed tm(3, s);
-    if ((e = launch_split_attention(p, bf16, kmap, vmap, num_sms, s, true)) != cudaSuccess)
+    if ((e = launch_split_attention(p, bf16, kmap, vmap, split_grid, s, true)) != cudaSuccess)
       return cuda_fail(e, "split attention kernel");
   }
-  if (p.tpt > 0) {
+  if (tiles) {
     Timed tm(5, s);
     if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s, true)) != cudaSuccess)
       return cuda_fail(e, "tile attention kernel");

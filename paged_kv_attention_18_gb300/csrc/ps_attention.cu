@@ -226,13 +226,17 @@ constexpr int kPlanRankSeqs = 512;  // tile sequences up to which every rank goe
 constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
-                                                    int tile_ctas) {
+                                                    int tile_ctas, bool after_scatter) {
   __shared__ int4 sh4[32];
   __shared__ longlong2 shl[32];
   extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
   pdl_launch_dependents();
-  pdl_wait();
+  // First in the chain, the planner waits for the previous work on the stream before it
+  // reads anything. After the step's scatter it starts once that kernel has seen the
+  // previous work finish, reads only the step's inputs and writes only the workspace, and
+  // waits for the scatter just before it ends, so that its completion stands for both.
+  if (!after_scatter) pdl_wait();
   const bool in_smem = p.B <= kPlanSmemSeqs;
   const int* qsl = p.qsl;
   const int* lens = p.seq_lens;
@@ -367,48 +371,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     n_tile = run_n;
   }
 
-  // tokens: splits holding the rows, first partial entry, the combine's token list and the
-  // slot of the token's new K/V (block_table[pos / 16] * 16 + pos % 16). The tokens are
-  // dealt to the CTAs in blocks of nth, round robin, and each thread takes four per round so
-  // their block-table reads are in flight together.
+  // tokens: splits holding the rows, first partial entry and the combine's token list. The
+  // tokens are dealt to the CTAs in blocks of nth, round robin, four per thread and round.
   constexpr int kTokUnroll = 4;
   const int tok_stride = gridDim.x * nth;
   // the token pass starts from the block's upper half: with few tokens it then runs on
   // other warps than the item pass below, which deals sequences to the low warps first
   const int ttid = (tid + nth / 2) % nth;
   for (int base = blockIdx.x * nth; base < p.T; base += kTokUnroll * tok_stride) {
-    int bb[kTokUnroll], blk[kTokUnroll];
-#pragma unroll
-    for (int u = 0; u < kTokUnroll; ++u) {
-      const int t = base + u * tok_stride + ttid;
-      bb[u] = -1;
-      blk[u] = -1;
-      if (t < p.T) {
-        const int b = last_le(qsl, p.B, t);
-        const SeqInfo s = seq_info(p, qsl, lens, b);
-        bb[u] = b;
-        if (p.slots && s.valid) {
-          const int pos = s.L - s.n + (t - s.tok0);
-          blk[u] = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pos / kBlockSize);
-        }
-      }
-    }
 #pragma unroll
     for (int u = 0; u < kTokUnroll; ++u) {
       const int t = base + u * tok_stride + ttid;
       if (t >= p.T) continue;
-      const int b = bb[u];
+      const int b = last_le(qsl, p.B, t);
       const SeqInfo s = seq_info(p, qsl, lens, b);
       const int i = t - s.tok0;
-      if (p.slots) {
-        int slot = -1;
-        if (s.valid) {
-          const int pos = s.L - s.n + i;
-          if (blk[u] >= 0 && blk[u] < p.num_blocks) slot = blk[u] * kBlockSize + pos % kBlockSize;
-          else record_error(p.err, kDevBadBlockId);
-        }
-        p.slots[t] = slot;
-      }
       int ns_t = 0, tb = 0;
       if (planned && s.valid && s.groups > 0) {
         const int ns = seq_splits(s, pps_d, pps_t);
@@ -517,6 +494,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     p.hdr[6] = pps_t;
     p.hdr[7] = planned ? tot.w : 0;
   }
+  if (after_scatter) pdl_wait();
 }
 
 // ----------------------------------------------------------------------------------
@@ -926,7 +904,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
 int attention_warps(int D) { return D == 128 ? SplitCfg<128>::kWarps : SplitCfg<64>::kWarps; }
 int attention_ctas(int D, int num_sms) { (void)D; return num_sms * PS_SPLIT_CTAS_PER_SM; }
 
-cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, bool after_scatter,
                         cudaStream_t stream) {
   const int smem =
       p.B <= kPlanSmemSeqs ? kPlanSmemArrays * (p.B + 1) * static_cast<int>(sizeof(int)) : 0;
@@ -940,33 +918,45 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas,
   const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 8;
   // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
-  // programmatic dependent launch: the planner's CTAs may start while the previous kernel
-  // on the stream (say, the last step's combine) finishes; they wait for it before reading
-  // or writing anything
+  // programmatic dependent launch: the planner's CTAs may start while the kernel before
+  // them on the stream finishes (see plan_kernel for what they wait for, and when)
   return launch_kernel(plan_kernel, dim3(ctas), dim3(1024), static_cast<size_t>(smem), stream,
-                       true, p, concurrency, tile_ctas);
+                       true, p, concurrency, tile_ctas, after_scatter);
 }
 
 template <bool kBF16, int D>
 static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                  const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                   bool pdl) {
   constexpr int smem = split_smem_bytes<D>();
   auto kern = split_attention_kernel<kBF16, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(attention_ctas(D, num_sms)), dim3(SplitCfg<D>::kWarps * 32),
-                       smem, stream, pdl, kmap, vmap, p);
+  return launch_kernel(kern, dim3(ctas), dim3(SplitCfg<D>::kWarps * 32), smem, stream, pdl, kmap,
+                       vmap, p);
+}
+
+int split_ctas(const AttnParams& p, int num_sms) {
+  // items <= H_kv x (sum over sequences of ceil(n G / 16)) x splits, and a sequence splits
+  // at most ceil(max_blocks / kMinSplitPages) ways: no more warps than that can find work
+  const int64_t per_split = static_cast<int64_t>(p.T) * p.G / 16 + 1 + p.B;
+  int64_t splits = (static_cast<int64_t>(p.max_blocks) + kMinSplitPages - 1) / kMinSplitPages;
+  splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
+  const int64_t items = static_cast<int64_t>(p.H_kv) * per_split * splits;
+  const int warps = attention_warps(p.D);
+  const int64_t need = (items + warps - 1) / warps;
+  const int full = attention_ctas(p.D, num_sms);
+  return static_cast<int>(need < full ? (need < 1 ? 1 : need) : full);
 }
 
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                   const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                    bool pdl) {
   if (p.D == 128)
-    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, num_sms, stream, pdl)
-                : launch_split_t<false, 128>(p, kmap, vmap, num_sms, stream, pdl);
-  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, num_sms, stream, pdl)
-              : launch_split_t<false, 64>(p, kmap, vmap, num_sms, stream, pdl);
+    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, ctas, stream, pdl)
+                : launch_split_t<false, 128>(p, kmap, vmap, ctas, stream, pdl);
+  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, ctas, stream, pdl)
+              : launch_split_t<false, 64>(p, kmap, vmap, ctas, stream, pdl);
 }
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,

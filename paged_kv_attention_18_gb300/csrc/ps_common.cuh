@@ -44,13 +44,14 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// One unit of attention work: 16 packed query rows of one sequence and one KV head,
-// over the KV pages [page_begin, page_end) (one split of the context).
+// One unit of attention work: packed query rows of one sequence and one KV head (16 for
+// the split kernel; query tiles for the tile kernel), over the KV pages
+// [page_begin, page_end) (one split of the context).
 struct __align__(16) WorkItem {
   int seq;         // sequence index b
   int kv;          // KV head
-  int row0;        // first packed row (query index * G + group member) of the 16
-  int nrows;       // valid rows, 1..16
+  int row0;        // first packed row (query index * G + group member) of the item
+  int nrows;       // valid rows: 1..16 (split kernel), the first query tile's (tile kernel)
   int page_begin;  // first KV page (16 keys) of this split
   int page_end;    // one past the last page needed by these rows in this split
   int split;       // split index s

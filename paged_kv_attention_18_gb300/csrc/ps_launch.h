@@ -39,7 +39,7 @@ struct AttnParams {
   float* part_o;                 // [cap_part, D] normalised partial outputs
   int cap_items, cap_part;
   int* err;                      // device error word
-  int32_t* slots;                // [T] slot of every token, written by the planner (or null)
+  int32_t* slots;                // [T] slot of every token, written by the step's scatter
 };
 
 // Launch `kern` on `s`; with `pdl` the launch may overlap the tail of the previous kernel
@@ -68,6 +68,14 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
                                      void* k_pool, void* v_pool, int T, int H_kv, int D,
                                      int num_blocks, int* err, int num_sms, cudaStream_t stream,
                                      bool pdl = false);
+
+// The step's KV scatter with its slot mapping (the first kernel of ps_attention_step): the
+// slot of every packed token is written to `slots` and its K/V rows to the pools.
+cudaError_t launch_step_scatter(const void* k, const void* v, const int32_t* block_tables,
+                                int max_blocks, const int32_t* seq_lens, const int32_t* qsl, int B,
+                                int T, int H_kv, int D, int num_blocks, int32_t* slots,
+                                void* k_pool, void* v_pool, int* err, int num_sms,
+                                cudaStream_t stream);
 
 // Copy n whole blocks (16 rows x H_kv x D, K and V): dst block dst_ids[i] of (dst_k, dst_v)
 // gets src block src_ids[i] of (src_k, src_v). Pools may be device or pinned host memory.
@@ -107,8 +115,11 @@ cudaError_t launch_spec_accept(const SpecParams& a, cudaStream_t stream);
 int attention_ctas(int D, int num_sms);
 int attention_warps(int D);
 
-// concurrency: split-kernel warps; tile_ctas: tile-kernel CTAs (work is sized for both)
-cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, cudaStream_t stream);
+// concurrency: split-kernel warps; tile_ctas: tile-kernel CTAs (work is sized for both).
+// after_scatter: the step's scatter kernel precedes the planner on the stream; the planner
+// then runs beside it and waits for it only before it ends.
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, bool after_scatter,
+                        cudaStream_t stream);
 
 // Query tokens per 128-row tile for G query heads per KV head (0 = use the split kernel).
 int tile_tokens(int G);
@@ -117,8 +128,12 @@ cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensor
                                   const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
                                   cudaStream_t stream, bool pdl);
 
+// CTAs for the split kernel: the full grid, or fewer when the batch's shape (T, B, the
+// block-table width) bounds its work items below one per warp of the full grid.
+int split_ctas(const AttnParams& p, int num_sms);
+
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream,
+                                   const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                    bool pdl);
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,
@@ -135,8 +150,8 @@ size_t partial_bytes(int64_t cap_part, int D);
 // False when even that does not fit.
 bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink);
 
-// The new tokens' K/V to scatter into the pools right after planning (the planner writes
-// their slots into AttnParams::slots).
+// The new tokens' K/V to scatter into the pools (the scatter writes their slots into
+// AttnParams::slots).
 struct ScatterArgs {
   const void* k;
   const void* v;

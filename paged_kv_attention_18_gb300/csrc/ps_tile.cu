@@ -458,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // on columns 32h..32h+31, which the loads of halves <= h have already read
         const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
         float m_tile = -INFINITY;
+        // l holds the earlier tiles' sum; this tile's halves are summed apart, so that a
+        // reference moved in half 1 can re-sum the half-0 P it re-rounds
+        float l_half0 = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t v[64];
@@ -487,12 +490,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha = move && m_ref != -INFINITY ? fast_exp2(m_ref - m_half) : 1.f;
             if (j > 0) rescale_o(alpha);
             l *= alpha;
-            if (h == 1) {  // the half of P already written: columns 0..31
+            if (h == 1) {
+              // the half of P already written (columns 0..31) is scaled and rounded again;
+              // its sum is taken anew from the values the PV product will read
               uint32_t q[32];
               tmem_ld32(tS, q);
               tmem_ld_wait();
+              float2 lq0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-              for (int e = 0; e < 32; ++e) q[e] = scale_pair<kBF16>(q[e], alpha);
+              for (int e = 0; e < 32; ++e) {
+                q[e] = scale_pair<kBF16>(q[e], alpha);
+                add_pair_exact<kBF16>(lq0[e & 1], q[e]);
+              }
+              l_half0 = (lq0[0].x + lq0[0].y) + (lq0[1].x + lq0[1].y);
               tmem_st32(tS, q);
               tmem_st_wait();
             }
@@ -511,7 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[e / 2] = pack2<kBF16>(fast_exp2(x.x), fast_exp2(x.y));
             add_pair_exact<kBF16>(lq[(e / 2) & 1], pk[e / 2]);
           }
-          l += (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
+          const float l_h = (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
+          if (h == 0) l_half0 = l_h;
+          else l += l_half0 + l_h;
           tmem_st16(tS + 32 * h, pk);
           tmem_st16(tS + 32 * h + 16, pk + 16);
         }

@@ -246,6 +246,18 @@ def test_large_score_jumps_mid_context(dtype):
     # Keys of a few pool blocks are scaled up so the running max jumps by far more than
     # 2^8 (and often 2^64) in the middle of KV tiles: every rescale path of the kernels
     # must keep the result equal to the plain softmax.
+    #
+    # Such rows are sharply peaked: the output is a mix of one or two V rows. The kernels
+    # multiply V by probabilities rounded to the 16-bit input type (the tensor core takes
+    # both operands in one type), 2^-9 relative in bf16, and the reference is scaled
+    # lazily, so even the largest weight carries that rounding. A near-even mix of two V
+    # rows that lie d apart then moves by up to about d * 2^-10, and the output's own
+    # rounding adds half an ulp (2^-8 for |o| in [2, 4)). With N(0, 1) values in bf16 the
+    # two together can pass 1e-2 (0.0117 measured, equal bit for bit to a CPU model of
+    # the kernel's steps), so the bf16 case draws V at 0.35 times that scale: outputs stay
+    # below 2, where the plain bound holds, while the keys jump just as far. The f16 case
+    # keeps N(0, 1) values (rounding 2^-11: within 2e-3 at |o| < 2, half an output ulp
+    # more above).
     seqs = [(700, 300), (900, 5), (1500, 1), (400, 128), (2100, 40)]
     wl = W.simple_workload("jumps", seed=31, dtype=dtype, H_q=12, H_kv=2, D=128, seqs=seqs)
     vals = oracle.decode_bits(wl.k_pool, dtype)
@@ -253,7 +265,9 @@ def test_large_score_jumps_mid_context(dtype):
     hot = rng.choice(wl.num_blocks, size=wl.num_blocks // 6, replace=False)
     vals[hot] *= 40.0
     wl.k_pool = W.round_to_bits(vals.astype(np.float32), dtype)
-    # sharply peaked rows return nearly one V row, |o| up to ~4.5: at |o| >= 4 (bf16) the
-    # rounding of the output alone can exceed the bound, and only there the check adds
-    # half an output ulp (gpu_util.SLACK_FROM)
+    if dtype == "bf16":
+        wl.v_pool = W.round_to_bits((0.35 * oracle.decode_bits(wl.v_pool, dtype)).astype(np.float32),
+                                    dtype)
+        st = wl.steps[0]
+        st.v = W.round_to_bits((0.35 * oracle.decode_bits(st.v, dtype)).astype(np.float32), dtype)
     check_workload(wl)
