@@ -741,8 +741,10 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     const uint32_t vbase = kbase + kPage;
 
     // S = Q K^T for the page's 16 keys: two n8 tiles
+    // two accumulators per n8 tile (even and odd k steps) halve the dependent mma chain
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
+      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int mi = lane >> 3, rr = lane & 7;
       const int key = (mi >> 1) * 8 + rr;
 #pragma unroll
@@ -751,9 +753,14 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
         const uint32_t addr = kbase + (chunk >> 3) * (kBlockSize * 128) + swz128(key, chunk & 7);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(addr, b0, b1, b2, b3);
-        mma_16816<kBF16>(s[0], qa[kk], b0, b1);
-        mma_16816<kBF16>(s[1], qa[kk], b2, b3);
+        float (*acc)[4] = (kk & 1) ? s2 : s;
+        mma_16816<kBF16>(acc[0], qa[kk], b0, b1);
+        mma_16816<kBF16>(acc[1], qa[kk], b2, b3);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     }
     // causal mask, online softmax
     const int key0 = comp_page * kBlockSize + 2 * t4;
