@@ -174,7 +174,13 @@ size_t workspace_fixed_bytes(int T, int B, int H_q, int H_kv, bool headroom, int
   int64_t ct = tpt > 0 ? H_kv * ((T64 + tpt - 1) / tpt + B64) : 1;
   if (headroom) {
     ci += H_kv * split_seqs * kSplitGroupLimit * (kMaxSplits - 1);
-    if (tpt > 0) ct += H_kv * split_seqs * kTileSplitQTiles * (kMaxSplits - 1);
+    if (tpt > 0) {
+      // pairs of query tiles: half the query tiles (rounded up per sequence) over at most
+      // T G / (16 kTileMinGroups + 1) tile-class sequences (each has n G > 16 kTileMinGroups)
+      const int64_t tile_seqs = T64 * G / (16 * kTileMinGroups + 1) + 1;
+      const int64_t pairs = ((T64 + tpt - 1) / tpt + 1) / 2 + tile_seqs;
+      ct += H_kv * pairs * (kMaxSplits - 1);
+    }
   }
   if (ci < 1) ci = 1;
   if (ct < 1) ct = 1;

@@ -49,7 +49,6 @@ __device__ __forceinline__ int seq_splits(const SeqInfo& s, int pps_dec, int pps
   if (s.groups == 0) return 0;
   int pps;
   if (s.tile) {
-    if (s.qtiles > kTileSplitQTiles) return 1;
     pps = pps_tile;
   } else {
     if (s.groups > kSplitGroupLimit) return 1;
@@ -170,27 +169,32 @@ __device__ __forceinline__ int split_entries_before(const SeqInfo& s, int ns, in
   return acc;
 }
 
-// Sums of two values over the block, returned to every thread.
-__device__ longlong2 block_sum2_ll(longlong2 v, longlong2* sh) {
+// Sums of three values over the block, returned to every thread.
+struct Sum3 {
+  long long x, y, z;
+};
+__device__ Sum3 block_sum3_ll(Sum3 v, Sum3* sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
     v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
   }
   if (lane == 0) sh[wid] = v;
   __syncthreads();
   if (wid == 0) {
-    longlong2 w = lane < nw ? sh[lane] : make_longlong2(0, 0);
+    Sum3 w = lane < nw ? sh[lane] : Sum3{0, 0, 0};
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       w.x += __shfl_xor_sync(0xffffffffu, w.x, o);
       w.y += __shfl_xor_sync(0xffffffffu, w.y, o);
+      w.z += __shfl_xor_sync(0xffffffffu, w.z, o);
     }
     if (lane == 0) sh[0] = w;
   }
   __syncthreads();
-  const longlong2 t = sh[0];
+  const Sum3 t = sh[0];
   __syncthreads();
   return t;
 }
@@ -228,7 +232,7 @@ constexpr int kPlanMaxCtas = 64;
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
                                                     int tile_ctas, bool after_scatter) {
   __shared__ int4 sh4[32];
-  __shared__ longlong2 shl[32];
+  __shared__ Sum3 shl[32];
   extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
   pdl_launch_dependents();
@@ -259,20 +263,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   }
 
   // cost of the batch in pages read, per kernel
-  long long wd = 0, wt = 0;
+  long long wd = 0, wt = 0, pairs = 0;
   for (int b = tid; b < p.B; b += nth) {
     const SeqInfo s = seq_info(p, qsl, lens, b);
     if (!s.valid) {
       record_error(p.err, kDevBadSequence);
       continue;
     }
-    if (s.tile) wt += static_cast<long long>(s.qtiles) * s.pages;
-    else wd += static_cast<long long>(s.groups) * s.pages;
+    if (s.tile) {
+      wt += static_cast<long long>(s.qtiles) * s.pages;
+      pairs += (s.qtiles + 1) / 2;
+    } else {
+      wd += static_cast<long long>(s.groups) * s.pages;
+    }
   }
-  const longlong2 W = block_sum2_ll(make_longlong2(wd, wt), shl);
+  const Sum3 W = block_sum3_ll(Sum3{wd, wt, pairs}, shl);
   const long long Wd = W.x * p.H_kv, Wt = W.y * p.H_kv;
   int pps_d = pages_per_split(Wd, concurrency, 1);
-  int pps_t = pages_per_split(Wt, tile_ctas, kTilePagesAlign);
+  // Tile items carry a fixed cost (query tiles loaded, the output written), so prefill
+  // chunks split their context only when the batch has fewer unsplit tile items than half
+  // the tile kernel's CTAs (few short chunks, or short chunks at the end of long contexts).
+  int pps_t = 2 * W.z * p.H_kv < tile_ctas ? pages_per_split(Wt, tile_ctas, kTilePagesAlign)
+                                            : (1 << 24);
 
   // per sequence: split-kernel items, tile-kernel items (pairs of query tiles), partial
   // entries and split tokens; coarser splits while the lists overflow the workspace
@@ -836,6 +848,11 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
 // ----------------------------------------------------------------------------------
 // A fixed grid walks the planner's list of split tokens, so a batch with no split rows
 // costs one small launch.
+#ifndef PS_COMBINE_UNROLL
+#define PS_COMBINE_UNROLL 8
+#endif
+constexpr int kCombineUnroll = PS_COMBINE_UNROLL;
+
 template <bool kBF16, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
   pdl_launch_dependents();
@@ -860,12 +877,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    // four partials' loads in flight per round
-    for (int s0 = 0; s0 < ns; s0 += 4) {
-      float ws[4];
-      float4 v[4];
+    // kCombineUnroll partials' loads in flight per round
+    for (int s0 = 0; s0 < ns; s0 += kCombineUnroll) {
+      float ws[kCombineUnroll];
+      float4 v[kCombineUnroll];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kCombineUnroll; ++u) {
         const int s = s0 + u;
         ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -882,7 +899,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kCombineUnroll; ++u) {
         acc[0] += ws[u] * v[u].x;
         acc[1] += ws[u] * v[u].y;
         if constexpr (kPer == 4) {
@@ -911,6 +928,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
 int attention_warps(int D) { return D == 128 ? SplitCfg<128>::kWarps : SplitCfg<64>::kWarps; }
 int attention_ctas(int D, int num_sms) { (void)D; return num_sms * PS_SPLIT_CTAS_PER_SM; }
 
+// Threads per planner CTA: a small batch needs fewer (its scans and barriers span fewer
+// warps); up to 1024.
+#ifndef PS_PLAN_MIN_THREADS
+#define PS_PLAN_MIN_THREADS 256
+#endif
+static int plan_threads(int B) {
+  int t = (B + 31) / 32 * 32;
+  t = t < PS_PLAN_MIN_THREADS ? PS_PLAN_MIN_THREADS : t;
+  return t > 1024 ? 1024 : t;
+}
+
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, bool after_scatter,
                         cudaStream_t stream) {
   const int smem =
@@ -927,8 +955,8 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, boo
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
   // programmatic dependent launch: the planner's CTAs may start while the kernel before
   // them on the stream finishes (see plan_kernel for what they wait for, and when)
-  return launch_kernel(plan_kernel, dim3(ctas), dim3(1024), static_cast<size_t>(smem), stream,
-                       true, p, concurrency, tile_ctas, after_scatter);
+  return launch_kernel(plan_kernel, dim3(ctas), dim3(plan_threads(p.B)), static_cast<size_t>(smem),
+                       stream, true, p, concurrency, tile_ctas, after_scatter);
 }
 
 template <bool kBF16, int D>

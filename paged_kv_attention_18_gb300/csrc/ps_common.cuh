@@ -17,7 +17,6 @@ constexpr int kMaxSplits = 32;      // KV splits of one query row, at most
 constexpr int kMinSplitPages = 8;   // pages in one split, at least
 constexpr int kSplitGroupLimit = 4; // only sequences with <= this many 16-row groups split
 constexpr int kTileMinGroups = 4;   // sequences with more 16-row groups than this use tiles
-constexpr int kTileSplitQTiles = 2; // tile-class sequences with <= this many query tiles split
 constexpr int kTilePagesAlign = 8;  // tile-class split sizes are whole 128-key tiles
 
 // Device error codes, stored in the library's device error word. A kernel that meets
