@@ -288,7 +288,9 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
     if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, s, true)) != cudaSuccess)
       return cuda_fail(e, "tile attention kernel");
   }
-  {
+  // A split holds at least kMinSplitPages pages, so with no block table longer than that
+  // no row is split and there is nothing to combine.
+  if (p.max_blocks > kMinSplitPages) {
     Timed tm(4, s);
     if ((e = launch_combine(p, bf16, num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
   }

@@ -944,8 +944,9 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, boo
   const int smem =
       p.B <= kPlanSmemSeqs ? kPlanSmemArrays * (p.B + 1) * static_cast<int>(sizeof(int)) : 0;
   if (smem > 48 * 1024) {
+    static std::atomic<uint64_t> done{0};
     const cudaError_t e =
-        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        ensure_smem_limit(plan_kernel, kPlanSmemArrays * (kPlanSmemSeqs + 1) * 4, done);
     if (e != cudaSuccess) return e;
   }
   // enough CTAs that the token and item passes are short (a CTA's warps share its SM's
@@ -965,7 +966,8 @@ static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
                                   bool pdl) {
   constexpr int smem = split_smem_bytes<D>();
   auto kern = split_attention_kernel<kBF16, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t e = ensure_smem_limit(kern, smem, done);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(ctas), dim3(SplitCfg<D>::kWarps * 32), smem, stream, pdl, kmap,
                        vmap, p);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ps {
 
 struct WorkItem;
@@ -41,6 +43,20 @@ struct AttnParams {
   int* err;                      // device error word
   int32_t* slots;                // [T] slot of every token, written by the step's scatter
 };
+
+// Raise `kern`'s dynamic shared-memory limit to `bytes` once per device: the setting lasts
+// for the process, and repeating it on every launch only costs host time.
+template <typename Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return ge;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Launch `kern` on `s`; with `pdl` the launch may overlap the tail of the previous kernel
 // on the stream (the kernel waits with pdl_wait before using that kernel's results).

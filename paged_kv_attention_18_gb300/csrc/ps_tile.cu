@@ -353,13 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // per K/V tile: PV of A, next S of A, PV of B, next S of B. A query tile's next S
         // overwrites its P in TMEM, so it is issued after that tile's PV (in order).
+        // A query tile's O is final after its last PV: its epilogue may start while the
+        // other tile's last PV still waits for P.
         for (int j = 0; j < nt && ok; ++j)
           for (int q = 0; q < ng && ok; ++q) {
             ok = issue_pv(q, j);
             if (ok && j + 1 < nt) ok = issue_s(q, j + 1);
+            if (ok && j + 1 == nt) umma_commit(&bars->o_done[q]);
           }
         if (!ok) break;
-        for (int q = 0; q < ng; ++q) umma_commit(&bars->o_done[q]);
         g += nt;
         ++qa;
         if (ng > 1) ++qb;
@@ -634,7 +636,8 @@ static cudaError_t launch_tile_t(const AttnParams& p, const CUtensorMap& kmap,
                                  cudaStream_t stream, bool pdl) {
   constexpr int smem = TileSmem<D>::kBytes;
   auto kern = tile_attention_kernel<kBF16, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t e = ensure_smem_limit(kern, smem, done);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(num_sms), dim3(kThreads), smem, stream, pdl, kmap, vmap, qmap,
                        p);
