@@ -55,6 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # committed ncu DRAM counters of the dominant kernels, with the sources they were taken on
 TRAFFIC_FILES = {
     ("split_attention", "qwen15b_decode"): "split_attention_qwen15b_decode_traffic.json",
+    ("split_attention", "spec_verify_long"): "split_attention_spec_verify_long_traffic.json",
+    ("tile_attention", "prefix_chunked_prefill"): "tile_attention_prefix_chunked_prefill_traffic.json",
     ("tile_attention", "long_prefill"): "tile_attention_long_prefill_traffic.json",
 }
 # the source text each kernel is built from: a whole file, or (file, first line, line that
