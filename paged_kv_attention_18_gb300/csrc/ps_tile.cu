@@ -144,6 +144,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  {
+    // Rows past the G * tpt rows a query tile holds are never written by TMA: zero them
+    // once, so that their S is 0 and they go through the softmax like any unmasked row.
+    const int rows = p.G * p.tpt;
+    const int words = (kRows - rows) * 128 / 16;  // 16-byte words per sub-tile
+    for (int i = threadIdx.x; i < 2 * kHalves * words; i += kThreads) {
+      const int sub = i / words, wd = i - sub * words;
+      reinterpret_cast<uint4*>(smem + L::kOffQ + sub * kSub + rows * 128)[wd] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();  // visible to the tensor core's reads
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -432,7 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
       float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
-        const int lim = key_hi - (pb * kBlockSize + j * kKeys);  // visible columns: c <= lim
+        // visible columns: c <= lim (a row past the tile's rows is computed unmasked and
+        // not written)
+        const int lim = valid ? key_hi - (pb * kBlockSize + j * kKeys) : kKeys;
         if (!wait(&bars->s_full[grp], sc & 1)) { ok = false; break; }
         ++sc;
         tc_fence_after();
