@@ -41,7 +41,7 @@ constexpr int kPagesPerTile = kKeys / kBlockSize;
 constexpr int kSub = kRows * 128; // bytes of one [128 rows x 64 elements] swizzled sub-tile
 constexpr int kKStages = 3;       // K tile stages (freed once both products S have read them)
 constexpr int kVStages = 2;       // V tile stages (freed once both products PV have read them)
-constexpr int kItemRing = 4;
+constexpr int kItemRing = 4;     // item indices handed from the fetching warp to the others
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
 // A larger jump inside a tile moves the reference at once; below it P can reach 2^kMove,
@@ -62,7 +62,8 @@ struct TileSmem {
   static constexpr int kOffK = kOffQ + 2 * kQ;
   static constexpr int kOffV = kOffK + kKStages * kK;
   static constexpr int kOffBar = kOffV + kVStages * kK;
-  static constexpr int kBytes = kOffBar + 512 + 1024;  // barriers, ring; alignment slack
+  static constexpr int kOffItems = kOffBar + 512;             // work items in flight
+  static constexpr int kBytes = kOffItems + 2 * kItemRing * 64 + 1024;  // + alignment slack
 };
 static_assert(TileSmem<128>::kBytes <= 232448, "tile kernel shared memory");
 
@@ -110,6 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   TileBars* bars = reinterpret_cast<TileBars*>(smem + L::kOffBar);
+  // Records of the items in flight: item it's record sits in slot it % (2 * kItemRing).
+  // The fetching warp runs at most kItemRing items ahead of the slowest reader (the index
+  // ring), so a slot is written again only after every reader has finished with it.
+  WorkItem* items = reinterpret_cast<WorkItem*>(smem + L::kOffItems);
   const uint32_t sQ = smem_u32(smem + L::kOffQ);
   const uint32_t sK = smem_u32(smem + L::kOffK);
   const uint32_t sV = smem_u32(smem + L::kOffV);
@@ -196,18 +201,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         const int slot = it % kItemRing;
         if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
-        if (lane == 0) {
-          idx = atomicAdd(p.hdr + 5, 1);
+        if (lane < 4) {
+          // lanes 0..3 copy the item's record into its shared-memory slot, lane 0 hands
+          // out the index (its arrival orders the copy before every reader's wait)
+          if (lane == 0) idx = atomicAdd(p.hdr + 5, 1);
+          idx = __shfl_sync(0x0000000fu, idx, 0);
           if (idx >= n_items) idx = -1;
-          bars->item_idx[slot] = idx;
-          mbar_arrive(&bars->item_full[slot]);
+          if (idx >= 0)
+            reinterpret_cast<uint4*>(items + it % (2 * kItemRing))[lane] =
+                __ldg(reinterpret_cast<const uint4*>(p.tile_items + idx) + lane);
+          __syncwarp(0x0000000fu);
+          if (lane == 0) {
+            bars->item_idx[slot] = idx;
+            mbar_arrive(&bars->item_full[slot]);
+          }
         }
+        __syncwarp();
         idx = __shfl_sync(0xffffffffu, idx, 0);
       } else {
         idx = next_item(it);
       }
       if (idx < 0) break;
-      const WorkItem& w = p.tile_items[idx];
+      const WorkItem& w = items[it % (2 * kItemRing)];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int seq = w.seq, kv = w.kv;
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = bars->item_idx[slot];
         mbar_arrive(&bars->item_empty[slot]);
         if (idx < 0) break;
-        const WorkItem& w = p.tile_items[idx];
+        const WorkItem& w = items[it % (2 * kItemRing)];
         const int pb = w.page_begin, pe = w.page_end;
         if (!tile_item_ok(w, p)) {
           record_error(p.err, kDevPlanOverflow);  // a plan this launch cannot use
@@ -393,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
       if (idx < 0) break;
-      const WorkItem& w = p.tile_items[idx];
+      const WorkItem& w = items[it % (2 * kItemRing)];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; ok; ++it) {
       const int idx = next_item(it);
       if (idx < 0) break;
-      const WorkItem& w = p.tile_items[idx];
+      const WorkItem& w = items[it % (2 * kItemRing)];
       const int pb = w.page_begin, pe = w.page_end;
       if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
@@ -437,8 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key_hi = min(pos, pe * kBlockSize - 1);  // last key of the item this row sees
       // the row's split count and partial base, fetched now so that the epilogue's
       // stores do not wait on them
+      // (both loads are issued at once; nothing waits for them before the epilogue)
       const int ns_t = valid ? __ldg(p.tok_ns + tok) : 0;
-      const int tok_part = valid && ns_t > 1 ? __ldg(p.tok_base + tok) : 0;
+      const int tok_part = valid ? __ldg(p.tok_base + tok) : 0;
       // m_ref: the reference max (log2 units) that P, O and l are currently taken against;
       // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
       float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
@@ -451,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // This group's previous PV has completed (this S was issued after it): O is stable.
         auto rescale_o = [&](float alpha) {
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(tO + c * 32, v);
@@ -476,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // l holds the earlier tiles' sum; this tile's halves are summed apart, so that a
         // reference moved in half 1 can re-sum the half-0 P it re-rounds
         float l_half0 = 0.f;
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t v[64];
           tmem_ld32(tS + 64 * h, v);
@@ -562,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t row_off = write ? (static_cast<int64_t>(tok) * p.H_q + head) * D : -1;
         const int g8 = lane & ~7, b = lane & 7;
         uint16_t* out = static_cast<uint16_t*>(p.out);
-#pragma unroll
+#pragma unroll 1
         for (int c2 = 0; c2 < D / 64; ++c2) {
           uint32_t v[64];
           tmem_ld32(tO + c2 * 64, v);
@@ -601,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // split partials (fp32), one row per lane
-#pragma unroll
+#pragma unroll 1
         for (int c2 = 0; c2 < D / 64; ++c2) {
           uint32_t v[64];
           tmem_ld32(tO + c2 * 64, v);
