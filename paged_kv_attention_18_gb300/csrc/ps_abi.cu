@@ -261,9 +261,23 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   if ((rc = make_pool_map(&kmap, k_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if (tiles && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
+  cudaError_t e;
+  if (direct_fits(p, num_sms)) {
+    // a small batch: the whole step (scatter included) in one launch, without a plan
+    p.direct = 1;
+    if (scatter) {
+      p.new_k = scatter->k;
+      p.new_v = scatter->v;
+      p.k_pool = k_pool;
+      p.v_pool = v_pool;
+    }
+    Timed tm(3, s);
+    if ((e = launch_direct_attention(p, bf16, kmap, vmap, num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "split attention kernel (direct)");
+    return PS_OK;
+  }
   const int split_grid = split_ctas(p, num_sms);
   const int concurrency = split_grid * attention_warps(p.D);
-  cudaError_t e;
   // With the step's K/V to cache, the scatter goes first and the planner runs beside it;
   // every later launch is chained with programmatic dependent launch.
   if (scatter) {

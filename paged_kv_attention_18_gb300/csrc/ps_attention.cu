@@ -575,7 +575,10 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
   __syncwarp();
   pdl_wait();  // the plan (and the KV scatter) before this kernel are complete
 
-  const int n_items = *reinterpret_cast<volatile int*>(p.hdr);
+  // direct mode: one item per (sequence, KV head), handed out round robin; otherwise the
+  // plan's list, fetched through its counter
+  const int n_items = p.direct ? p.B * p.H_kv : *reinterpret_cast<volatile int*>(p.hdr);
+  int direct_next = blockIdx.x * W + warp;
   const uint64_t policy = l2_policy_evict_first();
 
   // ---------------- issue side (runs ahead of compute by up to S pages) -------------
@@ -592,19 +595,77 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
                  : -1;
   };
 
+  // Direct mode: the record of item idx = (sequence idx / H_kv, KV head idx % H_kv), all
+  // of the sequence's rows (n * G <= 16) over its whole context, in one split; lane k
+  // returns field k. With the step's K/V given, the warp first writes the sequence's new
+  // rows of this head to the pools at their slots (the head-0 warp also records the
+  // slots), exactly as the step's scatter does, then orders those writes before its TMA
+  // reads of the pages. An invalid sequence records an error and gives an empty item.
+  auto direct_item = [&](int idx) -> int {
+    const int b = idx / p.H_kv, kv = idx - b * p.H_kv;
+    const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), L = __ldg(p.seq_lens + b);
+    const int n = q1 - q0, pe = (L + kBlockSize - 1) / kBlockSize;
+    if (idx == 0 && lane == 0 && (__ldg(p.qsl) != 0 || __ldg(p.qsl + p.B) != p.T))
+      record_error(p.err, kDevBadSequence);  // tokens outside every sequence
+    if (q0 < 0 || q1 > p.T || n < 0) {
+      if (lane == 0) record_error(p.err, kDevBadSequence);
+      return 0;
+    }
+    const bool bad = n > L || n * p.G > 16 || pe > p.max_blocks;
+    if (bad && lane == 0) record_error(p.err, kDevBadSequence);
+    if (p.new_k != nullptr) {
+      constexpr int kVecs = D / 8;  // 16-byte chunks of one head's row
+      const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+      for (int t = 0; t < n; ++t) {
+        int slot = -1;
+        if (!bad) {
+          const int pos = L - n + t;
+          const int blk = __ldg(bt + pos / kBlockSize);
+          if (blk >= 0 && blk < p.num_blocks) slot = blk * kBlockSize + pos % kBlockSize;
+          else if (lane == 0) record_error(p.err, kDevBadBlockId);
+        }
+        if (kv == 0 && lane == 0) p.slots[q0 + t] = slot;
+        if (slot >= 0 && lane < kVecs) {
+          const int64_t src = (static_cast<int64_t>(q0 + t) * p.H_kv + kv) * kVecs + lane;
+          const int64_t dst = (static_cast<int64_t>(slot) * p.H_kv + kv) * kVecs + lane;
+          static_cast<uint4*>(p.k_pool)[dst] = __ldcs(static_cast<const uint4*>(p.new_k) + src);
+          static_cast<uint4*>(p.v_pool)[dst] = __ldcs(static_cast<const uint4*>(p.new_v) + src);
+        }
+      }
+      fence_proxy_async_global();
+      __syncwarp();
+    }
+    if (bad || n == 0) return 0;
+    int f = 0;
+    f = lane == 0 ? b : f;
+    f = lane == 1 ? kv : f;
+    f = lane == 3 ? n * p.G : f;   // rows; row0 (lane 2) and page_begin (lane 4) are 0
+    f = lane == 5 ? pe : f;
+    f = lane == 7 ? 1 : f;         // one split (lane 6: split 0)
+    f = lane == 8 ? L : f;
+    f = lane == 9 ? n : f;
+    f = lane == 10 ? q0 : f;
+    return f;
+  };
+
   // Issue the next page of work into stage g_issue % S; false when nothing is left.
   auto issue_one = [&]() -> bool {
     while (iss_page >= iss_end) {
       if (no_more) return false;
       int idx = 0;
-      if (lane == 0) idx = atomicAdd(p.hdr + 1, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (p.direct) {
+        idx = direct_next;
+        direct_next += gridDim.x * W;
+      } else {
+        if (lane == 0) idx = atomicAdd(p.hdr + 1, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      }
       if (idx >= n_items) {
         no_more = true;
         return false;
       }
       const int* src = reinterpret_cast<const int*>(p.items + idx);
-      const int v = lane < 16 ? __ldg(src + lane) : 0;
+      const int v = p.direct ? direct_item(idx) : lane < 16 ? __ldg(src + lane) : 0;
       const int pb = __shfl_sync(0xffffffffu, v, 4), pe = __shfl_sync(0xffffffffu, v, 5);
       if (pe <= pb) continue;  // no key of this split is visible to these rows
       WorkItem* slot = ring + (ring_tail % kRing);
@@ -709,7 +770,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     for (int r = 0; r < 2; ++r) {
       if (row_tok[r] < 0) continue;
       const int tok = row_tok[r];
-      const int ns_t = __ldg(p.tok_ns + tok);
+      const int ns_t = p.direct ? 1 : __ldg(p.tok_ns + tok);
       if (cur.split >= ns_t) continue;  // this split holds no key visible to the row
       const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
       if (ns_t == 1) {
@@ -971,6 +1032,22 @@ static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(ctas), dim3(SplitCfg<D>::kWarps * 32), smem, stream, pdl, kmap,
                        vmap, p);
+}
+
+bool direct_fits(const AttnParams& p, int num_sms) {
+  const int64_t items = static_cast<int64_t>(p.B) * p.H_kv;
+  return static_cast<int64_t>(p.T) * p.G <= 16 && p.max_blocks <= kDirectMaxPages &&
+         items <= static_cast<int64_t>(num_sms) * attention_warps(p.D);
+}
+
+cudaError_t launch_direct_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                    const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(p.B) * p.H_kv;
+  const int warps = attention_warps(p.D);
+  int64_t ctas = (items + warps - 1) / warps;
+  if (ctas < 1) ctas = 1;
+  if (ctas > num_sms) ctas = num_sms;
+  return launch_split_attention(p, bf16, kmap, vmap, static_cast<int>(ctas), stream, false);
 }
 
 int split_ctas(const AttnParams& p, int num_sms) {

@@ -42,6 +42,14 @@ struct AttnParams {
   int cap_items, cap_part;
   int* err;                      // device error word
   int32_t* slots;                // [T] slot of every token, written by the step's scatter
+  // Direct mode (small batches, see launch_direct_attention): the split kernel takes one
+  // item per (sequence, KV head) straight from seq_lens and qsl instead of a plan, and,
+  // with new_k set, first scatters the step's K/V into the pools.
+  int direct;
+  const void* new_k;             // [T, H_kv, D] the step's K and V, or null
+  const void* new_v;
+  void* k_pool;                  // [num_blocks, 16, H_kv, D]
+  void* v_pool;
 };
 
 // Raise `kern`'s dynamic shared-memory limit to `bytes` once per device: the setting lasts
@@ -154,6 +162,20 @@ cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtenso
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,
                            bool pdl);
+
+// Largest block-table width (pages) the direct mode takes: one warp streams a sequence's
+// whole context, which for this many pages takes no longer than a plan would.
+constexpr int kDirectMaxPages = 64;
+
+// True when a batch of T packed tokens fits the direct mode: every sequence's rows (n * G
+// <= T * G) fit one 16-row group, no block table is wide enough for the planner to split a
+// row, and the items fit a few waves of the split kernel's warps.
+bool direct_fits(const AttnParams& p, int num_sms);
+
+// The whole step in one launch for such a batch: the split kernel in direct mode (p.direct
+// and, for a step with K/V to cache, p.new_k / p.new_v / p.k_pool / p.v_pool set).
+cudaError_t launch_direct_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                    const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
 
 // Workspace bytes before the split partials (header, work lists, per-token tables);
 // `headroom` reserves work-list room for splitting long contexts.

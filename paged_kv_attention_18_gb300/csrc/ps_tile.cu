@@ -227,18 +227,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pe <= pb || !tile_item_ok(w, p)) continue;
       const int seq = w.seq, kv = w.kv;
       const int nt = (pe - pb + kPagesPerTile - 1) / kPagesPerTile;
-      if (is_k) {
-        // query tiles: whole tokens x the G heads of this KV head. Each tile has its own
-        // buffer, refilled as soon as that tile's last S of the previous item has read it.
+      // query tiles (K warp): whole tokens x the G heads of this KV head. Each tile has its
+      // own buffer, refilled as soon as that tile's last S of the previous item has read
+      // it. They are loaded after the item's first K tile, whose stage frees earlier.
+      auto load_q = [&]() -> bool {
         const bool has_b = w.pad[0] > 0;
         const int tok = w.tok0 + w.row0 / p.G;
         const uint32_t tile_bytes = kHalves * 64 * 2 * p.G * p.tpt;
-        bool qok = true;
         for (int q = 0; q < (has_b ? 2 : 1); ++q) {
-          if (!wait(&bars->q_empty[q], ((q ? qb : qa) & 1) ^ 1)) {
-            qok = false;
-            break;
-          }
+          if (!wait(&bars->q_empty[q], ((q ? qb : qa) & 1) ^ 1)) return false;
           if (lane == 0) {
             mbar_arrive_expect_tx(&bars->q_full[q], tile_bytes);
             for (int h = 0; h < kHalves; ++h)
@@ -246,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           h * 64, kv * p.G, tok + q * p.tpt);
           }
         }
-        if (!qok) break;
         ++qa;
         if (has_b) ++qb;
-      }
+        return true;
+      };
       // K (or V) tiles of 8 pages; pages past the split read the zero fill. One lane per
       // page copy: lane = page * kHalves + half (64-element half of the head).
       const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
@@ -284,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kv * D + h * 64, row);
         }
         ++g;
+        if (is_k && j == 0 && !load_q()) { ok = false; break; }
       }
       if (!ok) break;
     }

@@ -271,3 +271,44 @@ def test_large_score_jumps_mid_context(dtype):
         st = wl.steps[0]
         st.v = W.round_to_bits((0.35 * oracle.decode_bits(st.v, dtype)).astype(np.float32), dtype)
     check_workload(wl)
+
+
+# ------------------------------------------------------------------------------------
+# small batches: the whole step in one launch (no plan)
+# ------------------------------------------------------------------------------------
+SMALL_BATCHES = [
+    # (dtype, H_q, H_kv, D, [(context after the step, query tokens), ...])
+    ("f16", 4, 2, 64, [(1, 1), (15, 1), (16, 1), (17, 1), (100, 1), (31, 0), (64, 1)]),
+    ("bf16", 8, 2, 128, [(40, 4), (0, 0), (16, 0)]),          # one 16-row group, G = 4
+    ("bf16", 12, 2, 128, [(90, 2), (7, 0)]),                  # verify-like rows, G = 6
+    ("f16", 8, 8, 64, [(1024, 1), (513, 1)]),                 # 64 pages, MHA (G = 1)
+    ("bf16", 16, 1, 128, [(33, 1)]),                          # G = 16: one row group
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_BATCHES)))
+@pytest.mark.parametrize("separate", [False, True])
+def test_small_batches_in_one_launch(case, separate):
+    dt, H_q, H_kv, D, seqs = SMALL_BATCHES[case]
+    wl = W.simple_workload(f"small{case}", seed=40 + case, dtype=dt, H_q=H_q, H_kv=H_kv, D=D,
+                           seqs=seqs)
+    assert wl.steps[0].T * (H_q // H_kv) <= 16
+    check_workload(wl, separate_calls=separate)
+
+
+def test_small_batch_skips_the_plan():
+    small = W.simple_workload("one_launch", seed=50, dtype="f16", H_q=4, H_kv=2, D=64,
+                              seqs=[(30, 1), (70, 1), (5, 1)])
+    large = W.simple_workload("planned", seed=51, dtype="f16", H_q=4, H_kv=2, D=64,
+                              seqs=[(30, 1)] * 9)  # 9 tokens x G = 2: 18 rows
+    launches = {}
+    for wl in (small, large):
+        pools = DevicePools(wl)
+        binding.profile_begin(8)
+        run_step(wl, wl.steps[0], pools)
+        prof = binding.profile_end()
+        launches[wl.name] = {k: n for k, (_, n) in prof.items()}
+    assert launches["one_launch"]["plan"] == 0 and launches["one_launch"]["split_attention"] == 1
+    assert launches["one_launch"]["reshape_and_cache"] == 0
+    assert launches["planned"]["plan"] == 1
+    check_workload(small)
