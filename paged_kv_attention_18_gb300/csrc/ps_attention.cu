@@ -542,7 +542,7 @@ constexpr int split_smem_bytes() {
          SplitCfg<D>::kWarps * (SplitCfg<D>::kStages + 2) * 64;
 }
 
-template <bool kBF16, int D>
+template <bool kBF16, int D, bool kDirect>
 __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM)
     split_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
 
   // direct mode: one item per (sequence, KV head), handed out round robin; otherwise the
   // plan's list, fetched through its counter
-  const int n_items = p.direct ? p.B * p.H_kv : *reinterpret_cast<volatile int*>(p.hdr);
+  const int n_items = kDirect ? p.B * p.H_kv : *reinterpret_cast<volatile int*>(p.hdr);
   int direct_next = blockIdx.x * W + warp;
   const uint64_t policy = l2_policy_evict_first();
 
@@ -597,13 +597,47 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
 
   // Direct mode: the record of item idx = (sequence idx / H_kv, KV head idx % H_kv), all
   // of the sequence's rows (n * G <= 16) over its whole context, in one split; lane k
-  // returns field k. With the step's K/V given, the warp first writes the sequence's new
-  // rows of this head to the pools at their slots (the head-0 warp also records the
-  // slots), exactly as the step's scatter does, then orders those writes before its TMA
-  // reads of the pages. An invalid sequence records an error and gives an empty item.
-  auto direct_item = [&](int idx) -> int {
+  // returns field k, and bt_lane the sequence's block-table entry for page `lane`. With
+  // the step's K/V given, the sequence's new rows of this head are written to the pools
+  // at their slots (the head-0 warp also records the slots), exactly as the step's scatter
+  // does, just before the first page holding one of them is copied (scatter_new below).
+  // An invalid sequence records an error, gives an empty item and slots of -1.
+  int dir_seq = 0, dir_kv = 0, dir_q0 = 0, dir_n = 0, dir_L = 0, dir_first_new = 0;
+  bool dir_pending = false;
+  auto scatter_new = [&](int bt_lane, bool bad) {
+    constexpr int kVecs = D / 8;  // 16-byte chunks of one head's row
+    const int32_t* bt = p.block_tables + static_cast<int64_t>(dir_seq) * p.max_blocks;
+    for (int t = 0; t < dir_n; ++t) {
+      const int64_t src = (static_cast<int64_t>(dir_q0 + t) * p.H_kv + dir_kv) * kVecs + lane;
+      uint4 kk = make_uint4(0, 0, 0, 0), vv = kk;
+      if (!bad && lane < kVecs) {
+        kk = __ldcs(static_cast<const uint4*>(p.new_k) + src);
+        vv = __ldcs(static_cast<const uint4*>(p.new_v) + src);
+      }
+      int slot = -1;
+      if (!bad) {
+        const int pos = dir_L - dir_n + t, page = pos / kBlockSize;
+        const int e = __shfl_sync(0xffffffffu, bt_lane, page & 31);
+        const int blk = page < 32 ? e : __ldg(bt + page);
+        if (blk >= 0 && blk < p.num_blocks) slot = blk * kBlockSize + pos % kBlockSize;
+        else if (lane == 0) record_error(p.err, kDevBadBlockId);
+      }
+      if (dir_kv == 0 && lane == 0) p.slots[dir_q0 + t] = slot;
+      if (slot >= 0 && lane < kVecs) {
+        const int64_t dst = (static_cast<int64_t>(slot) * p.H_kv + dir_kv) * kVecs + lane;
+        static_cast<uint4*>(p.k_pool)[dst] = kk;
+        static_cast<uint4*>(p.v_pool)[dst] = vv;
+      }
+    }
+    fence_proxy_async_global();  // before the TMA copies of these pages
+    __syncwarp();
+  };
+  auto direct_item = [&](int idx, int& bt_lane) -> int {
     const int b = idx / p.H_kv, kv = idx - b * p.H_kv;
+    const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+    // lengths and the block-table row are loaded together
     const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), L = __ldg(p.seq_lens + b);
+    const int bt_raw = lane < p.max_blocks ? __ldg(bt + lane) : -1;
     const int n = q1 - q0, pe = (L + kBlockSize - 1) / kBlockSize;
     if (idx == 0 && lane == 0 && (__ldg(p.qsl) != 0 || __ldg(p.qsl + p.B) != p.T))
       record_error(p.err, kDevBadSequence);  // tokens outside every sequence
@@ -613,27 +647,17 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     }
     const bool bad = n > L || n * p.G > 16 || pe > p.max_blocks;
     if (bad && lane == 0) record_error(p.err, kDevBadSequence);
-    if (p.new_k != nullptr) {
-      constexpr int kVecs = D / 8;  // 16-byte chunks of one head's row
-      const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
-      for (int t = 0; t < n; ++t) {
-        int slot = -1;
-        if (!bad) {
-          const int pos = L - n + t;
-          const int blk = __ldg(bt + pos / kBlockSize);
-          if (blk >= 0 && blk < p.num_blocks) slot = blk * kBlockSize + pos % kBlockSize;
-          else if (lane == 0) record_error(p.err, kDevBadBlockId);
-        }
-        if (kv == 0 && lane == 0) p.slots[q0 + t] = slot;
-        if (slot >= 0 && lane < kVecs) {
-          const int64_t src = (static_cast<int64_t>(q0 + t) * p.H_kv + kv) * kVecs + lane;
-          const int64_t dst = (static_cast<int64_t>(slot) * p.H_kv + kv) * kVecs + lane;
-          static_cast<uint4*>(p.k_pool)[dst] = __ldcs(static_cast<const uint4*>(p.new_k) + src);
-          static_cast<uint4*>(p.v_pool)[dst] = __ldcs(static_cast<const uint4*>(p.new_v) + src);
-        }
-      }
-      fence_proxy_async_global();
-      __syncwarp();
+    bt_lane = !bad && lane < pe ? bt_raw : -1;
+    dir_seq = b;
+    dir_kv = kv;
+    dir_q0 = q0;
+    dir_n = n;
+    dir_L = L;
+    dir_first_new = (L - n) / kBlockSize;
+    dir_pending = false;
+    if (p.new_k != nullptr && n > 0) {
+      if (bad) scatter_new(bt_lane, true);  // slots of -1 only
+      else dir_pending = true;
     }
     if (bad || n == 0) return 0;
     int f = 0;
@@ -653,7 +677,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     while (iss_page >= iss_end) {
       if (no_more) return false;
       int idx = 0;
-      if (p.direct) {
+      if constexpr (kDirect) {
         idx = direct_next;
         direct_next += gridDim.x * W;
       } else {
@@ -665,7 +689,10 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
         return false;
       }
       const int* src = reinterpret_cast<const int*>(p.items + idx);
-      const int v = p.direct ? direct_item(idx) : lane < 16 ? __ldg(src + lane) : 0;
+      int bt_direct = -1;
+      int v;
+      if constexpr (kDirect) v = direct_item(idx, bt_direct);
+      else v = lane < 16 ? __ldg(src + lane) : 0;
       const int pb = __shfl_sync(0xffffffffu, v, 4), pe = __shfl_sync(0xffffffffu, v, 5);
       if (pe <= pb) continue;  // no key of this split is visible to these rows
       WorkItem* slot = ring + (ring_tail % kRing);
@@ -675,7 +702,17 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
       iss_kv = __shfl_sync(0xffffffffu, v, 1);
       iss_page = pb;
       iss_end = pe;
-      load_bt(pb);
+      if constexpr (kDirect) {  // pages 0..31 of the sequence, read by direct_item
+        bt_base = 0;
+        bt_reg = bt_direct;
+      } else {
+        load_bt(pb);
+      }
+    }
+    if (kDirect && dir_pending && iss_page >= dir_first_new) {
+      // direct mode: the new tokens' rows go to the pools before their first page's copy
+      scatter_new(bt_base == 0 ? bt_reg : -1, false);
+      dir_pending = false;
     }
     if (iss_page - bt_base >= 32) load_bt(iss_page);
     const int blk = __shfl_sync(0xffffffffu, bt_reg, iss_page - bt_base);
@@ -770,7 +807,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     for (int r = 0; r < 2; ++r) {
       if (row_tok[r] < 0) continue;
       const int tok = row_tok[r];
-      const int ns_t = p.direct ? 1 : __ldg(p.tok_ns + tok);
+      const int ns_t = kDirect ? 1 : __ldg(p.tok_ns + tok);
       if (cur.split >= ns_t) continue;  // this split holds no key visible to the row
       const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
       if (ns_t == 1) {
@@ -1021,12 +1058,12 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, boo
                        stream, true, p, concurrency, tile_ctas, after_scatter);
 }
 
-template <bool kBF16, int D>
+template <bool kBF16, int D, bool kDirect>
 static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                   bool pdl) {
   constexpr int smem = split_smem_bytes<D>();
-  auto kern = split_attention_kernel<kBF16, D>;
+  auto kern = split_attention_kernel<kBF16, D, kDirect>;
   static std::atomic<uint64_t> done{0};
   const cudaError_t e = ensure_smem_limit(kern, smem, done);
   if (e != cudaSuccess) return e;
@@ -1066,11 +1103,19 @@ int split_ctas(const AttnParams& p, int num_sms) {
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                    bool pdl) {
+  // the direct mode is its own instantiation, so the planned kernel carries none of it
+  if (p.direct) {
+    if (p.D == 128)
+      return bf16 ? launch_split_t<true, 128, true>(p, kmap, vmap, ctas, stream, pdl)
+                  : launch_split_t<false, 128, true>(p, kmap, vmap, ctas, stream, pdl);
+    return bf16 ? launch_split_t<true, 64, true>(p, kmap, vmap, ctas, stream, pdl)
+                : launch_split_t<false, 64, true>(p, kmap, vmap, ctas, stream, pdl);
+  }
   if (p.D == 128)
-    return bf16 ? launch_split_t<true, 128>(p, kmap, vmap, ctas, stream, pdl)
-                : launch_split_t<false, 128>(p, kmap, vmap, ctas, stream, pdl);
-  return bf16 ? launch_split_t<true, 64>(p, kmap, vmap, ctas, stream, pdl)
-              : launch_split_t<false, 64>(p, kmap, vmap, ctas, stream, pdl);
+    return bf16 ? launch_split_t<true, 128, false>(p, kmap, vmap, ctas, stream, pdl)
+                : launch_split_t<false, 128, false>(p, kmap, vmap, ctas, stream, pdl);
+  return bf16 ? launch_split_t<true, 64, false>(p, kmap, vmap, ctas, stream, pdl)
+              : launch_split_t<false, 64, false>(p, kmap, vmap, ctas, stream, pdl);
 }
 
 cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStream_t stream,
