@@ -254,9 +254,13 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   int rc = current_device(&num_sms, &err);
   if (rc) return rc;
   p.err = err;
-  // Only a sequence with more than 16 * kTileMinGroups packed rows (n * G) reaches the
-  // tile kernel, and n <= T: for a smaller batch the tile kernel is not launched at all.
-  const bool tiles = p.tpt > 0 && static_cast<int64_t>(p.T) * p.G > 16 * kTileMinGroups;
+  // Only a sequence with more than 16 * kTileMinGroups packed rows (n * G) goes to the tile
+  // kernel. With one token or more in every sequence, none has more than T - B + 1 tokens;
+  // when even that cannot reach a tile the tile kernel is not launched, and the planner is
+  // told so (tpt = 0): should a sequence still have that many rows (other sequences
+  // without tokens), the split kernel takes it.
+  const bool tiles = p.tpt > 0 && (static_cast<int64_t>(p.T) - p.B + 1) * p.G > 16 * kTileMinGroups;
+  if (!tiles) p.tpt = 0;
   CUtensorMap kmap, vmap, qmap;
   if ((rc = make_pool_map(&kmap, k_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;

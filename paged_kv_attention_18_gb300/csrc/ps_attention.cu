@@ -235,11 +235,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   __shared__ Sum3 shl[32];
   extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
-  pdl_launch_dependents();
   // First in the chain, the planner waits for the previous work on the stream before it
   // reads anything. After the step's scatter it starts once that kernel has seen the
   // previous work finish, reads only the step's inputs and writes only the workspace, and
   // waits for the scatter just before it ends, so that its completion stands for both.
+  // It lets the attention kernels launch only once its lists are written: their CTAs,
+  // resident early and waiting, slowed the planner's own passes.
   if (!after_scatter) pdl_wait();
   const bool in_smem = p.B <= kPlanSmemSeqs;
   const int* qsl = p.qsl;
@@ -496,6 +497,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       }
     }
   }
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && tid == 0) {
     p.hdr[0] = tot.x;
     p.hdr[1] = 0;

@@ -312,3 +312,30 @@ def test_small_batch_skips_the_plan():
     assert launches["one_launch"]["reshape_and_cache"] == 0
     assert launches["planned"]["plan"] == 1
     check_workload(small)
+
+
+def test_long_sequence_among_empty_ones_takes_the_split_kernel():
+    # T = B: with a token in every sequence no sequence could reach a query tile, so the
+    # tile kernel is not launched; here one sequence holds all 12 tokens (72 rows at G = 6)
+    # and the others none, and the split kernel takes its rows
+    seqs = [(0, 0)] * 5 + [(300, 12)] + [(40, 0)] * 6
+    wl = W.simple_workload("one_long", seed=60, dtype="bf16", H_q=12, H_kv=2, D=128, seqs=seqs)
+    st = wl.steps[0]
+    assert st.T == st.B == 12
+    pools = DevicePools(wl)
+    binding.profile_begin(8)
+    run_step(wl, st, pools)
+    prof = binding.profile_end()
+    assert prof["tile_attention"][1] == 0 and prof["split_attention"][1] == 1
+    check_workload(wl)
+
+
+def test_decode_batch_launches_no_tile_kernel():
+    wl = W.simple_workload("decodes", seed=61, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(200 + 37 * i, 1) for i in range(40)])
+    pools = DevicePools(wl)
+    binding.profile_begin(8)
+    run_step(wl, wl.steps[0], pools)
+    prof = binding.profile_end()
+    assert prof["tile_attention"][1] == 0 and prof["plan"][1] == 1
+    check_workload(wl)
