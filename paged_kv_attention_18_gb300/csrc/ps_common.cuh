@@ -258,14 +258,14 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
-// acc.x += low 16-bit value of the pair, acc.y += high one, both exactly widened. A bf16
-// value is the upper half of an fp32 one, so widening is a shift or a mask, and the two
-// sums take one packed add.
+// acc.x += low 16-bit value of the pair, acc.y += high one, each exactly widened and
+// added in fp32 (round to nearest) by one mixed-precision add per value.
 template <bool kBF16>
 __device__ __forceinline__ void add_pair_exact(float2& acc, uint32_t packed) {
   if constexpr (kBF16) {
-    acc = fadd2(acc, make_float2(__uint_as_float(packed << 16),
-                                 __uint_as_float(packed & 0xffff0000u)));
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y) : "r"(packed));
   } else {
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
         "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
