@@ -48,6 +48,12 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2
 // which must stay finite in the 16-bit type (fp16 tops out near 2^16, bf16 near 2^128).
 template <bool kBF16>
 constexpr float kMoveLog2 = kBF16 ? 64.f : 15.f;
+// Largest row sum of a 64-column half of P taken against the current reference without
+// looking at the half's max: every P is then at most this (bf16: 2^64, as above; fp16:
+// 64 finite values, so none overflowed). A larger (or infinite) sum sends the half
+// through the max and the reference move.
+template <bool kBF16>
+constexpr float kHalfSumMax = kBF16 ? 18446744073709551616.f : 4194304.f;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns of softmax group g: S (and P over it) at g*256, O at g*256 + 128
@@ -486,10 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(s*scale*log2e - m_ref) as 16-bit pairs written over S; half h of P lands
         // on columns 32h..32h+31, which the loads of halves <= h have already read
         const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
-        float m_tile = -INFINITY;
         // l holds the earlier tiles' sum; this tile's halves are summed apart, so that a
         // reference moved in half 1 can re-sum the half-0 P it re-rounds
-        float l_half0 = 0.f;
+        float l_half0 = 0.f, l_h = 0.f;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t v[64];
@@ -501,62 +506,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 64; ++e)
               if (64 * h + e > lim) v[e] = __float_as_uint(-INFINITY);
           }
-          // four independent max chains
-          float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int e = 0; e < 64; e += 8)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mq[k] = fmax3(mq[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
-          const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
-          const float m_half = mx == -INFINITY ? -INFINITY : mx * sl2;
-          m_tile = fmaxf(m_tile, m_half);
-          // no reference yet, or a jump P could overflow on: move the reference now,
-          // rescaling what is already taken against the old one
-          const bool move = m_half > m_ref + kMoveLog2<kBF16> ||
-                            (m_ref == -INFINITY && m_half != -INFINITY);
-          if (__any_sync(0xffffffffu, move)) {
-            const float alpha = move && m_ref != -INFINITY ? fast_exp2(m_ref - m_half) : 1.f;
-            if (j > 0) rescale_o(alpha);
-            l *= alpha;
-            if (h == 1) {
-              // the half of P already written (columns 0..31) is scaled and rounded again;
-              // its sum is taken anew from the values the PV product will read
-              uint32_t q[32];
-              tmem_ld32(tS, q);
-              tmem_ld_wait();
-              float2 lq0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                q[e] = scale_pair<kBF16>(q[e], alpha);
-                add_pair_exact<kBF16>(lq0[e & 1], q[e]);
-              }
-              l_half0 = (lq0[0].x + lq0[0].y) + (lq0[1].x + lq0[1].y);
-              tmem_st32(tS, q);
-              tmem_st_wait();
-            }
-            if (move) m_ref = m_half;
-          }
-          const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
           uint32_t pk[32];
-          float2 lq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // four sums
-          // scale and subtract two scores per packed fma; the row sum adds the 16-bit P
-          // values the MMA sees, widened exactly
-          const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+          // P is taken against the row's reference without the half's max; the max (and a
+          // move of the reference) is taken only when there is no reference yet, or when
+          // the half's sum shows that P outgrew its bound, and P is then taken again
+          bool with_max = __any_sync(0xffffffffu, m_ref == -INFINITY);
+#pragma unroll 1
+          for (int pass = 0; pass < 2; ++pass) {
+            if (with_max) {
+              // four independent max chains
+              float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                   sl2x2, nm2);
-            pk[e / 2] = pack2<kBF16>(fast_exp2(x.x), fast_exp2(x.y));
-            add_pair_exact<kBF16>(lq[(e / 2) & 1], pk[e / 2]);
+              for (int e = 0; e < 64; e += 8)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mq[k] = fmax3(mq[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
+              const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+              const float m_half = mx == -INFINITY ? -INFINITY : mx * sl2;
+              // no reference yet, or a jump P could overflow on: move the reference now,
+              // rescaling what is already taken against the old one
+              const bool move = m_half > m_ref + kMoveLog2<kBF16> ||
+                                (m_ref == -INFINITY && m_half != -INFINITY);
+              if (__any_sync(0xffffffffu, move)) {
+                const float alpha = move && m_ref != -INFINITY ? fast_exp2(m_ref - m_half) : 1.f;
+                if (j > 0) rescale_o(alpha);
+                l *= alpha;
+                if (h == 1) {
+                  // the half of P already written (columns 0..31) is scaled and rounded
+                  // again; its sum is taken anew from the values the PV product will read
+                  uint32_t q[32];
+                  tmem_st_wait();
+                  tmem_ld32(tS, q);
+                  tmem_ld_wait();
+                  float2 lq0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) {
+                    q[e] = scale_pair<kBF16>(q[e], alpha);
+                    add_pair_exact<kBF16>(lq0[e & 1], q[e]);
+                  }
+                  l_half0 = (lq0[0].x + lq0[0].y) + (lq0[1].x + lq0[1].y);
+                  tmem_st32(tS, q);
+                  tmem_st_wait();
+                }
+                if (move) m_ref = m_half;
+              }
+            }
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            float2 lq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // four sums
+            // scale and subtract two scores per packed fma; the row sum adds the 16-bit P
+            // values the MMA sees, widened exactly
+            const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                     sl2x2, nm2);
+              pk[e / 2] = pack2<kBF16>(fast_exp2(x.x), fast_exp2(x.y));
+              add_pair_exact<kBF16>(lq[(e / 2) & 1], pk[e / 2]);
+            }
+            // P goes out before its sum is checked; a second pass writes it again
+            if (pass > 0) tmem_st_wait();
+            tmem_st16(tS + 32 * h, pk);
+            tmem_st16(tS + 32 * h + 16, pk + 16);
+            l_h = (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
+            if (with_max || __all_sync(0xffffffffu, l_h <= kHalfSumMax<kBF16>)) break;
+            with_max = true;
           }
-          const float l_h = (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
           if (h == 0) l_half0 = l_h;
           else l += l_half0 + l_h;
-          tmem_st16(tS + 32 * h, pk);
-          tmem_st16(tS + 32 * h + 16, pk + 16);
         }
-        m_next = m_tile > m_ref + kRescaleLog2 ? m_tile : m_ref;
+        // O is rescaled lazily: when this tile's P summed to more than 2^8, the reference
+        // moves up by log2 of that sum before the next tile (the new reference is at least
+        // the row's max, so P stays at most 1 there)
+        const float l_tile = l_half0 + l_h;
+        m_next = l_tile > (1 << static_cast<int>(kRescaleLog2)) ? m_ref + __log2f(l_tile) : m_ref;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
