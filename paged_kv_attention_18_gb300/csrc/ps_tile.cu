@@ -591,48 +591,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool write = valid && w.split < ns_t && l > 0.f;
       const float inv = write ? 1.f / l : 0.f;
       if (__all_sync(0xffffffffu, !write || ns_t == 1)) {
-        // Direct output. Each lane holds 64 columns (128 bytes) of its row per step; an
-        // 8 x 8 transpose of 16-byte segments inside each group of eight lanes lets every
-        // store instruction write four whole 128-byte rows (eight lanes per row) instead
-        // of touching 32 rows at once.
-        const int64_t row_off = write ? (static_cast<int64_t>(tok) * p.H_q + head) * D : -1;
-        const int g8 = lane & ~7, b = lane & 7;
-        uint16_t* out = static_cast<uint16_t*>(p.out);
+        // Direct output: each lane writes its own row, 32 columns (64 bytes) at a time,
+        // as two 32-byte stores when the output is 32-byte aligned (two 16-byte stores
+        // otherwise), so every store instruction fills whole 32-byte sectors of 32 rows.
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + head) * D;
+        const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll 1
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          uint32_t v[64];
-          tmem_ld32(tO + c2 * 64, v);
-          tmem_ld32(tO + c2 * 64 + 32, v + 32);
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(tO + c4 * 32, v);
           tmem_ld_wait();
-          uint4 x[8];  // x[s]: segment s (columns 8s..8s+7) of this lane's row
+          uint32_t w[16];
 #pragma unroll
-          for (int sg = 0; sg < 8; ++sg)
-            x[sg] = make_uint4(
-                pack2<kBF16>(__uint_as_float(v[8 * sg + 0]) * inv, __uint_as_float(v[8 * sg + 1]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * sg + 2]) * inv, __uint_as_float(v[8 * sg + 3]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * sg + 4]) * inv, __uint_as_float(v[8 * sg + 5]) * inv),
-                pack2<kBF16>(__uint_as_float(v[8 * sg + 6]) * inv, __uint_as_float(v[8 * sg + 7]) * inv));
-          // butterfly transpose: afterwards x[k] is segment b of the row of lane g8 + k
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack2<kBF16>(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+          if (write) {
+            if (wide) {
+              st_global_v8(dst + c4 * 32, w);
+              st_global_v8(dst + c4 * 32 + 16, w + 8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c4 * 32);
 #pragma unroll
-          for (int m = 4; m >= 1; m >>= 1) {
-            const bool hi = (b & m) != 0;
-#pragma unroll
-            for (int sg = 0; sg < 8; ++sg) {
-              if (sg & m) continue;
-              const uint4 send = hi ? x[sg] : x[sg | m];
-              uint4 recv;
-              recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
-              recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
-              recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
-              recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
-              if (hi) x[sg] = recv;
-              else x[sg | m] = recv;
+              for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int64_t ro = __shfl_sync(0xffffffffu, row_off, g8 + k);
-            if (ro >= 0) reinterpret_cast<uint4*>(out + ro + c2 * 64)[b] = x[k];
           }
         }
       } else {

@@ -339,3 +339,22 @@ def test_decode_batch_launches_no_tile_kernel():
     prof = binding.profile_end()
     assert prof["tile_attention"][1] == 0 and prof["plan"][1] == 1
     check_workload(wl)
+
+
+def test_output_aligned_to_16_bytes_only():
+    # the tile kernel writes 32-byte pieces of each row when the output allows it, and
+    # 16-byte pieces otherwise: both give the same bits
+    wl = W.simple_workload("align", seed=70, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(400, 300), (90, 64), (700, 1)])
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    q = dev(st.q, "bf16")
+    bt, sl, qs = dev(st.block_tables), dev(st.seq_lens), dev(st.query_start_loc)
+    ref = binding.paged_attention(q, pools.k, pools.v, bt, sl, qs, wl.scale)
+    buf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(q.shape)  # 16 bytes past a 256-byte boundary
+    assert out.data_ptr() % 32 == 16
+    binding.paged_attention(q, pools.k, pools.v, bt, sl, qs, wl.scale, out=out)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
