@@ -280,6 +280,10 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
       return cuda_fail(e, "split attention kernel (direct)");
     return PS_OK;
   }
+  // A batch of so few sequences that each could have its own tile item runs on the tile
+  // kernel alone: its decode or verify rows become single query tiles (split along the
+  // context, since tile items are scarce), and the split kernel is not launched.
+  if (tiles && static_cast<int64_t>(p.B) * p.H_kv * 2 <= num_sms) p.all_tiles = 1;
   const int split_grid = split_ctas(p, num_sms);
   const int concurrency = split_grid * attention_warps(p.D);
   // With the step's K/V to cache, the scatter goes first and the planner runs beside it;
@@ -296,7 +300,7 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
     if ((e = launch_plan(p, concurrency, num_sms, scatter != nullptr, s)) != cudaSuccess)
       return cuda_fail(e, "plan kernel");
   }
-  {
+  if (!p.all_tiles) {
     Timed tm(3, s);
     if ((e = launch_split_attention(p, bf16, kmap, vmap, split_grid, s, true)) != cudaSuccess)
       return cuda_fail(e, "split attention kernel");

@@ -40,7 +40,7 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, const int* qsl,
   s.valid = s.n >= 0 && s.n <= s.L && s.pages <= p.max_blocks;
   const int rows = s.valid ? s.n * p.G : 0;
   s.groups = (rows + 15) / 16;
-  s.tile = p.tpt > 0 && s.groups > kTileMinGroups;
+  s.tile = p.tpt > 0 && (s.groups > kTileMinGroups || (p.all_tiles && s.groups > 0));
   s.qtiles = s.tile ? (s.n + p.tpt - 1) / p.tpt : 0;
   return s;
 }

@@ -32,6 +32,7 @@ struct AttnParams {
   int* seq_off_t;                // [B + 1] first tile-kernel item of each sequence
   int cap_tile;
   int tpt;                       // query tokens per 128-row tile (0: no tile kernel)
+  int all_tiles;                 // every sequence with rows goes to the tile kernel (no split kernel)
   int* tok_ns;                   // [T] splits holding each token's rows (0 = none)
   int* tok_base;                 // [T] first partial entry of each token
   int* seq_off_p;                // [B + 1] first partial entry of each sequence
