@@ -874,7 +874,8 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     }
-    // causal mask, online softmax
+    // causal mask and row max on the raw scores (the scale is positive, so the max of the
+    // scaled scores is the scaled max)
     const int key0 = comp_page * kBlockSize + 2 * t4;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -883,7 +884,7 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
       for (int e = 0; e < 4; ++e) {
         const int r = e >> 1;
         const int key = key0 + nt * 8 + (e & 1);
-        const float x = key <= row_pos[r] ? s[nt][e] * scale_log2 : -INFINITY;
+        const float x = key <= row_pos[r] ? s[nt][e] : -INFINITY;
         s[nt][e] = x;
         mx[r] = fmaxf(mx[r], x);
       }
@@ -892,29 +893,46 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
     for (int r = 0; r < 2; ++r) {
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float m_new = fmaxf(m_run[r], mx[r]);
+      const float m_new = fmaxf(m_run[r], mx[r] == -INFINITY ? -INFINITY : mx[r] * scale_log2);
       m_use[r] = m_new == -INFINITY ? 0.f : m_new;
       alpha[r] = fast_exp2(m_run[r] - m_use[r]);
       m_run[r] = m_new;
     }
+    // P = 2^(s * scale * log2 e - m): one packed fma per pair of scores of a row
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = fast_exp2(s[nt][e] - m_use[e >> 1]);
+      for (int r = 0; r < 2; ++r) {
+        const float2 x = ffma2(make_float2(s[nt][2 * r], s[nt][2 * r + 1]), sc2,
+                               make_float2(-m_use[r], -m_use[r]));
+        s[nt][2 * r] = fast_exp2(x.x);
+        s[nt][2 * r + 1] = fast_exp2(x.y);
+      }
     uint32_t pa[4];
     pa[0] = pack2<kBF16>(s[0][0], s[0][1]);
     pa[1] = pack2<kBF16>(s[0][2], s[0][3]);
     pa[2] = pack2<kBF16>(s[1][0], s[1][1]);
     pa[3] = pack2<kBF16>(s[1][2], s[1][3]);
-    // the row sums use the rounded P the tensor core multiplies with
-    l_run[0] = l_run[0] * alpha[0] + pair_sum<kBF16>(pa[0]) + pair_sum<kBF16>(pa[2]);
-    l_run[1] = l_run[1] * alpha[1] + pair_sum<kBF16>(pa[1]) + pair_sum<kBF16>(pa[3]);
+    // the row sums use the rounded P the tensor core multiplies with (each value widened
+    // exactly and added in fp32)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float2 acc = make_float2(l_run[r] * alpha[r], 0.f);
+      add_pair_exact<kBF16>(acc, pa[r]);
+      add_pair_exact<kBF16>(acc, pa[2 + r]);
+      l_run[r] = acc.x + acc.y;
+    }
+    // O rescaled by packed multiplies (a thread's accumulators pair up by row)
+    const float2 a0 = make_float2(alpha[0], alpha[0]), a1 = make_float2(alpha[1], alpha[1]);
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
-      o[j][0] *= alpha[0];
-      o[j][1] *= alpha[0];
-      o[j][2] *= alpha[1];
-      o[j][3] *= alpha[1];
+      const float2 u = fmul2(make_float2(o[j][0], o[j][1]), a0);
+      const float2 w = fmul2(make_float2(o[j][2], o[j][3]), a1);
+      o[j][0] = u.x;
+      o[j][1] = u.y;
+      o[j][2] = w.x;
+      o[j][3] = w.y;
     }
     // O += P V: V page is [key][d], read transposed
     {

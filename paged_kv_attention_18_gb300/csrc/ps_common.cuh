@@ -231,18 +231,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Sum of the two 16-bit values of a packed pair, in fp32.
-template <bool kBF16>
-__device__ __forceinline__ float pair_sum(uint32_t packed) {
-  if constexpr (kBF16) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&packed));
-    return f.x + f.y;
-  } else {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&packed));
-    return f.x + f.y;
-  }
-}
-
 // a * b + c on two fp32 lanes in one packed instruction (sm_100 f32x2 arithmetic).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
@@ -254,12 +242,12 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-// a + b on two fp32 lanes in one packed instruction.
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+// a * b on two fp32 lanes in one packed instruction.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   float2 d;
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
