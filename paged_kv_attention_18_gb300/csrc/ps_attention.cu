@@ -199,12 +199,29 @@ __device__ Sum3 block_sum3_ll(Sum3 v, Sum3* sh) {
   return t;
 }
 
+// Items per worker that the split sizes aim at: more items balance the workers' ends
+// better, fewer carry less per-item cost (query load, partial output, combine).
+#ifndef PS_SPLIT_ITEMS_PER_WORKER
+#define PS_SPLIT_ITEMS_PER_WORKER 4
+#endif
+
 __device__ __forceinline__ int pages_per_split(long long work, long long workers, int align) {
-  const long long target = workers * 4;
+  const long long target = workers * PS_SPLIT_ITEMS_PER_WORKER;
   long long pps = (work + target - 1) / (target > 0 ? target : 1);
   if (pps < kMinSplitPages) pps = kMinSplitPages;
   pps = (pps + align - 1) / align * align;
   return static_cast<int>(pps > (1 << 24) ? (1 << 24) : pps);
+}
+
+// Split-kernel items go out longest first, by class of their length in pages: 0 for
+// items longer than the target (sequences at the split cap), then by quarters of the
+// target. Items are fetched in list order, so the short ones fill the workers' ends.
+__device__ __forceinline__ int split_class(const SeqInfo& s, int ns, int pps) {
+  const int len = (s.pages + ns - 1) / ns;
+  return len > pps ? 0 : 4 * len > 3 * pps ? 1 : 2 * len > pps ? 2 : 3;
+}
+__device__ __forceinline__ int int4_at(const int4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
 __device__ __forceinline__ void store_item(WorkItem* dst_item, const WorkItem& it) {
@@ -289,26 +306,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
 
   // per sequence: split-kernel items, tile-kernel items (pairs of query tiles), partial
   // entries and split tokens; coarser splits while the lists overflow the workspace
-  int4 tot = make_int4(0, 0, 0, 0);
+  // (split-kernel items: the offset within the sequence's length class, run_d the
+  // classes' sizes)
+  int4 tot = make_int4(0, 0, 0, 0), run_d = make_int4(0, 0, 0, 0);
   for (int attempt = 0; attempt < 32; ++attempt) {
     int4 run = make_int4(0, 0, 0, 0);
+    run_d = make_int4(0, 0, 0, 0);
     for (int base = 0; base < p.B; base += nth) {
       const int b = base + tid;
-      int4 c = make_int4(0, 0, 0, 0);
+      int4 c = make_int4(0, 0, 0, 0), cd = make_int4(0, 0, 0, 0);
+      int kd = 0;
       if (b < p.B) {
         const SeqInfo s = seq_info(p, qsl, lens, b);
         const int ns = seq_splits(s, pps_d, pps_t);
-        if (s.tile) c.y = (s.qtiles + 1) / 2 * ns * p.H_kv;
-        else c.x = s.groups * ns * p.H_kv;
+        if (s.tile) {
+          c.y = (s.qtiles + 1) / 2 * ns * p.H_kv;
+        } else if (ns > 0) {
+          c.x = s.groups * ns * p.H_kv;
+          kd = split_class(s, ns, pps_d);
+          cd = make_int4(kd == 0 ? c.x : 0, kd == 1 ? c.x : 0, kd == 2 ? c.x : 0,
+                         kd == 3 ? c.x : 0);
+        }
         if (ns > 1) {
           c.z = split_entries_before(s, ns, s.n) * p.H_q;
           c.w = s.n - split_first_token(s, ns, 1);
         }
       }
-      int4 t4;
+      int4 t4, td;
       const int4 ex = block_exscan4(c, sh4, t4);
+      const int4 exd = block_exscan4(cd, sh4, td);
       if (b < p.B) {
-        off_d[b] = run.x + ex.x;
+        off_d[b] = int4_at(run_d, kd) + int4_at(exd, kd);
         off_t[b] = run.y + ex.y;
         off_p[b] = run.z + ex.z;
         off_s[b] = run.w + ex.w;
@@ -317,6 +345,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
       run.y += t4.y;
       run.z += t4.z;
       run.w += t4.w;
+      run_d.x += td.x;
+      run_d.y += td.y;
+      run_d.z += td.z;
+      run_d.w += td.w;
     }
     tot = run;
     if (tot.x <= p.cap_items && tot.y <= p.cap_tile && tot.z <= p.cap_part) break;
@@ -424,7 +456,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     if (!s.valid || s.groups == 0) continue;
     const int ns = seq_splits(s, pps_d, pps_t);
     if (!s.tile) {
-      const int cnt = s.groups * ns * p.H_kv, first = off_d[b], rows = s.n * p.G;
+      const int kd = split_class(s, ns, pps_d);
+      const int cls_base = (kd > 0 ? run_d.x : 0) + (kd > 1 ? run_d.y : 0) + (kd > 2 ? run_d.z : 0);
+      const int cnt = s.groups * ns * p.H_kv, first = cls_base + off_d[b], rows = s.n * p.G;
       for (int local = lane; local < cnt; local += 32) {
         const int j = local % s.groups;
         const int rest = local / s.groups;

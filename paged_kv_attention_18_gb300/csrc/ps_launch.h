@@ -27,7 +27,7 @@ struct AttnParams {
   // [7] tokens whose rows are split (entries of tok_list)
   int* hdr;
   WorkItem* items;               // [cap_items] split-kernel work (decode rows)
-  int* seq_off;                  // [B + 1] first split-kernel item of each sequence
+  int* seq_off;                  // [B + 1] sequence's first split item within its length class
   WorkItem* tile_items;          // [cap_tile] tile-kernel work (prefill / verify rows)
   int* seq_off_t;                // [B + 1] first tile-kernel item of each sequence
   int cap_tile;
