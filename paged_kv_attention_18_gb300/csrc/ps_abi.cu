@@ -306,6 +306,24 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
       return cuda_fail(e, "split attention kernel (direct)");
     return PS_OK;
   }
+  // A few sequences with query tiles and short contexts: the tile kernel alone, right after
+  // the step's scatter, each CTA deriving its items (every sequence unsplit) from seq_lens
+  // and qsl. No plan, nothing to combine.
+  if (tiles && direct_tile_fits(p, num_sms)) {
+    if (scatter) {
+      Timed tm(1, s);
+      if ((e = launch_step_scatter(scatter->k, scatter->v, p.block_tables, p.max_blocks,
+                                   p.seq_lens, p.qsl, p.B, p.T, p.H_kv, p.D, p.num_blocks,
+                                   p.slots, k_pool, v_pool, err, num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "KV scatter kernel");
+      p.after_scatter = 1;
+    }
+    Timed tm(5, s);
+    if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, direct_tile_ctas(p, num_sms), s,
+                                   true, true)) != cudaSuccess)
+      return cuda_fail(e, "tile attention kernel (direct)");
+    return PS_OK;
+  }
   // A batch of so few sequences that each could have its own tile item runs on the tile
   // kernel alone: its decode or verify rows become single query tiles (split along the
   // context, since tile items are scarce), and the split kernel is not launched.

@@ -303,6 +303,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // the tile kernel's CTAs (few short chunks, or short chunks at the end of long contexts).
   int pps_t = 2 * W.z * p.H_kv < tile_ctas ? pages_per_split(Wt, tile_ctas, kTilePagesAlign)
                                             : (1 << 24);
+#ifdef PS_TILE_ALL_NOSPLIT
+  if (p.all_tiles) pps_t = 1 << 24;
+#endif
 
   // per sequence: split-kernel items, tile-kernel items (pairs of query tiles), partial
   // entries and split tokens; coarser splits while the lists overflow the workspace

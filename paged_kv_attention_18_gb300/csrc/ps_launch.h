@@ -47,6 +47,10 @@ struct AttnParams {
   // item per (sequence, KV head) straight from seq_lens and qsl instead of a plan, and,
   // with new_k set, first scatters the step's K/V into the pools.
   int direct;
+  // The tile kernel's direct mode was launched right after the step's scatter, which
+  // waited for the earlier work on the stream: the step's inputs may be read before the
+  // wait for the scatter itself.
+  int after_scatter;
   const void* new_k;             // [T, H_kv, D] the step's K and V, or null
   const void* new_v;
   void* k_pool;                  // [num_blocks, 16, H_kv, D]
@@ -149,9 +153,24 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, boo
 // Query tokens per 128-row tile for G query heads per KV head (0 = use the split kernel).
 int tile_tokens(int G);
 
+// The tile kernel on `ctas` CTAs: from the plan's list, or, in direct mode, every
+// sequence unsplit from items each CTA derives from seq_lens and qsl (see
+// direct_tile_fits).
 cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                  cudaStream_t stream, bool pdl);
+                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int ctas,
+                                  cudaStream_t stream, bool pdl, bool direct = false);
+
+// Sequences the tile kernel's direct mode takes at most (one warp lane each).
+constexpr int kDirectTileMaxSeqs = 32;
+
+// True when a batch with query tiles fits the tile kernel's direct mode: at most
+// kDirectTileMaxSeqs sequences, so few that each could have its own tile items, and no
+// block table wider than kDirectMaxPages, so no item is long enough to want a split.
+bool direct_tile_fits(const AttnParams& p, int num_sms);
+
+// CTAs for the direct tile mode: the items of the batch, bounded from T, B and the tile
+// size, at most one per SM.
+int direct_tile_ctas(const AttnParams& p, int num_sms);
 
 // CTAs for the split kernel: the full grid, or fewer when the batch's shape (T, B, the
 // block-table width) bounds its work items below one per warp of the full grid.

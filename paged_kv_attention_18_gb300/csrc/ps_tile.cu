@@ -100,7 +100,10 @@ __device__ __forceinline__ bool tile_item_ok(const WorkItem& w, const AttnParams
 
 }  // namespace
 
-template <bool kBF16, int D>
+// kDirect: no plan. Each CTA derives its items from seq_lens and qsl (every sequence
+// unsplit, its query-tile pairs longest first), and only the K/V producers wait for the
+// kernel before this one (the step's scatter) before their first copy from the pools.
+template <bool kBF16, int D, bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
     tile_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap,
@@ -109,10 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kHalves = D / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
-  pdl_wait();  // the plan and the kernels before this one are complete
-  const int n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
-  if (n_items == 0) return;  // nothing planned for this kernel (uniform across the grid)
 
+  // The set-up (barriers, TMEM, zeroed query rows, descriptor prefetch) touches only this
+  // CTA's own state, so it runs while the kernels before this one finish.
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -150,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bars->abort = 0;
     fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -171,6 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
+
+  int n_items = 0;
+  if constexpr (!kDirect) {
+    pdl_wait();  // the plan and the kernels before this one are complete
+    n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
+    if (n_items == 0) {  // nothing planned for this kernel (uniform across the grid)
+      if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  } else if (!p.after_scatter) {
+    pdl_wait();  // the step's inputs may still be being written by the kernel before
+  }
 
   // Bounded wait with a warp-uniform outcome: if any lane gives up (or another role has
   // given up), the whole warp leaves its loop together.
@@ -196,15 +213,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 || warp == 2) {
     // ===================== producers: warp 0 (items, Q, K), warp 2 (V) ================
     const bool is_k = warp == 0;
-    if (lane == 0) {
-      tma_prefetch_desc(is_k ? &kmap : &vmap);
-      if (is_k) tma_prefetch_desc(&qmap);
-    }
     const int n_stages = is_k ? kKStages : kVStages;
     uint32_t g = 0, qa = 0, qb = 0;
+    bool waited = !kDirect;  // direct mode: the pools are read after the step's scatter
+    // Direct mode: lane b holds sequence b's query tokens n, context L, first token t0 and
+    // query-tile pairs (0 for a sequence without rows or an invalid one). Items go rank by
+    // rank (rank r: every sequence's r-th longest pair, in batch order, each KV head), so
+    // csum(r) = H_kv * sum_b min(pairs_b, r) items come before rank r; CTA c takes items
+    // c, c + gridDim.x, ...
+    int d_n = 0, d_L = 0, d_t0 = 0, d_pairs = 0, d_max = 0, d_total = 0;
+    auto csum = [&](int r) -> int {
+      int v = min(d_pairs, r);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      return v * p.H_kv;
+    };
+    if constexpr (kDirect) {
+      if (is_k && lane < p.B) {
+        const int q0 = __ldg(p.qsl + lane), q1 = __ldg(p.qsl + lane + 1);
+        const int L = __ldg(p.seq_lens + lane), n = q1 - q0;
+        const bool valid = n >= 0 && n <= L && (L + kBlockSize - 1) / kBlockSize <= p.max_blocks &&
+                           q0 >= 0 && q1 <= p.T;
+        if (!valid) {
+          if (blockIdx.x == 0) record_error(p.err, kDevBadSequence);
+        } else if (n > 0) {
+          d_n = n;
+          d_L = L;
+          d_t0 = q0;
+          d_pairs = ((n + p.tpt - 1) / p.tpt + 1) / 2;
+        }
+      }
+      d_max = d_pairs;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) d_max = max(d_max, __shfl_xor_sync(0xffffffffu, d_max, o));
+      d_total = csum(d_max);
+    }
+    // field `lane` of direct item idx (< d_total)
+    auto direct_field = [&](int idx) -> int {
+      int lo = 0, hi = d_max - 1;  // rank: the last r with csum(r) <= idx
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (csum(mid) <= idx) lo = mid;
+        else hi = mid - 1;
+      }
+      const int r = lo, k = idx - csum(r);
+      const int nth = k / p.H_kv, kv = k - nth * p.H_kv;
+      // the nth (from 0) sequence in batch order that has a pair of rank r
+      const unsigned has = __ballot_sync(0xffffffffu, d_pairs > r);
+      const bool hit = ((has >> lane) & 1u) && __popc(has & ((1u << lane) - 1u)) == nth;
+      const int b = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+      const int n = __shfl_sync(0xffffffffu, d_n, b), L = __shfl_sync(0xffffffffu, d_L, b);
+      const int t0 = __shfl_sync(0xffffffffu, d_t0, b);
+      const int j = __shfl_sync(0xffffffffu, d_pairs, b) - 1 - r;  // rank 0: the last pair
+      const int qa_ = 2 * j * p.tpt, qb_ = qa_ + p.tpt;
+      const int na = min(p.tpt, n - qa_), nb = qb_ < n ? min(p.tpt, n - qb_) : 0;
+      const int i_last = nb > 0 ? qb_ + nb - 1 : qa_ + na - 1;
+      const int pe = min((L + kBlockSize - 1) / kBlockSize, (L - n + i_last) / kBlockSize + 1);
+      int f = 0;  // seq, kv, row0, nrows, page_begin 0, page_end, split 0, nsplit 1, L, n, t0
+      f = lane == 0 ? b : f;
+      f = lane == 1 ? kv : f;
+      f = lane == 2 ? qa_ * p.G : f;
+      f = lane == 3 ? na * p.G : f;
+      f = lane == 5 ? pe : f;
+      f = lane == 7 ? 1 : f;
+      f = lane == 8 ? L : f;
+      f = lane == 9 ? n : f;
+      f = lane == 10 ? t0 : f;
+      f = lane == 11 ? nb * p.G : f;  // rows of query tile B
+      return f;
+    };
     for (int it = 0;; ++it) {
       int idx = 0;
-      if (is_k) {
+      if (is_k && kDirect) {
+        const int slot = it % kItemRing;
+        if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
+        idx = blockIdx.x + it * static_cast<int>(gridDim.x);
+        if (idx >= d_total) idx = -1;
+        if (idx >= 0) {
+          const int f = direct_field(idx);
+          if (lane < 16) reinterpret_cast<int*>(items + it % (2 * kItemRing))[lane] = f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          bars->item_idx[slot] = idx;
+          mbar_arrive(&bars->item_full[slot]);
+        }
+      } else if (is_k) {
         const int slot = it % kItemRing;
         if (!wait(&bars->item_empty[slot], ((it / kItemRing) & 1) ^ 1)) break;
         if (lane < 4) {
@@ -269,6 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
         uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
         if (!wait(empty, ((g / n_stages) & 1) ^ 1)) { ok = false; break; }
+        if (!waited) {
+          pdl_wait();  // the step's scatter has written the new tokens' rows
+          waited = true;
+        }
         const int blk = __shfl_sync(0xffffffffu, bt_reg, (first - bt_base + pp) & 31);
         uint8_t* dst = smem + (is_k ? L::kOffK : L::kOffV) + st * L::kK;
         if (lane == 0) mbar_arrive_expect_tx(full, L::kK);
@@ -457,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row's split count and partial base, fetched now so that the epilogue's
       // stores do not wait on them
       // (both loads are issued at once; nothing waits for them before the epilogue)
-      const int ns_t = valid ? __ldg(p.tok_ns + tok) : 0;
-      const int tok_part = valid ? __ldg(p.tok_base + tok) : 0;
+      const int ns_t = !valid ? 0 : kDirect ? 1 : __ldg(p.tok_ns + tok);
+      const int tok_part = kDirect || !valid ? 0 : __ldg(p.tok_base + tok);
       // m_ref: the reference max (log2 units) that P, O and l are currently taken against;
       // m_next: a max more than 2^8 above it seen in the last tile, applied before the next
       float m_ref = -INFINITY, m_next = -INFINITY, l = 0.f;
@@ -660,27 +758,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int tile_tokens(int G) { return G >= 1 && G <= 16 ? kRows / G : 0; }
 
-template <bool kBF16, int D>
+template <bool kBF16, int D, bool kDirect>
 static cudaError_t launch_tile_t(const AttnParams& p, const CUtensorMap& kmap,
-                                 const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
+                                 const CUtensorMap& vmap, const CUtensorMap& qmap, int ctas,
                                  cudaStream_t stream, bool pdl) {
   constexpr int smem = TileSmem<D>::kBytes;
-  auto kern = tile_attention_kernel<kBF16, D>;
+  auto kern = tile_attention_kernel<kBF16, D, kDirect>;
   static std::atomic<uint64_t> done{0};
   const cudaError_t e = ensure_smem_limit(kern, smem, done);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(num_sms), dim3(kThreads), smem, stream, pdl, kmap, vmap, qmap,
-                       p);
+  return launch_kernel(kern, dim3(ctas), dim3(kThreads), smem, stream, pdl, kmap, vmap, qmap, p);
+}
+
+template <bool kDirect>
+static cudaError_t launch_tile_d(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, const CUtensorMap& qmap, int ctas,
+                                 cudaStream_t stream, bool pdl) {
+  if (p.D == 128)
+    return bf16 ? launch_tile_t<true, 128, kDirect>(p, kmap, vmap, qmap, ctas, stream, pdl)
+                : launch_tile_t<false, 128, kDirect>(p, kmap, vmap, qmap, ctas, stream, pdl);
+  return bf16 ? launch_tile_t<true, 64, kDirect>(p, kmap, vmap, qmap, ctas, stream, pdl)
+              : launch_tile_t<false, 64, kDirect>(p, kmap, vmap, qmap, ctas, stream, pdl);
 }
 
 cudaError_t launch_tile_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                  cudaStream_t stream, bool pdl) {
-  if (p.D == 128)
-    return bf16 ? launch_tile_t<true, 128>(p, kmap, vmap, qmap, num_sms, stream, pdl)
-                : launch_tile_t<false, 128>(p, kmap, vmap, qmap, num_sms, stream, pdl);
-  return bf16 ? launch_tile_t<true, 64>(p, kmap, vmap, qmap, num_sms, stream, pdl)
-              : launch_tile_t<false, 64>(p, kmap, vmap, qmap, num_sms, stream, pdl);
+                                  const CUtensorMap& vmap, const CUtensorMap& qmap, int ctas,
+                                  cudaStream_t stream, bool pdl, bool direct) {
+  return direct ? launch_tile_d<true>(p, bf16, kmap, vmap, qmap, ctas, stream, pdl)
+                : launch_tile_d<false>(p, bf16, kmap, vmap, qmap, ctas, stream, pdl);
+}
+
+bool direct_tile_fits(const AttnParams& p, int num_sms) {
+  return p.tpt > 0 && p.B <= kDirectTileMaxSeqs && p.max_blocks <= kDirectMaxPages &&
+         static_cast<int64_t>(p.B) * p.H_kv * 2 <= num_sms;
+}
+
+int direct_tile_ctas(const AttnParams& p, int num_sms) {
+  // a sequence of n tokens has ceil(ceil(n / tpt) / 2) <= n / (2 tpt) + 1 pairs
+  const int64_t items = static_cast<int64_t>(p.H_kv) * (p.T / (2 * p.tpt) + 1 + p.B);
+  return static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);
 }
 
 }  // namespace ps

@@ -314,6 +314,49 @@ def test_small_batch_skips_the_plan():
     check_workload(small)
 
 
+# Batches for the tile kernel's direct mode: query tiles, at most 32 sequences, few enough
+# that each could have its own tile items, no block table wider than 64 pages
+DIRECT_TILE_BATCHES = [
+    ("f16", 14, 2, 64, [(97, 1), (520, 1), (256, 256), (768, 256)]),   # decodes + chunks
+    ("bf16", 12, 2, 128, [(1024, 1024)]),                                # a whole prompt
+    ("bf16", 8, 8, 128, [(300, 150), (0, 0), (129, 129)]),               # G = 1, an empty one
+    ("f16", 16, 1, 64, [(40, 9), (17, 17), (1000, 33)]),                 # G = 16: 8-token tiles
+    ("bf16", 12, 2, 128, [(64 + 5 * i, 3 + i % 4) for i in range(32)]),  # 32 sequences
+]
+
+
+@pytest.mark.parametrize("case", range(len(DIRECT_TILE_BATCHES)))
+@pytest.mark.parametrize("separate", [False, True])
+def test_direct_tile_batches(case, separate):
+    dt, H_q, H_kv, D, seqs = DIRECT_TILE_BATCHES[case]
+    wl = W.simple_workload(f"dtile{case}", seed=70 + case, dtype=dt, H_q=H_q, H_kv=H_kv, D=D,
+                           seqs=seqs)
+    pools = DevicePools(wl)
+    binding.profile_begin(8)
+    run_step(wl, wl.steps[0], pools, separate_calls=separate)
+    prof = binding.profile_end()
+    # the tile kernel alone: no plan, no split kernel, nothing to combine
+    assert prof["tile_attention"][1] == 1
+    assert prof["plan"][1] == 0 and prof["split_attention"][1] == 0 and prof["combine"][1] == 0
+    check_workload(wl, separate_calls=separate)
+
+
+def test_direct_tile_bad_sequence_sets_device_error():
+    wl = W.simple_workload("dtile_bad", seed=80, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=[(200, 100), (300, 40)])
+    st = wl.steps[0]
+    sl = st.seq_lens.copy()
+    sl[1] = 30  # 40 query tokens over a 30-token context: the sequence is skipped
+    pools = DevicePools(wl)
+    out = binding.paged_attention(dev(st.q, "bf16"), pools.k, pools.v, dev(st.block_tables),
+                                  dev(sl), dev(st.query_start_loc), wl.scale)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 3
+    ref = oracle.paged_attention(st.q, wl.k_pool, wl.v_pool, st.block_tables, st.seq_lens,
+                                 st.query_start_loc, wl.scale, "bf16", acc=np.float32)
+    assert np.abs(out.float().cpu().numpy()[:100] - ref[:100]).max() <= TOL["bf16"]
+
+
 def test_long_sequence_among_empty_ones_takes_the_split_kernel():
     # T = B: with a token in every sequence no sequence could reach a query tile, so the
     # tile kernel is not launched; here one sequence holds all 12 tokens (72 rows at G = 6)
