@@ -330,18 +330,18 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   if (tiles && static_cast<int64_t>(p.B) * p.H_kv * 2 <= num_sms) p.all_tiles = 1;
   const int split_grid = split_ctas(p, num_sms);
   const int concurrency = split_grid * attention_warps(p.D);
-  // With the step's K/V to cache, the scatter goes first and the planner runs beside it;
-  // every later launch is chained with programmatic dependent launch.
-  if (scatter) {
-    Timed tm(1, s);
-    if ((e = launch_step_scatter(scatter->k, scatter->v, p.block_tables, p.max_blocks, p.seq_lens,
-                                 p.qsl, p.B, p.T, p.H_kv, p.D, p.num_blocks, p.slots, k_pool,
-                                 v_pool, err, num_sms, s)) != cudaSuccess)
-      return cuda_fail(e, "KV scatter kernel");
-  }
+  // The planner goes first, with the step's KV scatter (if any) on extra CTAs of the same
+  // launch; every later launch is chained with programmatic dependent launch.
   {
+    AttnParams pp = p;
+    if (scatter) {
+      pp.new_k = scatter->k;
+      pp.new_v = scatter->v;
+      pp.k_pool = k_pool;
+      pp.v_pool = v_pool;
+    }
     Timed tm(2, s);
-    if ((e = launch_plan(p, concurrency, num_sms, scatter != nullptr, s)) != cudaSuccess)
+    if ((e = launch_plan(pp, concurrency, num_sms, num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "plan kernel");
   }
   // With both kernels, the tile kernel runs on the side stream beside the split kernel:

@@ -18,6 +18,7 @@
 // rows whose context was split, by log-sum-exp weights.
 #include "ps_common.cuh"
 #include "ps_launch.h"
+#include "ps_scatter.cuh"
 
 namespace ps {
 
@@ -247,18 +248,27 @@ constexpr int kPlanRankSeqs = 512;  // tile sequences up to which every rank goe
 constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
-                                                    int tile_ctas, bool after_scatter) {
+                                                    int tile_ctas, int plan_ctas) {
   __shared__ int4 sh4[32];
   __shared__ Sum3 shl[32];
   extern __shared__ int plan_smem[];
   const int tid = threadIdx.x, nth = blockDim.x;
-  // First in the chain, the planner waits for the previous work on the stream before it
-  // reads anything. After the step's scatter it starts once that kernel has seen the
-  // previous work finish, reads only the step's inputs and writes only the workspace, and
-  // waits for the scatter just before it ends, so that its completion stands for both.
-  // It lets the attention kernels launch only once its lists are written: their CTAs,
-  // resident early and waiting, slowed the planner's own passes.
-  if (!after_scatter) pdl_wait();
+  // First in the chain, every CTA waits for the previous work on the stream before it
+  // reads anything. CTAs plan_ctas and up carry the step's KV scatter (when p.new_k is
+  // set), beside the planning CTAs: the attention kernels' wait on this grid then covers
+  // both, at the cost of one launch. The planning CTAs let the attention kernels launch
+  // only once their lists are written: those CTAs, resident early and waiting, slowed the
+  // planner's own passes.
+  pdl_wait();
+  if (static_cast<int>(blockIdx.x) >= plan_ctas) {
+    scatter_step_tokens(static_cast<const uint4*>(p.new_k), static_cast<const uint4*>(p.new_v),
+                        p.block_tables, p.max_blocks, p.seq_lens, p.qsl, p.B, p.T,
+                        p.H_kv * p.D / 8, p.num_blocks, p.slots, static_cast<uint4*>(p.k_pool),
+                        static_cast<uint4*>(p.v_pool), p.err,
+                        (static_cast<int>(blockIdx.x) - plan_ctas) * (nth >> 5) + (tid >> 5),
+                        (static_cast<int>(gridDim.x) - plan_ctas) * (nth >> 5));
+    return;
+  }
   const bool in_smem = p.B <= kPlanSmemSeqs;
   const int* qsl = p.qsl;
   const int* lens = p.seq_lens;
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // tokens: splits holding the rows, first partial entry and the combine's token list. The
   // tokens are dealt to the CTAs in blocks of nth, round robin, four per thread and round.
   constexpr int kTokUnroll = 4;
-  const int tok_stride = gridDim.x * nth;
+  const int tok_stride = plan_ctas * nth;
   // the token pass starts from the block's upper half: with few tokens it then runs on
   // other warps than the item pass below, which deals sequences to the low warps first
   const int ttid = (tid + nth / 2) % nth;
@@ -453,8 +463,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // (rows sharing pages run back to back); tile-kernel items as pairs of consecutive query
   // tiles (A, B), placed in the rank order above
   const int lane = tid & 31, nw = nth >> 5;
-  const int gw = (tid >> 5) * gridDim.x + blockIdx.x;  // sequences dealt across the CTAs
-  for (int b = planned ? gw : p.B; b < p.B; b += gridDim.x * nw) {
+  const int gw = (tid >> 5) * plan_ctas + blockIdx.x;  // sequences dealt across the CTAs
+  for (int b = planned ? gw : p.B; b < p.B; b += plan_ctas * nw) {
     const SeqInfo s = seq_info(p, qsl, lens, b);
     if (!s.valid || s.groups == 0) continue;
     const int ns = seq_splits(s, pps_d, pps_t);
@@ -545,7 +555,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
     p.hdr[6] = pps_t;
     p.hdr[7] = planned ? tot.w : 0;
   }
-  if (after_scatter) pdl_wait();
 }
 
 // ----------------------------------------------------------------------------------
@@ -1094,7 +1103,7 @@ static int plan_threads(int B) {
   return t > 1024 ? 1024 : t;
 }
 
-cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, bool after_scatter,
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int num_sms,
                         cudaStream_t stream) {
   const int smem =
       p.B <= kPlanSmemSeqs ? kPlanSmemArrays * (p.B + 1) * static_cast<int>(sizeof(int)) : 0;
@@ -1109,10 +1118,18 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, boo
   const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 8;
   // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
-  // programmatic dependent launch: the planner's CTAs may start while the kernel before
-  // them on the stream finishes (see plan_kernel for what they wait for, and when)
-  return launch_kernel(plan_kernel, dim3(ctas), dim3(plan_threads(p.B)), static_cast<size_t>(smem),
-                       stream, true, p, concurrency, tile_ctas, after_scatter);
+  // the scatter CTAs: one warp per token, at most 64 warps per SM in all
+  const int threads = plan_threads(p.B), warps = threads / 32;
+  int64_t scatter = 0;
+  if (p.new_k != nullptr && p.T > 0) {
+    scatter = (static_cast<int64_t>(p.T) + warps - 1) / warps;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 64 / warps;
+    if (scatter > cap) scatter = cap;
+  }
+  // programmatic dependent launch: the CTAs may start while the kernel before them on the
+  // stream finishes (see plan_kernel for what they wait for, and when)
+  return launch_kernel(plan_kernel, dim3(static_cast<unsigned>(ctas + scatter)), dim3(threads),
+                       static_cast<size_t>(smem), stream, true, p, concurrency, tile_ctas, ctas);
 }
 
 template <bool kBF16, int D, bool kDirect>

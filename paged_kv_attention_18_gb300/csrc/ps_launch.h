@@ -145,9 +145,9 @@ int attention_ctas(int D, int num_sms);
 int attention_warps(int D);
 
 // concurrency: split-kernel warps; tile_ctas: tile-kernel CTAs (work is sized for both).
-// after_scatter: the step's scatter kernel precedes the planner on the stream; the planner
-// then runs beside it and waits for it only before it ends.
-cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, bool after_scatter,
+// With p.new_k set, the same launch also carries the step's KV scatter (p.new_k, p.new_v
+// into p.k_pool, p.v_pool, slots to p.slots) on extra CTAs beside the planning ones.
+cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int num_sms,
                         cudaStream_t stream);
 
 // Query tokens per 128-row tile for G query heads per KV head (0 = use the split kernel).

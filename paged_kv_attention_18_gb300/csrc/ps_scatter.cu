@@ -10,6 +10,7 @@
 // backend writes K/V into the pool).
 #include "ps_common.cuh"
 #include "ps_launch.h"
+#include "ps_scatter.cuh"
 
 namespace ps {
 
@@ -73,31 +74,12 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
   }
 }
 
-// Sequence of packed token t: the largest b in [0, B) with qsl[b] <= t (empty sequences
-// share their start with the next one), found by the whole warp in 32-way rounds, so a
-// batch of B sequences takes ceil(log32(B)) rounds of loads instead of log2(B).
-__device__ __forceinline__ int warp_find_seq(const int32_t* __restrict__ qsl, int B, int t,
-                                             int lane) {
-  int lo = 0, n = B;  // the answer lies in [lo, lo + n); qsl[lo] <= t throughout
-  while (n > 1) {
-    const int step = (n + 31) / 32;
-    const int idx = lo + lane * step;
-    const bool le = idx < lo + n && __ldg(qsl + idx) <= t;
-    const unsigned m = __ballot_sync(0xffffffffu, le) | 1u;
-    const int k = 31 - __clz(m);
-    const int end = lo + n;
-    lo += k * step;
-    n = min(step, end - lo);
-  }
-  return lo;
-}
-
-// The step's KV scatter with its slot mapping, first in the step's launch chain: one warp
-// per packed token finds the token's sequence and position (the last n positions of the
-// context are the step's tokens), reads its block-table entry, writes the slot and copies
-// the token's K and V rows there in 16-byte chunks. It lets the planner start as soon as
-// the previous work on the stream is done, so the two run side by side; the planner
-// waits for this kernel before it ends.
+// The step's KV scatter with its slot mapping, first in the launch chain of the tile
+// kernel's direct mode: one warp per packed token finds the token's sequence and position
+// (the last n positions of the context are the step's tokens), reads its block-table
+// entry, writes the slot and copies the token's K and V rows there in 16-byte chunks. It
+// lets the tile kernel start as soon as the previous work on the stream is done; the tile
+// kernel's K/V producers wait for this kernel before their first copy from the pools.
 __global__ void __launch_bounds__(256) step_scatter_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int32_t* __restrict__ block_tables, int max_blocks, const int32_t* __restrict__ seq_lens,
@@ -105,34 +87,9 @@ __global__ void __launch_bounds__(256) step_scatter_kernel(
     int32_t* __restrict__ slots, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int* err) {
   pdl_wait();               // the previous kernel on the stream has finished
   pdl_launch_dependents();  // the planner may start now
-  const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const int b = warp_find_seq(qsl, B, t, lane);
-    int slot = -1;
-    if (lane == 0) {
-      const int start = __ldg(qsl + b), end = __ldg(qsl + b + 1);
-      const int n = end - start, L = __ldg(seq_lens + b);
-      const int pos = L - n + (t - start);
-      if (t < start || t >= end || n > L || pos < 0 || pos / kBlockSize >= max_blocks) {
-        record_error(err, kDevBadSequence);
-      } else {
-        const int blk = __ldg(block_tables + static_cast<int64_t>(b) * max_blocks + pos / kBlockSize);
-        if (blk < 0 || blk >= num_blocks) record_error(err, kDevBadBlockId);
-        else slot = blk * kBlockSize + pos % kBlockSize;
-      }
-      slots[t] = slot;
-    }
-    slot = __shfl_sync(0xffffffffu, slot, 0);
-    if (slot < 0) continue;
-    const int64_t src = static_cast<int64_t>(t) * row_vecs, dst = static_cast<int64_t>(slot) * row_vecs;
-    for (int c = lane; c < row_vecs; c += 32) {
-      const uint4 kk = __ldcs(k + src + c);
-      const uint4 vv = __ldcs(v + src + c);
-      k_pool[dst + c] = kk;
-      v_pool[dst + c] = vv;
-    }
-  }
+  scatter_step_tokens(k, v, block_tables, max_blocks, seq_lens, qsl, B, T, row_vecs, num_blocks,
+                      slots, k_pool, v_pool, err, (blockIdx.x * blockDim.x + threadIdx.x) >> 5,
+                      gridDim.x * (blockDim.x >> 5));
 }
 
 cudaError_t launch_step_scatter(const void* k, const void* v, const int32_t* block_tables,
