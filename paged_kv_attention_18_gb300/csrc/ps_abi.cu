@@ -93,31 +93,6 @@ struct Timed {
 thread_local char g_last_error[256] = "";
 int cuda_fail(cudaError_t e, const char* where);
 
-// A second stream and two events per host thread and device. When a step runs both the
-// split and the tile kernel, the caller's stream forks to this stream after the plan (the
-// tile kernel runs there, beside the split kernel) and joins it again before the combine.
-// One host thread's calls are sequential, so no two calls share these at once; they live
-// as long as the process.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t plan = nullptr, tile = nullptr;
-};
-thread_local SideStream g_side[kMaxDevices];
-
-int side_stream(SideStream** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PS_ERR_CUDA;
-  SideStream& x = g_side[dev];
-  if (!x.s) {
-    cudaError_t e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x.plan, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x.tile, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "side stream");
-  }
-  *out = &x;
-  return PS_OK;
-}
-
 // PS_ERR_CUDA, remembering which step failed and CUDA's message for ps_last_error_message.
 int cuda_fail(cudaError_t e, const char* where) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
@@ -344,45 +319,28 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
     if ((e = launch_plan(pp, concurrency, num_sms, num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "plan kernel");
   }
-  // With both kernels, the tile kernel runs on the side stream beside the split kernel:
-  // neither reads the other's results, and the tile kernel's CTAs take their items from a
-  // counter, so CTAs that start late (on SMs the split kernel still holds) just join in.
-  // While the timing hook records, the two run one after the other, so that each one's
-  // events time that kernel alone.
-  bool profiling;
-  {
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    profiling = g_prof.on;
-  }
-  const bool fork = tiles && !p.all_tiles && !profiling;
-  SideStream* side = nullptr;
-  if (fork) {
-    if ((rc = side_stream(&side))) return rc;
-    if ((e = cudaEventRecord(side->plan, s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(side->s, side->plan, 0)) != cudaSuccess)
-      return cuda_fail(e, "fork to the side stream");
-  }
+  // One stream, every launch chained with programmatic dependent launch. With both
+  // kernels, the tile kernel follows the split kernel and runs beside it: it reads the
+  // plan without waiting (the split kernel lets it launch only once the plan is complete),
+  // and its CTAs take their items from a counter, so CTAs that start late (on SMs the split
+  // kernel still holds) just join in.
   if (!p.all_tiles) {
     Timed tm(3, s);
     if ((e = launch_split_attention(p, bf16, kmap, vmap, split_grid, s, true)) != cudaSuccess)
       return cuda_fail(e, "split attention kernel");
   }
   if (tiles) {
-    cudaStream_t ts = fork ? side->s : s;
-    Timed tm(5, ts);
-    if ((e = launch_tile_attention(p, bf16, kmap, vmap, qmap, num_sms, ts, !fork)) != cudaSuccess)
+    AttnParams pt = p;
+    pt.after_split = !p.all_tiles;
+    Timed tm(5, s);
+    if ((e = launch_tile_attention(pt, bf16, kmap, vmap, qmap, num_sms, s, true)) != cudaSuccess)
       return cuda_fail(e, "tile attention kernel");
-  }
-  if (fork) {
-    if ((e = cudaEventRecord(side->tile, side->s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s, side->tile, 0)) != cudaSuccess)
-      return cuda_fail(e, "join from the side stream");
   }
   // A split holds at least kMinSplitPages pages, so with no block table longer than that
   // no row is split and there is nothing to combine.
   if (p.max_blocks > kMinSplitPages) {
     Timed tm(4, s);
-    if ((e = launch_combine(p, bf16, num_sms, s, !fork)) != cudaSuccess) return cuda_fail(e, "combine kernel");
+    if ((e = launch_combine(p, bf16, num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
   }
   return PS_OK;
 }

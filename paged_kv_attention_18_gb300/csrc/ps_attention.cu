@@ -613,7 +613,6 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
       reinterpret_cast<WorkItem*>(smem + W * S * kStage + W * S * 8) + warp * kRing;
   const uint32_t tiles_addr = smem_u32(tiles);
 
-  pdl_launch_dependents();
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
@@ -622,6 +621,9 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
   }
   __syncwarp();
   pdl_wait();  // the plan (and the KV scatter) before this kernel are complete
+  // Dependents launch only now: the tile kernel after this one reads the plan without a
+  // wait of its own.
+  pdl_launch_dependents();
 
   // direct mode: one item per (sequence, KV head), handed out round robin; otherwise the
   // plan's list, fetched through its counter

@@ -51,6 +51,11 @@ struct AttnParams {
   // waited for the earlier work on the stream: the step's inputs may be read before the
   // wait for the scatter itself.
   int after_scatter;
+  // The tile kernel follows the split kernel on the stream. The split kernel lets its
+  // dependents launch only once the plan is complete, so the tile kernel reads the plan
+  // without waiting, runs beside the split kernel, and waits for it only before it ends
+  // (one thread), so that its completion stands for both for the combine.
+  int after_split;
   const void* new_k;             // [T, H_kv, D] the step's K and V, or null
   const void* new_v;
   void* k_pool;                  // [num_blocks, 16, H_kv, D]

@@ -179,10 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int n_items = 0;
   if constexpr (!kDirect) {
-    pdl_wait();  // the plan and the kernels before this one are complete
+    // the plan and the kernels before this one are complete; after the split kernel,
+    // which let this kernel launch only once the plan was complete, the plan is read
+    // without a wait and the wait for the split kernel comes at the end
+    if (!p.after_split) pdl_wait();
     n_items = *reinterpret_cast<volatile const int*>(p.hdr + 4);
     if (n_items == 0) {  // nothing planned for this kernel (uniform across the grid)
       if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+      if (p.after_split && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
       return;
     }
   } else if (!p.after_scatter) {
@@ -754,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (!kDirect && p.after_split && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 int tile_tokens(int G) { return G >= 1 && G <= 16 ? kRows / G : 0; }
