@@ -1096,6 +1096,10 @@ int attention_ctas(int D, int num_sms) { (void)D; return num_sms * PS_SPLIT_CTAS
 
 // Threads per planner CTA: a small batch needs fewer (its scans and barriers span fewer
 // warps); up to 1024.
+// Packed tokens per planning CTA (the token pass's share of each CTA).
+#ifndef PS_PLAN_TOKENS_PER_CTA
+#define PS_PLAN_TOKENS_PER_CTA 256
+#endif
 #ifndef PS_PLAN_MIN_THREADS
 #define PS_PLAN_MIN_THREADS 256
 #endif
@@ -1117,7 +1121,7 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int
   }
   // enough CTAs that the token and item passes are short (a CTA's warps share its SM's
   // issue slots, and emitting a sequence's items is division-heavy); each repeats the scan
-  const int64_t want = 1 + static_cast<int64_t>(p.T) / 1024 + p.B / 8;
+  const int64_t want = 1 + static_cast<int64_t>(p.T) / PS_PLAN_TOKENS_PER_CTA + p.B / 8;
   // (one CTA when the offsets live in global memory: the CTAs' scans would share them)
   const int ctas = p.B > kPlanSmemSeqs ? 1 : static_cast<int>(want < kPlanMaxCtas ? want : kPlanMaxCtas);
   // the scatter CTAs: one warp per token, at most 64 warps per SM in all
