@@ -71,6 +71,19 @@ def test_spec_verify_long_full_size():
                                                              long_rows)))
 
 
+def test_long_prefill_sampled():
+    # 16384 tokens in one step: the planner at its CTA cap, the scatter CTAs looping over
+    # more tokens than they have warps (every pool row is still compared exactly)
+    wl = W.long_prefill()
+    st = wl.steps[0]
+    assert st.T == 16384
+    rng = np.random.default_rng(103)
+    qsl = st.query_start_loc
+    rows = [int(qsl[b]) for b in range(st.B)] + [int(qsl[b + 1]) - 1 for b in range(st.B)]
+    rows = sorted(set(rows + rng.choice(st.T, size=60, replace=False).tolist()))
+    check_workload(wl, rows_for_step=lambda i, s_: rows)
+
+
 # ------------------------------------------------------------------------------------
 # randomized small shapes: several tiles, splits and ragged tails, compared in full
 # ------------------------------------------------------------------------------------
