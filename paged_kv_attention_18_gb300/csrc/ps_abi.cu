@@ -649,12 +649,52 @@ size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq,
   return staging_layout(T, B, max_blocks_per_seq, H_q, H_kv, D, ws).total;
 }
 
+namespace {
+// The device's view of a host buffer the kernels may read directly: page-locked, mapped
+// for the device and 4-byte aligned; null otherwise (the buffer is then copied by a
+// copy operation). Not called while a graph is being captured.
+const void* device_view(const void* h) {
+  if (!h || (reinterpret_cast<uintptr_t>(h) & 3u)) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer ||
+      (reinterpret_cast<uintptr_t>(a.devicePointer) & 3u))
+    return nullptr;
+  return a.devicePointer;
+}
+
+// The host step. dev[i] is the device's view of input i (q, k, v, block tables, lengths,
+// offsets) or null: inputs with a view are gathered by one kernel that reads them across
+// the host link, the others copied one by one.
+int host_step(const void* q, const void* k, const void* v, const int32_t* block_tables,
+              const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
+              void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
+              int num_blocks, float scale, void* staging, size_t staging_bytes, int dtype,
+              void* stream, const void* const dev[6]);
+}  // namespace
+
 int ps_attention_step_host(const void* q, const void* k, const void* v,
                            const int32_t* block_tables, const int32_t* seq_lens,
                            const int32_t* query_start_loc, void* out, void* k_pool, void* v_pool,
                            int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
                            int num_blocks, float scale, void* staging, size_t staging_bytes,
                            int dtype, void* stream) {
+  const void* dev[6] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
+                        device_view(seq_lens), device_view(query_start_loc)};
+  return host_step(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                   max_blocks_per_seq, B, T, H_q, H_kv, D, num_blocks, scale, staging,
+                   staging_bytes, dtype, stream, dev);
+}
+
+namespace {
+int host_step(const void* q, const void* k, const void* v, const int32_t* block_tables,
+              const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
+              void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
+              int num_blocks, float scale, void* staging, size_t staging_bytes, int dtype,
+              void* stream, const void* const dev[6]) {
   int rc = check_shapes(H_q, H_kv, D, dtype);
   if (rc) return rc;
   if ((rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
@@ -683,9 +723,21 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
       {st + l.sl, seq_lens, static_cast<size_t>(B) * 4},
       {st + l.qsl, query_start_loc, static_cast<size_t>(B + 1) * 4},
   };
-  for (const Copy& c : in)
-    if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  ps::CopySegments segs{};
+  for (int i = 0; i < 6; ++i) {
+    const Copy& c = in[i];
+    if (c.bytes == 0) continue;
+    if (dev[i] && c.bytes % 4 == 0) {
+      segs.seg[segs.n++] = ps::CopySegment{c.dst, dev[i], static_cast<int64_t>(c.bytes)};
+    } else if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
       return PS_ERR_CUDA;
+    }
+  }
+  if (segs.n > 0) {
+    int num_sms = 0, *err = nullptr;
+    if ((rc = ps::current_device(&num_sms, &err))) return rc;
+    if (ps::launch_gather_in(segs, num_sms, s) != cudaSuccess) return PS_ERR_CUDA;
+  }
   rc = ps_attention_step(st + l.q, st + l.k, st + l.v, k_pool, v_pool,
                          reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
                          reinterpret_cast<const int32_t*>(st + l.sl),
@@ -698,6 +750,7 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
     return PS_ERR_CUDA;
   return PS_OK;
 }
+}  // namespace
 
 // One host step in a CUDA graph: the copies in, the step's kernels and the copy out are
 // captured from a private stream and instantiated once; each launch replays them with the
@@ -738,6 +791,8 @@ int ps_attention_step_host_graph_create(const void* q, const void* k, const void
     }
     if (a.type != cudaMemoryTypeHost) return PS_ERR_ARG;
   }
+  const void* dev[6] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
+                        device_view(seq_lens), device_view(query_start_loc)};
   cudaStream_t cs;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "graph stream");
@@ -746,9 +801,9 @@ int ps_attention_step_host_graph_create(const void* q, const void* k, const void
     cudaStreamDestroy(cs);
     return cuda_fail(e, "graph capture");
   }
-  rc = ps_attention_step_host(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool,
-                              v_pool, max_blocks_per_seq, B, T, H_q, H_kv, D, num_blocks, scale,
-                              staging, staging_bytes, dtype, cs);
+  rc = host_step(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
+                 max_blocks_per_seq, B, T, H_q, H_kv, D, num_blocks, scale, staging,
+                 staging_bytes, dtype, cs, dev);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(cs, &g);  // ends the capture whatever the step returned
   cudaStreamDestroy(cs);

@@ -108,6 +108,38 @@ cudaError_t launch_step_scatter(const void* k, const void* v, const int32_t* blo
                        slots, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
 }
 
+// The host step's input copies in one launch: each CTA's threads walk the segments'
+// 16-byte chunks (4-byte words for a segment whose addresses or size are not 16-byte
+// multiples), reading the page-locked host buffers directly.
+__global__ void __launch_bounds__(256) gather_in_kernel(const CopySegments segs) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int k = 0; k < segs.n; ++k) {
+    const CopySegment& c = segs.seg[k];
+    const bool wide = ((reinterpret_cast<uintptr_t>(c.dst) | reinterpret_cast<uintptr_t>(c.src) |
+                        static_cast<uintptr_t>(c.bytes)) & 15u) == 0;
+    if (wide) {
+      const uint4* src = static_cast<const uint4*>(c.src);
+      uint4* dst = static_cast<uint4*>(c.dst);
+      for (int64_t i = tid; i < c.bytes / 16; i += nth) dst[i] = src[i];
+    } else {
+      const uint32_t* src = static_cast<const uint32_t*>(c.src);
+      uint32_t* dst = static_cast<uint32_t*>(c.dst);
+      for (int64_t i = tid; i < c.bytes / 4; i += nth) dst[i] = src[i];
+    }
+  }
+}
+
+cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream) {
+  int64_t chunks = 0;
+  for (int k = 0; k < segs.n; ++k) chunks += segs.seg[k].bytes / 16 + 1;
+  int64_t blocks = (chunks + 255) / 256;
+  if (blocks > 2 * static_cast<int64_t>(num_sms)) blocks = 2 * static_cast<int64_t>(num_sms);
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(gather_in_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                       false, segs);
+}
+
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                                 const int32_t* qsl, int B, int T, int num_blocks, int32_t* slots,
                                 int* err, cudaStream_t stream) {

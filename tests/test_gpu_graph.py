@@ -170,3 +170,25 @@ def test_host_step_graph_rejects_pageable_buffers():
     ref = oracle.paged_attention(st.q, kref, vref, st.block_tables, st.seq_lens,
                                  st.query_start_loc, wl.scale, wl.dtype, acc=np.float32)
     assert np.abs(out.float().numpy() - ref).max() <= TOL[wl.dtype]
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("name", ["qwen05b_mixed", "qwen15b_decode"])
+def test_host_step_pinned_and_pageable(name, pinned):
+    # ps_attention_step_host: page-locked inputs are gathered by one kernel reading them
+    # across the host link, pageable ones copied one by one; the pools and the output must
+    # match the oracle either way
+    wl = W.named(name, batch=16) if name == "qwen15b_decode" else W.named(name)
+    st = wl.steps[0]
+    pools = DevicePools(wl)
+    q, k, v, bt, sl, qs, out, staging = _host_step_tensors(wl, st, pinned=pinned)
+    binding.attention_step_host(q, k, v, bt, sl, qs, out, pools.k, pools.v, wl.scale, staging)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    slots_ref = oracle.slot_mapping(st.block_tables, st.seq_lens, st.query_start_loc)
+    kref, vref = oracle.reshape_and_cache(st.k, st.v, slots_ref, wl.k_pool, wl.v_pool)
+    assert np.array_equal(host_bits(pools.k), kref)
+    assert np.array_equal(host_bits(pools.v), vref)
+    ref = oracle.paged_attention(st.q, kref, vref, st.block_tables, st.seq_lens,
+                                 st.query_start_loc, wl.scale, wl.dtype, acc=np.float32)
+    assert np.abs(out.float().numpy() - ref).max() <= TOL[wl.dtype]
