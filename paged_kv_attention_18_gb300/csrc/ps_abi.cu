@@ -666,14 +666,15 @@ const void* device_view(const void* h) {
   return a.devicePointer;
 }
 
-// The host step. dev[i] is the device's view of input i (q, k, v, block tables, lengths,
-// offsets) or null: inputs with a view are gathered by one kernel that reads them across
-// the host link, the others copied one by one.
+// The host step. dev[i] is the device's view of host buffer i (q, k, v, block tables,
+// lengths, offsets, out) or null: inputs with a view are gathered by one kernel that reads
+// them across the host link, the others copied one by one; an output with a view is
+// written by a kernel, otherwise copied.
 int host_step(const void* q, const void* k, const void* v, const int32_t* block_tables,
               const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
               void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
               int num_blocks, float scale, void* staging, size_t staging_bytes, int dtype,
-              void* stream, const void* const dev[6]);
+              void* stream, const void* const dev[7]);
 }  // namespace
 
 int ps_attention_step_host(const void* q, const void* k, const void* v,
@@ -682,8 +683,8 @@ int ps_attention_step_host(const void* q, const void* k, const void* v,
                            int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
                            int num_blocks, float scale, void* staging, size_t staging_bytes,
                            int dtype, void* stream) {
-  const void* dev[6] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
-                        device_view(seq_lens), device_view(query_start_loc)};
+  const void* dev[7] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
+                        device_view(seq_lens), device_view(query_start_loc), device_view(out)};
   return host_step(q, k, v, block_tables, seq_lens, query_start_loc, out, k_pool, v_pool,
                    max_blocks_per_seq, B, T, H_q, H_kv, D, num_blocks, scale, staging,
                    staging_bytes, dtype, stream, dev);
@@ -694,7 +695,7 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
               const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
               void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
               int num_blocks, float scale, void* staging, size_t staging_bytes, int dtype,
-              void* stream, const void* const dev[6]) {
+              void* stream, const void* const dev[7]) {
   int rc = check_shapes(H_q, H_kv, D, dtype);
   if (rc) return rc;
   if ((rc = check_batch(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, B, T,
@@ -736,7 +737,7 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
   if (segs.n > 0) {
     int num_sms = 0, *err = nullptr;
     if ((rc = ps::current_device(&num_sms, &err))) return rc;
-    if (ps::launch_gather_in(segs, num_sms, s) != cudaSuccess) return PS_ERR_CUDA;
+    if (ps::launch_gather_in(segs, num_sms, s, false) != cudaSuccess) return PS_ERR_CUDA;
   }
   rc = ps_attention_step(st + l.q, st + l.k, st + l.v, k_pool, v_pool,
                          reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
@@ -745,9 +746,21 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
                          num_blocks, scale, st + l.out, reinterpret_cast<int32_t*>(st + l.slots),
                          st + l.ws, ws_bytes, dtype, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out, st + l.out, static_cast<size_t>(T) * H_q * D * 2,
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  // the output: written straight into the page-locked host buffer by a kernel that follows
+  // the step's last kernel, or copied
+  const size_t out_bytes = static_cast<size_t>(T) * H_q * D * 2;
+  if (dev[6] && out_bytes % 4 == 0) {
+    ps::CopySegments o{};
+    o.seg[0] = ps::CopySegment{const_cast<void*>(dev[6]), st + l.out,
+                               static_cast<int64_t>(out_bytes)};
+    o.n = 1;
+    int num_sms = 0, *err = nullptr;
+    if ((rc = ps::current_device(&num_sms, &err))) return rc;
+    if (ps::launch_gather_in(o, num_sms, s, true) != cudaSuccess) return PS_ERR_CUDA;
+  } else if (cudaMemcpyAsync(out, st + l.out, out_bytes, cudaMemcpyDeviceToHost, s) !=
+             cudaSuccess) {
     return PS_ERR_CUDA;
+  }
   return PS_OK;
 }
 }  // namespace
@@ -791,8 +804,8 @@ int ps_attention_step_host_graph_create(const void* q, const void* k, const void
     }
     if (a.type != cudaMemoryTypeHost) return PS_ERR_ARG;
   }
-  const void* dev[6] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
-                        device_view(seq_lens), device_view(query_start_loc)};
+  const void* dev[7] = {device_view(q), device_view(k), device_view(v), device_view(block_tables),
+                        device_view(seq_lens), device_view(query_start_loc), device_view(out)};
   cudaStream_t cs;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "graph stream");

@@ -94,8 +94,10 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
-// Copies from page-locked host memory (or device memory) into device memory, several
-// buffers in one launch; each buffer's address and size must be multiples of 4 bytes.
+// Copies between page-locked host memory (through its device view) and device memory,
+// several buffers in one launch; each buffer's address and size must be multiples of 4
+// bytes. With pdl, it may start while the kernel before it runs and waits for it before
+// reading.
 struct CopySegment {
   void* dst;
   const void* src;
@@ -105,7 +107,8 @@ struct CopySegments {
   CopySegment seg[8];
   int n;
 };
-cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream);
+cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream,
+                             bool pdl);
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                                 const int32_t* qsl, int B, int T, int num_blocks, int32_t* slots,

@@ -108,10 +108,13 @@ cudaError_t launch_step_scatter(const void* k, const void* v, const int32_t* blo
                        slots, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
 }
 
-// The host step's input copies in one launch: each CTA's threads walk the segments'
-// 16-byte chunks (4-byte words for a segment whose addresses or size are not 16-byte
-// multiples), reading the page-locked host buffers directly.
+// The host step's copies in one launch: each CTA's threads walk the segments' 16-byte
+// chunks (4-byte words for a segment whose addresses or size are not 16-byte multiples),
+// reading or writing the page-locked host buffers directly. Launched after the kernel
+// that writes its sources, it waits for that kernel first.
 __global__ void __launch_bounds__(256) gather_in_kernel(const CopySegments segs) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int k = 0; k < segs.n; ++k) {
@@ -130,14 +133,15 @@ __global__ void __launch_bounds__(256) gather_in_kernel(const CopySegments segs)
   }
 }
 
-cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream,
+                             bool pdl) {
   int64_t chunks = 0;
   for (int k = 0; k < segs.n; ++k) chunks += segs.seg[k].bytes / 16 + 1;
   int64_t blocks = (chunks + 255) / 256;
   if (blocks > 2 * static_cast<int64_t>(num_sms)) blocks = 2 * static_cast<int64_t>(num_sms);
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_in_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                       false, segs);
+                       pdl, segs);
 }
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
