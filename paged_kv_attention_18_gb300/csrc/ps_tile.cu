@@ -693,28 +693,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool write = valid && w.split < ns_t && l > 0.f;
       const float inv = write ? 1.f / l : 0.f;
       if (__all_sync(0xffffffffu, !write || ns_t == 1)) {
-        // Direct output: each lane writes its own row, 32 columns (64 bytes) at a time,
-        // as two 32-byte stores when the output is 32-byte aligned (two 16-byte stores
+        // Direct output: each lane writes its own row, 64 columns (128 bytes) per TMEM
+        // wait, as 32-byte stores when the output is 32-byte aligned (16-byte stores
         // otherwise), so every store instruction fills whole 32-byte sectors of 32 rows.
         uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + head) * D;
         const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll 1
-        for (int c4 = 0; c4 < D / 32; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(tO + c4 * 32, v);
+        for (int c4 = 0; c4 < D / 64; ++c4) {
+          uint32_t v[64];
+          tmem_ld32(tO + c4 * 64, v);
+          tmem_ld32(tO + c4 * 64 + 32, v + 32);
           tmem_ld_wait();
-          uint32_t w[16];
+          uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack2<kBF16>(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+          for (int e = 0; e < 32; ++e) {
+            const float2 x =
+                fmul2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), inv2);
+            w[e] = pack2<kBF16>(x.x, x.y);
+          }
           if (write) {
             if (wide) {
-              st_global_v8(dst + c4 * 32, w);
-              st_global_v8(dst + c4 * 32 + 16, w + 8);
-            } else {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c4 * 32);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              for (int q = 0; q < 4; ++q) st_global_v8(dst + c4 * 64 + 16 * q, w + 8 * q);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c4 * 64);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
           }
         }
