@@ -296,6 +296,7 @@ SMALL_BATCHES = [
     ("bf16", 12, 2, 128, [(90, 2), (7, 0)]),                  # verify-like rows, G = 6
     ("f16", 8, 8, 64, [(1024, 1), (513, 1)]),                 # 64 pages, MHA (G = 1)
     ("bf16", 16, 1, 128, [(33, 1)]),                          # G = 16: one row group
+    ("f16", 4, 2, 64, [(17, 2), (33, 2), (2, 2)]),            # two new rows across pages
 ]
 
 
