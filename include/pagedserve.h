@@ -294,8 +294,10 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
  *   staging        DEVICE scratch of at least ps_attention_step_host_staging_size() bytes,
  *                  256-byte aligned, owned by the caller (inputs, slot mapping, output and
  *                  the attention workspace are placed in it).
- * Host memory must stay valid and unmodified until the stream completes. Copies are one
- * cudaMemcpyAsync per array.
+ * Host memory must stay valid and unmodified until the stream completes. Page-locked host
+ * arrays that the device can address (pinned and mapped, 4-byte aligned) are read by one
+ * kernel that gathers all such inputs across the host link, and `out` is then written by
+ * a kernel after the step's last one; any other array is copied with one cudaMemcpyAsync.
  */
 size_t ps_attention_step_host_staging_size(int T, int B, int max_blocks_per_seq, int H_q,
                                            int H_kv, int D, int max_seq_len);
@@ -364,9 +366,11 @@ const char* ps_status_string(int status);
  * around the next n launches of each kernel kind (host memory only; events are created
  * here, not in the timed calls). ps_profile_end() waits for the recorded events and
  * stops recording. ps_profile_read(kind, &ms, &launches) then gives the summed device
- * time and the launch count of one kind: 0 slot mapping, 1 KV scatter, 2 planner,
- * 3 split attention (decode and verify rows), 4 split combine, 5 tile attention (prefill
- * rows, tcgen05), 6 block copy, 7 speculative acceptance, 8 rotary KV scatter.
+ * time and the launch count of one kind: 0 slot mapping, 1 KV scatter as its own launch
+ * (ps_reshape_and_cache, or the step's scatter ahead of the tile kernel's direct mode),
+ * 2 planner (carrying the step's KV scatter when there is one), 3 split attention (decode
+ * and verify rows), 4 split combine, 5 tile attention (prefill rows, tcgen05), 6 block
+ * copy, 7 speculative acceptance, 8 rotary KV scatter.
  */
 int ps_profile_begin(int max_launches_per_kind);
 int ps_profile_end(void);
