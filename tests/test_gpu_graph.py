@@ -17,9 +17,19 @@ from tests.gpu_util import TOL, DevicePools, dev, host_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["qwen05b_mixed", "tiny_decode"])
+def _graph_workload(name):
+    if name == "planned_both":
+        # 39 sequences with contexts past 64 pages: the planned chain with both attention
+        # kernels (the tile kernel reading the plan without a wait of its own)
+        seqs = [(800 + 37 * i, 1) for i in range(37)] + [(1500, 200), (600, 150)]
+        return W.simple_workload("planned_both", seed=91, dtype="bf16", H_q=12, H_kv=2,
+                                 D=128, seqs=seqs)
+    return W.named(name)
+
+
+@pytest.mark.parametrize("name", ["qwen05b_mixed", "tiny_decode", "planned_both"])
 def test_step_replayed_from_cuda_graph(name):
-    wl = W.named(name)
+    wl = _graph_workload(name)
     st = wl.steps[0]
     pools = DevicePools(wl)
     dt = wl.dtype
