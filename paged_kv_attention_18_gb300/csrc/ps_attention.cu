@@ -629,6 +629,8 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
   // plan's list, fetched through its counter
   const int n_items = kDirect ? p.B * p.H_kv : *reinterpret_cast<volatile int*>(p.hdr);
   int direct_next = blockIdx.x * W + warp;
+  bool first_fetch = true;
+  const bool tile_planned = !kDirect && *reinterpret_cast<volatile int*>(p.hdr + 4) > 0;
   const uint64_t policy = l2_policy_evict_first();
 
   // ---------------- issue side (runs ahead of compute by up to S pages) -------------
@@ -730,8 +732,18 @@ __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM
       if constexpr (kDirect) {
         idx = direct_next;
         direct_next += gridDim.x * W;
+      } else if (first_fetch) {
+        // each warp's first item is its own, with no trip to the counter: the list is
+        // longest first and the kernel's CTAs (one per SM) are all resident by then. With
+        // tile items planned, a CTA's warps take consecutive items, so the split work sits
+        // on as few SMs as it needs and the rest are free early for the tile kernel;
+        // otherwise the items are dealt across the CTAs, so neighbouring items run on
+        // different SMs.
+        idx = tile_planned ? static_cast<int>(blockIdx.x) * W + warp
+                           : warp * static_cast<int>(gridDim.x) + blockIdx.x;
+        first_fetch = false;
       } else {
-        if (lane == 0) idx = atomicAdd(p.hdr + 1, 1);
+        if (lane == 0) idx = atomicAdd(p.hdr + 1, 1) + static_cast<int>(gridDim.x) * W;
         idx = __shfl_sync(0xffffffffu, idx, 0);
       }
       if (idx >= n_items) {
