@@ -340,7 +340,8 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   // no row is split and there is nothing to combine.
   if (p.max_blocks > kMinSplitPages) {
     Timed tm(4, s);
-    if ((e = launch_combine(p, bf16, num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "combine kernel");
+    if ((e = launch_combine(p, bf16, num_sms, s, true)) != cudaSuccess)
+      return cuda_fail(e, "combine kernel");
   }
   return PS_OK;
 }

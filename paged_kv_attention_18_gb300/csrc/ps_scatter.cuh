@@ -48,7 +48,8 @@ __device__ __forceinline__ void scatter_step_tokens(
       if (t < start || t >= end || n > L || pos < 0 || pos / kBlockSize >= max_blocks) {
         record_error(err, kDevBadSequence);
       } else {
-        const int blk = __ldg(block_tables + static_cast<int64_t>(b) * max_blocks + pos / kBlockSize);
+        const int blk =
+            __ldg(block_tables + static_cast<int64_t>(b) * max_blocks + pos / kBlockSize);
         if (blk < 0 || blk >= num_blocks) record_error(err, kDevBadBlockId);
         else slot = blk * kBlockSize + pos % kBlockSize;
       }
@@ -56,7 +57,8 @@ __device__ __forceinline__ void scatter_step_tokens(
     }
     slot = __shfl_sync(0xffffffffu, slot, 0);
     if (slot < 0) continue;
-    const int64_t src = static_cast<int64_t>(t) * row_vecs, dst = static_cast<int64_t>(slot) * row_vecs;
+    const int64_t src = static_cast<int64_t>(t) * row_vecs;
+    const int64_t dst = static_cast<int64_t>(slot) * row_vecs;
     for (int c = lane; c < row_vecs; c += 32) {
       const uint4 kk = __ldcs(k + src + c);
       const uint4 vv = __ldcs(v + src + c);
