@@ -582,20 +582,26 @@ struct SplitCfg<64> {
   static constexpr int kWarps = PS_SPLIT_WARPS, kStages = 2 * PS_SPLIT_STAGES;
 };
 
-template <int D>
+// kS > 0 overrides the ring's stage count (the direct mode's small ring for short
+// contexts, see launch_split_attention).
+template <int D, int kS = 0>
+constexpr int split_stages() {
+  return kS > 0 ? kS : SplitCfg<D>::kStages;
+}
+template <int D, int kS = 0>
 constexpr int split_smem_bytes() {
   return 1024 /*alignment slack*/ +
-         SplitCfg<D>::kWarps * SplitCfg<D>::kStages * (2 * kBlockSize * D * 2) +
-         SplitCfg<D>::kWarps * SplitCfg<D>::kStages * 8 +
-         SplitCfg<D>::kWarps * (SplitCfg<D>::kStages + 2) * 64;
+         SplitCfg<D>::kWarps * split_stages<D, kS>() * (2 * kBlockSize * D * 2) +
+         SplitCfg<D>::kWarps * split_stages<D, kS>() * 8 +
+         SplitCfg<D>::kWarps * (split_stages<D, kS>() + 2) * 64;
 }
 
-template <bool kBF16, int D, bool kDirect>
+template <bool kBF16, int D, bool kDirect, int kS = 0>
 __global__ void __launch_bounds__(SplitCfg<D>::kWarps * 32, PS_SPLIT_CTAS_PER_SM)
     split_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   constexpr int W = SplitCfg<D>::kWarps;
-  constexpr int S = SplitCfg<D>::kStages;
+  constexpr int S = split_stages<D, kS>();
   constexpr int kRing = S + 2;
   constexpr int kPage = kBlockSize * D * 2;  // bytes of one page of K (or V), one head
   constexpr int kStage = 2 * kPage;
@@ -1150,12 +1156,12 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int
                        static_cast<size_t>(smem), stream, true, p, concurrency, tile_ctas, ctas);
 }
 
-template <bool kBF16, int D, bool kDirect>
+template <bool kBF16, int D, bool kDirect, int kS = 0>
 static cudaError_t launch_split_t(const AttnParams& p, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                   bool pdl) {
-  constexpr int smem = split_smem_bytes<D>();
-  auto kern = split_attention_kernel<kBF16, D, kDirect>;
+  constexpr int smem = split_smem_bytes<D, kS>();
+  auto kern = split_attention_kernel<kBF16, D, kDirect, kS>;
   static std::atomic<uint64_t> done{0};
   const cudaError_t e = ensure_smem_limit(kern, smem, done);
   if (e != cudaSuccess) return e;
@@ -1195,7 +1201,16 @@ int split_ctas(const AttnParams& p, int num_sms) {
 cudaError_t launch_split_attention(const AttnParams& p, bool bf16, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int ctas, cudaStream_t stream,
                                    bool pdl) {
-  // the direct mode is its own instantiation, so the planned kernel carries none of it
+  // the direct mode is its own instantiation, so the planned kernel carries none of it;
+  // with no block table longer than kDirectSmallPages its ring has two stages: a warp
+  // streams at most that many pages, and the smaller footprint starts the launch sooner
+  if (p.direct && p.max_blocks <= kDirectSmallPages) {
+    if (p.D == 128)
+      return bf16 ? launch_split_t<true, 128, true, 2>(p, kmap, vmap, ctas, stream, pdl)
+                  : launch_split_t<false, 128, true, 2>(p, kmap, vmap, ctas, stream, pdl);
+    return bf16 ? launch_split_t<true, 64, true, 2>(p, kmap, vmap, ctas, stream, pdl)
+                : launch_split_t<false, 64, true, 2>(p, kmap, vmap, ctas, stream, pdl);
+  }
   if (p.direct) {
     if (p.D == 128)
       return bf16 ? launch_split_t<true, 128, true>(p, kmap, vmap, ctas, stream, pdl)

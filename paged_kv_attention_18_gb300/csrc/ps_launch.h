@@ -207,6 +207,8 @@ cudaError_t launch_combine(const AttnParams& p, bool bf16, int num_sms, cudaStre
 // Largest block-table width (pages) the direct mode takes: one warp streams a sequence's
 // whole context, which for this many pages takes no longer than a plan would.
 constexpr int kDirectMaxPages = 64;
+// Block-table width (pages) up to which the direct mode's ring has two stages.
+constexpr int kDirectSmallPages = 8;
 
 // True when a batch of T packed tokens fits the direct mode: every sequence's rows (n * G
 // <= T * G) fit one 16-row group, no block table is wide enough for the planner to split a
