@@ -355,6 +355,23 @@ def test_direct_tile_batches(case, separate):
     check_workload(wl, separate_calls=separate)
 
 
+@pytest.mark.parametrize("separate", [False, True])
+def test_split_rows_of_both_kernels_combined(separate):
+    # 38 long decodes (the split kernel splits them) beside two short chunks of long
+    # contexts (too few tile items: the planner splits those too); one combine after the
+    # tile kernel merges the partials of both kernels' rows
+    seqs = [(1000 + (53 * i) % 2000, 1) for i in range(38)] + [(3000, 64), (2500, 100)]
+    wl = W.simple_workload("both_split", seed=90, dtype="bf16", H_q=12, H_kv=2, D=128,
+                           seqs=seqs)
+    pools = DevicePools(wl)
+    binding.profile_begin(8)
+    run_step(wl, wl.steps[0], pools, separate_calls=separate)
+    prof = binding.profile_end()
+    assert prof["split_attention"][1] == 1 and prof["tile_attention"][1] == 1
+    assert prof["combine"][1] == 1
+    check_workload(wl, separate_calls=separate)
+
+
 def test_direct_tile_bad_sequence_sets_device_error():
     wl = W.simple_workload("dtile_bad", seed=80, dtype="bf16", H_q=12, H_kv=2, D=128,
                            seqs=[(200, 100), (300, 40)])
