@@ -1010,7 +1010,7 @@ def run_spec_accept(args, rank, world, local_rank) -> dict | None:
                    "l2": "probability rows (400 MB target, 320 MB draft) larger than L2"},
         "roofline": {"bound": "hbm", "achieved": head["gbs"] / world, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": head["gbs"] / world / peaks["hbm_gbs"],
-                     "traffic": None, "kernel": "spec_chunk_kernel + spec_final_kernel",
+                     "traffic": None, "kernel": "spec_run_kernel + spec_final_kernel",
                      "peak_source": f"{peaks_src} (hbm_gbs)"},
         "modes": res,
         "gpu_launches": 2 * args.steps,

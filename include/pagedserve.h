@@ -191,8 +191,9 @@ int ps_rope_reshape_and_cache(void* q, const void* k, const void* v, const int32
  *   workspace     device scratch of ps_spec_accept_workspace_size(B, k, V) bytes,
  *                 256-byte aligned.
  * Probabilities are expected in [0, 1]; other values give unspecified tokens, never a
- * fault. B = 0 is a no-op; k = 0 draws one token from p_0; k > 31 returns
- * PS_ERR_UNSUPPORTED.
+ * fault. B = 0 is a no-op; k = 0 draws one token from p_0; k > 31 or V > 2^30 returns
+ * PS_ERR_UNSUPPORTED. Rows are read as 16-byte words when V is a multiple of 4 and both
+ * probability arrays are 16-byte aligned, and as 4-byte words otherwise.
  */
 size_t ps_spec_accept_workspace_size(int B, int k, int V);
 int ps_spec_accept(const float* target_probs, const float* draft_probs,

@@ -465,8 +465,8 @@ size_t ps_spec_accept_workspace_size(int B, int k, int V) {
   if (B < 0 || k < 0 || V <= 0) return 0;
   const size_t c = static_cast<size_t>(ps::spec_chunks(V));
   const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
-  return ps::up256(static_cast<size_t>(B) * c * 8) + 2 * ps::up256(rows * 4) +
-         ps::up256(static_cast<size_t>(B) * 4);
+  const size_t runs = static_cast<size_t>(B) * ps::spec_runs(V);
+  return ps::up256(runs * 8) + 2 * ps::up256(rows * 4) + ps::up256(static_cast<size_t>(B) * 4);
 }
 
 int ps_spec_accept(const float* target_probs, const float* draft_probs,
@@ -475,6 +475,7 @@ int ps_spec_accept(const float* target_probs, const float* draft_probs,
                    size_t workspace_bytes, void* stream) {
   if (B < 0 || k < 0 || V <= 0) return PS_ERR_ARG;
   if (k > 31) return PS_ERR_UNSUPPORTED;  // one lane per draft decides the acceptance
+  if (V > (1 << 30)) return PS_ERR_UNSUPPORTED;  // token indices stay 32-bit
   if (B == 0) return PS_OK;
   if (!target_probs || !out_tokens || !num_accepted) return PS_ERR_ARG;
   if (k > 0 && !draft_tokens) return PS_ERR_ARG;
@@ -487,6 +488,7 @@ int ps_spec_accept(const float* target_probs, const float* draft_probs,
   if (rc) return rc;
   const size_t c = static_cast<size_t>(ps::spec_chunks(V));
   const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
+  const size_t runs = ps::up256(static_cast<size_t>(B) * ps::spec_runs(V) * 8);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   ps::SpecParams a = {};
   a.p = target_probs;
@@ -500,9 +502,10 @@ int ps_spec_accept(const float* target_probs, const float* draft_probs,
   a.out = out_tokens;
   a.num = num_accepted;
   a.wsum = reinterpret_cast<long long*>(ws);
-  a.amax_v = reinterpret_cast<float*>(ws + ps::up256(static_cast<size_t>(B) * c * 8));
-  a.amax_i = reinterpret_cast<int*>(ws + ps::up256(static_cast<size_t>(B) * c * 8) + ps::up256(rows * 4));
-  a.acc = reinterpret_cast<int*>(ws + ps::up256(static_cast<size_t>(B) * c * 8) + 2 * ps::up256(rows * 4));
+  a.amax_v = reinterpret_cast<float*>(ws + runs);
+  a.amax_i = reinterpret_cast<int*>(ws + runs + ps::up256(rows * 4));
+  a.acc = reinterpret_cast<int*>(ws + runs + 2 * ps::up256(rows * 4));
+  a.num_sms = ds->num_sms;
   a.err = ds->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Timed tm(7, s);

@@ -12,10 +12,12 @@
 // their sums are exact in any order; the sample is the first token whose running sum of
 // W exceeds floor(R * Z / 2^32), Z the total. Argmax ties go to the lowest token.
 //
-// Two kernels: the first, one CTA per (sequence, chunk of the vocabulary), reduces its
-// chunk of the rows it needs (fixed-point sums of the residual row, or argmaxes of every
-// row in greedy mode) so the whole GPU streams the probability rows; the second, one CTA
-// per sequence, combines the chunks and scans only the chunk that holds the sample.
+// Two kernels per call. Rejection rule: the first streams the one residual row each
+// sequence needs as 128-token runs, spread evenly over about four CTAs per SM, and writes
+// every run's fixed-point sum; the second, one CTA per sequence, scans those sums, then
+// reads only the run that holds the sample. Greedy: the first, one CTA per (sequence,
+// chunk of the vocabulary), takes the chunk argmax of every row; the second combines them.
+// Every sum is an exact integer, so how a row is cut into runs never changes the token.
 #include "ps_common.cuh"
 #include "ps_launch.h"
 
@@ -24,35 +26,24 @@ namespace ps {
 namespace {
 
 constexpr int kThreads = 256;  // also the largest chunk count (spec_chunks caps it at 64)
+constexpr int kWarps = kThreads / 32;
+constexpr int kRun = 128;          // tokens per run: four per lane
+#ifndef PS_SPEC_CTAS_PER_SM
+#define PS_SPEC_CTAS_PER_SM 4
+#endif
+constexpr int kCtasPerSm = PS_SPEC_CTAS_PER_SM;        // resident run-kernel CTAs per SM
 
-// trunc(w * 2^40) for w > 0 (0 otherwise), from the float's fields: a normal w is
-// (2^23 + mantissa) * 2^(exponent - 150), so the result is that integer shifted by
-// exponent - 110; subnormals (below 2^-126) give 0. Integer shifts only: the same value
-// as an exact float-to-integer conversion, without the conversion unit.
-__device__ __forceinline__ int64_t fixed_weight(float w) {
-  if (!(w > 0.f)) return 0;
-  const uint32_t bits = __float_as_uint(w);
-  const int e = static_cast<int>(bits >> 23);  // sign bit is 0
-  if (e == 0) return 0;
-  const uint64_t m = (bits & 0x7fffffu) | 0x800000u;
-  const int sh = e - 110;
-  if (sh >= 0) return static_cast<int64_t>(m << sh);  // w < 2^23, so sh <= 39
-  return sh > -64 ? static_cast<int64_t>(m >> -sh) : 0;
+// trunc(w * 2^40) for w > 0, 0 for w <= 0 and NaN: scaling by 2^40 is exact and the
+// conversion truncates toward zero, so this is the exact integer for every w below 2^23.
+__device__ __forceinline__ long long fixed_weight(float w) {
+  return w > 0.f ? static_cast<long long>(__float2ull_rz(w * 1099511627776.0f)) : 0;
 }
 
-// Residual weight of token v at row r: max(p - q, 0) with q the draft distribution, or
-// the one-hot of the draft token when there is none (a deterministic proposer), or 0 when
-// r is the bonus row or the draft was invalid (the weight is then p itself).
-__device__ __forceinline__ float residual(const SpecParams& a, int b, int r, bool bonus,
-                                          int64_t v, float pv) {
-  if (bonus) return pv;
-  float qv;
-  if (a.q) {
-    qv = a.q[(static_cast<int64_t>(b) * a.k + r) * a.V + v];
-  } else {
-    qv = v == a.drafts[b * a.k + r] ? 1.f : 0.f;
-  }
-  return fmaxf(__fsub_rn(pv, qv), 0.f);
+// The fixed-point weight of one token: max(p - q_e, 0), q_e the draft's probability of the
+// token (1 at the draft token of a one-hot row; 0 on a row drawn from p itself, whose
+// weight is then p).
+__device__ __forceinline__ long long token_weight(float pv, float qe) {
+  return fixed_weight(fmaxf(__fsub_rn(pv, qe), 0.f));
 }
 
 // Acceptance of sequence b's drafts under the rejection rule, by the calling warp (one
@@ -81,23 +72,6 @@ __device__ int accepted_warp(const SpecParams& a, int b, bool* plain, bool* inva
   *invalid = rej != 0 && inv;
   *plain = rej == 0 || *invalid;
   return r;
-}
-
-// The acceptance of sequence b, decided by warp 0 and shared with the block.
-__device__ int accepted_block(const SpecParams& a, int b, bool* plain, bool* invalid) {
-  __shared__ int sh_r, sh_flags;
-  if (threadIdx.x < 32) {
-    bool pl, inv;
-    const int r = accepted_warp(a, b, &pl, &inv);
-    if (threadIdx.x == 0) {
-      sh_r = r;
-      sh_flags = (pl ? 1 : 0) | (inv ? 2 : 0);
-    }
-  }
-  __syncthreads();
-  *plain = sh_flags & 1;
-  *invalid = (sh_flags & 2) != 0;
-  return sh_r;
 }
 
 template <typename T>
@@ -140,93 +114,202 @@ __device__ void block_argmax(float& v, int& i, float* shv, int* shi) {
   __syncthreads();
 }
 
-// grid (chunks, B): chunk statistics of the rows sequence b needs. With V a multiple of 4
-// every row starts 16-byte aligned and chunks are multiples of 8 tokens, so rows stream
-// as float4 loads, two per thread in flight.
+// grid (chunks, B), greedy rule: the argmax of each of sequence b's k + 1 rows over one
+// chunk of the vocabulary. With V a multiple of 4 and p 16-byte aligned every row starts
+// 16-byte aligned and chunks are multiples of 8 tokens, so rows stream as float4 loads,
+// four per thread in flight.
 __global__ void __launch_bounds__(kThreads) spec_chunk_kernel(const SpecParams a) {
-  __shared__ long long shl[kThreads / 32];
   __shared__ float shv[kThreads / 32];
   __shared__ int shi[kThreads / 32];
   pdl_launch_dependents();
   const int c = blockIdx.x, b = blockIdx.y;
   const int64_t lo = static_cast<int64_t>(c) * a.chunk;
   const int64_t hi = lo + a.chunk < a.V ? lo + a.chunk : a.V;
-  const bool vec = (a.V & 3) == 0;
-  if (a.greedy) {
-    for (int i = 0; i <= a.k; ++i) {
-      const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + i) * a.V;
-      float v = -INFINITY;
-      int t = INT32_MAX;
+  const bool vec = a.vec != 0;
+  for (int i = 0; i <= a.k; ++i) {
+    const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + i) * a.V;
+    float v = -INFINITY;
+    int t = INT32_MAX;
+    if (vec) {
+      // four float4 loads per thread in flight
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      for (int64_t x0 = lo / 4 + threadIdx.x; x0 < hi / 4; x0 += 4 * kThreads) {
+        float4 f[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t x = x0 + u * kThreads;
+          f[u] = x < hi / 4 ? __ldcs(r4 + x) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int base = static_cast<int>(4 * (x0 + u * kThreads));
+          amax_merge(v, t, f[u].x, base);
+          amax_merge(v, t, f[u].y, base + 1);
+          amax_merge(v, t, f[u].z, base + 2);
+          amax_merge(v, t, f[u].w, base + 3);
+        }
+      }
+    } else {
+      for (int64_t x = lo + threadIdx.x; x < hi; x += kThreads)
+        amax_merge(v, t, row[x], static_cast<int>(x));
+    }
+    block_argmax(v, t, shv, shi);
+    if (threadIdx.x == 0) {
+      const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.chunks + c;
+      a.amax_v[o] = v;
+      a.amax_i[o] = t;
+    }
+  }
+}
+
+// Sums over the warp of N values per lane: lane l returns the sum of value l / (32 / N)
+// (lanes other than the first of each group of 32 / N hold the same sum). Each exchange
+// at distance 16, 8, ... halves the values a lane holds, the two halves of the warp
+// keeping different ones; the rest is a plain butterfly.
+template <int N>
+__device__ __forceinline__ long long warp_sum_n(long long (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = N / 2, dist = 16; half >= 1; half /= 2, dist /= 2) {
+    const bool up = lane & dist;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const long long keep = up ? v[i + half] : v[i];
+      const long long send = up ? v[i] : v[i + half];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, dist);
+    }
+  }
+#pragma unroll
+  for (int dist = 16 / N; dist >= 1; dist /= 2) v[0] += __shfl_xor_sync(0xffffffffu, v[0], dist);
+  return v[0];
+}
+
+// trunc(w * 2^40) = hi * 2^20 + lo with hi = floor(y), y = w * 2^20, and lo = floor((y - hi)
+// * 2^20), for 0 <= w < 8: adding 2^23 rounded toward zero drops the fraction of any value
+// in [0, 2^23), and every other step is exact, so both parts are integers held exactly in
+// fp32 and their sums over a few tokens stay exact.
+__device__ __forceinline__ void weight_parts(float w, float& hi, float& lo) {
+  const float y = w * 1048576.0f;
+  hi = __fsub_rn(__fadd_rz(y, 8388608.0f), 8388608.0f);
+  const float z = __fsub_rn(y, hi) * 1048576.0f;
+  lo = __fsub_rn(__fadd_rz(z, 8388608.0f), 8388608.0f);
+}
+
+// An integer-valued float in [0, 2^23) as an integer: its bits after adding 2^23.
+__device__ __forceinline__ int small_int(float x) {
+  return __float_as_int(__fadd_rn(x, 8388608.0f)) - 0x4B000000;
+}
+
+// Rejection rule, grid G (one wave of resident CTAs). The rows the sequences need are cut
+// into runs of 128 tokens, listed sequence by sequence: U = B * runs. CTA j takes the
+// runs [j*U/G, (j+1)*U/G), so every CTA streams the same number of bytes; its warp w
+// takes runs w*N .. w*N+N-1 of each group of 8N (N = 4 with draft rows q, 8 without), loads
+// all N before summing any, and writes each run's fixed-point residual sum. Tokens past the
+// end of a row load as zeros, which weigh 0. A warp decides the acceptance of a sequence
+// when it first meets one of its runs (the one that holds run 0 records it).
+template <bool kQ>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_run_kernel(const SpecParams a) {
+  constexpr int kN = kQ ? 4 : 8;  // runs a warp loads before summing any
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t U = static_cast<int64_t>(a.B) * a.runs;
+  const int64_t u_lo = U * blockIdx.x / gridDim.x;
+  const int64_t u_hi = U * (blockIdx.x + 1) / gridDim.x;
+  const bool vec = a.vec != 0;
+  // (sequence, run) of the warp's first run of the group, advanced without division
+  int64_t u0 = u_lo + warp * kN;
+  int b0 = static_cast<int>(u0 / a.runs);
+  int m0 = static_cast<int>(u0 - static_cast<int64_t>(b0) * a.runs);
+  // the acceptance of the sequence the warp last met, and its row pointers
+  int cur_b = -1, draft = -1;
+  const float* row = nullptr;
+  const float* qrow = nullptr;
+  for (; u0 < u_hi; u0 += kWarps * kN) {
+    float4 f[kN], g[kQ ? kN : 1];  // p, and q (0 on a row without one)
+    int dl[kN];  // the one-hot draft token relative to the run, -1 for none
+    int b = b0, m = m0;
+#pragma unroll
+    for (int t = 0; t < kN; ++t) {
+      f[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kQ) g[t] = f[t];
+      dl[t] = -1;
+      if (t > 0 && ++m == a.runs) {
+        m = 0;
+        ++b;
+      }
+      if (u0 + t >= u_hi) continue;  // warp-uniform
+      if (b != cur_b) {
+        bool plain, invalid;
+        const int r = accepted_warp(a, b, &plain, &invalid);
+        if (m == 0 && lane == 0)
+          a.acc[b] = r | (plain ? 1 << 8 : 0) | (invalid ? 1 << 9 : 0);
+        cur_b = b;
+        row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
+        qrow = (kQ && !plain) ? a.q + (static_cast<int64_t>(b) * a.k + r) * a.V : nullptr;
+        draft = (!kQ && !plain) ? a.drafts[b * a.k + r] : -1;
+      }
+      const int t0 = m * kRun;
+      dl[t] = draft >= t0 && draft < t0 + kRun ? draft - t0 : -1;
       if (vec) {
-        // four float4 loads per thread in flight
-        const float4* r4 = reinterpret_cast<const float4*>(row);
-        for (int64_t x0 = lo / 4 + threadIdx.x; x0 < hi / 4; x0 += 4 * kThreads) {
-          float4 f[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int64_t x = x0 + u * kThreads;
-            f[u] = x < hi / 4 ? __ldcs(r4 + x) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int base = static_cast<int>(4 * (x0 + u * kThreads));
-            amax_merge(v, t, f[u].x, base);
-            amax_merge(v, t, f[u].y, base + 1);
-            amax_merge(v, t, f[u].z, base + 2);
-            amax_merge(v, t, f[u].w, base + 3);
-          }
+        // lane l: tokens t0 + 4l .. t0 + 4l + 3 (V a multiple of 4: all or none in range)
+        const int v = t0 + 4 * lane;
+        if (v < a.V) {
+          f[t] = __ldcs(reinterpret_cast<const float4*>(row + v));
+          if (kQ && qrow) g[t] = __ldcs(reinterpret_cast<const float4*>(qrow + v));
         }
       } else {
-        for (int64_t x = lo + threadIdx.x; x < hi; x += kThreads)
-          amax_merge(v, t, row[x], static_cast<int>(x));
-      }
-      block_argmax(v, t, shv, shi);
-      if (threadIdx.x == 0) {
-        const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.chunks + c;
-        a.amax_v[o] = v;
-        a.amax_i[o] = t;
-      }
-    }
-    return;
-  }
-  bool plain, invalid;
-  const int r = accepted_block(a, b, &plain, &invalid);
-  if (c == 0 && threadIdx.x == 0) a.acc[b] = r | (plain ? 1 << 8 : 0) | (invalid ? 1 << 9 : 0);
-  const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
-  const float* qrow = (!plain && a.q) ? a.q + (static_cast<int64_t>(b) * a.k + r) * a.V : nullptr;
-  const int draft = (!plain && !a.q) ? a.drafts[b * a.k + r] : -1;
-  long long s = 0;
-  if (vec) {
-    // four float4 loads of p (and of q) per thread in flight
-    const float4* p4 = reinterpret_cast<const float4*>(row);
-    const float4* q4 = reinterpret_cast<const float4*>(qrow);
-    for (int64_t x0 = lo / 4 + threadIdx.x; x0 < hi / 4; x0 += 4 * kThreads) {
-      float4 f[4], g[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t x = x0 + u * kThreads;
-        const bool in = x < hi / 4;
-        f[u] = in ? __ldcs(p4 + x) : make_float4(0.f, 0.f, 0.f, 0.f);
-        g[u] = (in && qrow) ? __ldcs(q4 + x) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float pv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-        const float qv[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+        // lane l: tokens t0 + l + 32e, 4-byte loads
+        float* fe = &f[t].x;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int64_t v = 4 * (x0 + u * kThreads) + e;
-          const float qe = qrow ? qv[e] : (v == draft ? 1.f : 0.f);
-          s += fixed_weight(plain ? pv[e] : fmaxf(__fsub_rn(pv[e], qe), 0.f));
+          const int v = t0 + lane + 32 * e;
+          if (v < a.V) {
+            fe[e] = __ldcs(row + v);
+            if (kQ && qrow) (&g[t].x)[e] = __ldcs(qrow + v);
+          }
         }
       }
     }
-  } else {
-    for (int64_t x = lo + threadIdx.x; x < hi; x += kThreads)
-      s += fixed_weight(residual(a, b, r, plain, x, row[x]));
+    long long s[kN];
+#pragma unroll
+    for (int t = 0; t < kN; ++t) {
+      const float pv[4] = {f[t].x, f[t].y, f[t].z, f[t].w};
+      float qv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (kQ) {
+        qv[0] = g[kQ ? t : 0].x;
+        qv[1] = g[kQ ? t : 0].y;
+        qv[2] = g[kQ ? t : 0].z;
+        qv[3] = g[kQ ? t : 0].w;
+      } else if (dl[t] >= 0) {  // warp-uniform: the draft token of a one-hot row is here
+        const int l = vec ? dl[t] >> 2 : dl[t] & 31;
+        const int e = vec ? dl[t] & 3 : dl[t] >> 5;
+        if (lane == l) {
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            if (x == e) qv[x] = 1.f;
+        }
+      }
+      float hs = 0.f, ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float hi, lo;
+        weight_parts(fmaxf(__fsub_rn(pv[e], qv[e]), 0.f), hi, lo);
+        hs += hi;
+        ls += lo;
+      }
+      s[t] = (static_cast<long long>(small_int(hs)) << 20) + small_int(ls);
+    }
+    const long long tot = warp_sum_n<kN>(s);
+    const int j = lane / (32 / kN);
+    if (lane % (32 / kN) == 0 && u0 + j < u_hi) a.wsum[u0 + j] = tot;
+    // (b, m) is the group's last run; the next group starts kWarps * kN runs after its first
+    b0 = b;
+    m0 = m + (kWarps - 1) * kN + 1;
+    while (m0 >= a.runs) {
+      m0 -= a.runs;
+      ++b0;
+    }
   }
-  s = block_sum(s, shl);
-  if (threadIdx.x == 0) a.wsum[static_cast<int64_t>(b) * a.chunks + c] = s;
 }
 
 // Exclusive scan of one value per thread over the block; *total gets the block's sum.
@@ -250,59 +333,32 @@ __device__ long long block_exscan_ll(long long v, long long* sh, long long* tota
   return before + inc - v;
 }
 
-// Token of the first running sum above `target` within [lo, hi) of row r (weights
-// recomputed), given the sum `base` of every weight before lo; one CTA. Each thread sums
-// 32 consecutive tokens, a block scan places the target in one thread's run, and that
-// thread walks its 32 tokens again.
-__device__ int scan_for(const SpecParams& a, int b, int r, bool plain, int64_t lo, int64_t hi,
-                        long long base, unsigned long long target, long long* sh) {
+// Token of the first running sum above `target` along all of row r of p (weights p
+// itself, the draw when no residual mass is left); one CTA. Each thread sums 32
+// consecutive tokens, a block scan places the target in one thread's run, and that thread
+// walks its 32 tokens again.
+__device__ int scan_row_p(const SpecParams& a, int b, int r, unsigned long long target,
+                          long long* sh) {
   __shared__ int found;
   constexpr int kPer = 32;
   const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
-  const float* qrow = (!plain && a.q) ? a.q + (static_cast<int64_t>(b) * a.k + r) * a.V : nullptr;
-  const int draft = (!plain && !a.q) ? a.drafts[b * a.k + r] : -1;
-  const bool vec = (a.V & 3) == 0 && (lo & 7) == 0;
-  auto weight = [&](int64_t x, float pv, float qv) -> long long {
-    if (x >= hi) return 0;
-    if (plain) return fixed_weight(pv);
-    const float qe = qrow ? qv : (x == draft ? 1.f : 0.f);
-    return fixed_weight(fmaxf(__fsub_rn(pv, qe), 0.f));
-  };
-  // sum (or, with `target_in`, locate) over the run [first, first + 32)
+  // sum (or, with `locate`, find the token) over the run [first, first + 32)
   auto run_sum = [&](int64_t first, bool locate, long long acc) -> long long {
     long long sum = 0;
-    if (vec && first + kPer <= hi) {
-      const float4* p4 = reinterpret_cast<const float4*>(row + first);
-      const float4* q4 = reinterpret_cast<const float4*>(qrow ? qrow + first : row + first);
-#pragma unroll
-      for (int e4 = 0; e4 < kPer / 4; ++e4) {
-        const float4 f = p4[e4];
-        const float4 g = qrow ? q4[e4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float pv[4] = {f.x, f.y, f.z, f.w};
-        const float qv[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int64_t x = first + 4 * e4 + e;
-          sum += weight(x, pv[e], qv[e]);
-          if (locate && static_cast<unsigned long long>(acc + sum) > target) return x;
-        }
-      }
-    } else {
-      for (int e = 0; e < kPer; ++e) {
-        const int64_t x = first + e;
-        if (x >= hi) break;
-        sum += weight(x, row[x], qrow ? qrow[x] : 0.f);
-        if (locate && static_cast<unsigned long long>(acc + sum) > target) return x;
-      }
+    for (int e = 0; e < kPer; ++e) {
+      const int64_t x = first + e;
+      if (x >= a.V) break;
+      sum += token_weight(row[x], 0.f);
+      if (locate && static_cast<unsigned long long>(acc + sum) > target) return x;
     }
     return locate ? -1 : sum;
   };
   if (threadIdx.x == 0) found = -1;
   __syncthreads();
-  long long run = base;
-  for (int64_t tile = lo; tile < hi; tile += static_cast<int64_t>(kThreads) * kPer) {
+  long long run = 0;
+  for (int64_t tile = 0; tile < a.V; tile += static_cast<int64_t>(kThreads) * kPer) {
     const int64_t first = tile + static_cast<int64_t>(threadIdx.x) * kPer;
-    const long long mine = first < hi ? run_sum(first, false, 0) : 0;
+    const long long mine = first < a.V ? run_sum(first, false, 0) : 0;
     long long total;
     const long long acc = run + block_exscan_ll(mine, sh, &total);
     if (mine > 0 && static_cast<unsigned long long>(acc) <= target &&
@@ -315,13 +371,52 @@ __device__ int scan_for(const SpecParams& a, int b, int r, bool plain, int64_t l
   return found;
 }
 
+// Token of the first running sum above `target` within run m of sequence b's row r, given
+// the sum `base` of every weight before the run; the calling warp (lane l holds tokens
+// 128m + 4l .. 128m + 4l + 3, in order). -1 when no token reaches the target.
+__device__ int run_locate(const SpecParams& a, int b, int r, bool plain, int m, long long base,
+                          unsigned long long target) {
+  const int lane = threadIdx.x & 31;
+  const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
+  const float* qrow = (!plain && a.q) ? a.q + (static_cast<int64_t>(b) * a.k + r) * a.V : nullptr;
+  const int draft = (!plain && !a.q) ? a.drafts[b * a.k + r] : -1;
+  const int64_t v0 = static_cast<int64_t>(m) * kRun + 4 * lane;
+  long long w[4], mine = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int64_t v = v0 + e;
+    w[e] = v < a.V ? token_weight(row[v], v == draft ? 1.f : (qrow ? qrow[v] : 0.f)) : 0;
+    mine += w[e];
+  }
+  long long inc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  const unsigned hit =
+      __ballot_sync(0xffffffffu, static_cast<unsigned long long>(base + inc) > target);
+  if (!hit) return -1;
+  const int first = __ffs(hit) - 1;
+  int tok = -1;
+  if (lane == first) {
+    long long acc = base + inc - mine;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc += w[e];
+      if (tok < 0 && static_cast<unsigned long long>(acc) > target) tok = static_cast<int>(v0 + e);
+    }
+  }
+  return __shfl_sync(0xffffffffu, tok, first);
+}
+
 // grid B: acceptance and the final token of each sequence
 __global__ void __launch_bounds__(kThreads) spec_final_kernel(const SpecParams a) {
   __shared__ long long shl[kThreads / 32];
   __shared__ float shv[kThreads / 32];
   __shared__ int shi[kThreads / 32];
   __shared__ long long sh_base;
-  __shared__ int sh_chunk;
+  __shared__ int sh_run;
   pdl_launch_dependents();
   pdl_wait();
   const int b = blockIdx.x;
@@ -341,43 +436,56 @@ __global__ void __launch_bounds__(kThreads) spec_final_kernel(const SpecParams a
       ++n_acc;
     }
   } else {
-    // the acceptance recorded by the first chunk's CTA, and the chunk sums (chunks <=
-    // threads) with their scan, loaded together
+    // the acceptance recorded with the sequence's first run; thread t sums the run sums
+    // [t*per, (t+1)*per) of the row
     const int info = a.acc[b];
     const int r = info & 0xff;
     const bool plain = (info >> 8) & 1, invalid = (info >> 9) & 1;
     if (invalid && threadIdx.x == 0) record_error(a.err, kDevBadToken);
     n_acc = r;
     const unsigned long long R = a.rnd[b * (a.k + 1) + a.k];
+    const long long* rs = a.wsum + static_cast<int64_t>(b) * a.runs;
+    const int per = (a.runs + kThreads - 1) / kThreads;
+    const int m0 = min(static_cast<int>(threadIdx.x) * per, a.runs);
+    const int m1 = min(m0 + per, a.runs);
+    long long cs = 0;
+    for (int m = m0; m < m1; ++m) cs += rs[m];
     if (threadIdx.x == 0) {
       sh_base = 0;
-      sh_chunk = 0;
+      sh_run = -1;
     }
-    const long long cs = threadIdx.x < a.chunks ? a.wsum[static_cast<int64_t>(b) * a.chunks + threadIdx.x] : 0;
     long long Z;
     const long long before = block_exscan_ll(cs, shl, &Z);
+    tok = -1;
     if (Z > 0) {
       const unsigned long long target = __umul64hi(static_cast<unsigned long long>(Z), R << 32);
-      // the chunk holding the target
-      if (threadIdx.x < a.chunks && cs > 0 && static_cast<unsigned long long>(before) <= target &&
+      // the run holding the target, found by the thread whose runs hold it
+      if (cs > 0 && static_cast<unsigned long long>(before) <= target &&
           static_cast<unsigned long long>(before + cs) > target) {
-        sh_base = before;
-        sh_chunk = threadIdx.x;
+        long long acc = before;
+        for (int m = m0; m < m1; ++m) {
+          const long long w = rs[m];
+          if (static_cast<unsigned long long>(acc + w) > target) {
+            sh_run = m;
+            sh_base = acc;
+            break;
+          }
+          acc += w;
+        }
       }
       __syncthreads();
-      const int64_t lo = static_cast<int64_t>(sh_chunk) * a.chunk;
-      const int64_t hi = lo + a.chunk < a.V ? lo + a.chunk : a.V;
-      tok = scan_for(a, b, r, plain, lo, hi, sh_base, target, shl);
+      if (threadIdx.x < 32 && sh_run >= 0)
+        tok = run_locate(a, b, r, plain, sh_run, sh_base, target);
     } else {
       // no residual mass (p <= q at every token): draw from p_r itself over the row
       long long Zp = 0;
       const float* row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
-      for (int64_t x = threadIdx.x; x < a.V; x += kThreads) Zp += fixed_weight(row[x]);
+      for (int64_t x = threadIdx.x; x < a.V; x += kThreads)
+        Zp += token_weight(row[x], 0.f);
       Zp = block_sum(Zp, shl);
-      tok = 0;
       if (Zp > 0) {
         const unsigned long long target = __umul64hi(static_cast<unsigned long long>(Zp), R << 32);
-        tok = scan_for(a, b, r, true, 0, a.V, 0, target, shl);
+        tok = scan_row_p(a, b, r, target, shl);
       }
     }
     if (tok < 0) tok = 0;
@@ -397,14 +505,30 @@ int spec_chunks(int V) {
   return c < 1 ? 1 : (c > 64 ? 64 : c);
 }
 
+int spec_runs(int V) { return (V + kRun - 1) / kRun; }
+
 cudaError_t launch_spec_accept(const SpecParams& a0, cudaStream_t stream) {
   if (a0.B == 0) return cudaSuccess;
   SpecParams a = a0;
   a.chunks = spec_chunks(a.V);
   a.chunk = ((a.V + a.chunks - 1) / a.chunks + 7) / 8 * 8;  // multiples of 8 tokens
   a.chunks = (a.V + a.chunk - 1) / a.chunk;
-  cudaError_t e = launch_kernel(spec_chunk_kernel, dim3(a.chunks, a.B), dim3(kThreads), 0,
-                                stream, false, a);
+  a.runs = spec_runs(a.V);
+  a.vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
+          (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+  cudaError_t e;
+  if (a.greedy) {
+    e = launch_kernel(spec_chunk_kernel, dim3(a.chunks, a.B), dim3(kThreads), 0, stream, false, a);
+  } else {
+    // one wave of resident CTAs, each at least one load group per warp
+    const int n = a.q ? 4 : 8;
+    const int64_t units = static_cast<int64_t>(a.B) * a.runs;
+    const int64_t by_work = (units + kWarps * n - 1) / (kWarps * n);
+    const int64_t cap = kCtasPerSm * static_cast<int64_t>(a.num_sms > 0 ? a.num_sms : 1);
+    const int grid = static_cast<int>(by_work < cap ? by_work : cap);
+    e = a.q ? launch_kernel(spec_run_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, false, a)
+            : launch_kernel(spec_run_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, false, a);
+  }
   if (e != cudaSuccess) return e;
   return launch_kernel(spec_final_kernel, dim3(a.B), dim3(kThreads), 0, stream, true, a);
 }

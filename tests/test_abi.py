@@ -157,6 +157,7 @@ def test_spec_accept_rejects(lib):
     assert f(*args(B=-1)) == -1              # batch
     assert f(*args(V=0)) == -1               # vocabulary
     assert f(*args(k=32)) == -2              # one lane per draft: k <= 31
+    assert f(*args(V=(1 << 30) + 1)) == -2   # token indices stay 32-bit
     assert f(*args(r=None)) == -1            # random words needed by the rejection rule
     assert f(*args(dr=None)) == -1           # drafts needed when k > 0
     assert f(*args(ws=FAKE + 16)) == -4      # workspace alignment (256 bytes)

@@ -38,7 +38,10 @@ def run(p, drafts, rnd, q=None, greedy=False):
     return out.cpu().numpy(), num.cpu().numpy()
 
 
-@pytest.mark.parametrize("B,k,V", [(64, 4, 1000), (37, 3, 3001), (20, 4, 8197), (9, 1, 50000)])
+# (512, 2, 200): two 128-token runs per row, so one CTA's share of runs spans many
+# sequences and its warps decide many acceptances
+@pytest.mark.parametrize("B,k,V", [(64, 4, 1000), (37, 3, 3001), (20, 4, 8197), (9, 1, 50000),
+                                   (512, 2, 200)])
 @pytest.mark.parametrize("mode", ["draft_model", "ngram", "greedy"])
 def test_matches_oracle(B, k, V, mode):
     p, q, drafts, rnd = make_case(B, k, V, seed=B + k + V, peak=6.0 if mode == "ngram" else 2.0)
@@ -73,6 +76,26 @@ def test_full_vocabulary_batch():
     assert binding.device_error() == 0
     np.testing.assert_array_equal(got[1], ref[1])
     np.testing.assert_array_equal(got[0], ref[0])
+
+
+def test_unaligned_rows_take_word_loads():
+    # V a multiple of 4 but p and q 4 bytes past a 16-byte boundary: rows read as 4-byte words
+    B, k, V = 24, 3, 4096
+    p, q, drafts, rnd = make_case(B, k, V, seed=77)
+    flat_p = torch.zeros(p.size + 1, dtype=torch.float32, device="cuda")
+    flat_q = torch.zeros(q.size + 1, dtype=torch.float32, device="cuda")
+    pd = flat_p[1:].view(B, k + 1, V)
+    qd = flat_q[1:].view(B, k, V)
+    pd.copy_(torch.from_numpy(p))
+    qd.copy_(torch.from_numpy(q))
+    assert pd.data_ptr() % 16 == 4 and qd.data_ptr() % 16 == 4
+    out, num = binding.spec_accept(pd, torch.from_numpy(drafts).cuda(),
+                                   torch.from_numpy(rnd.view(np.int32)).cuda(), qd)
+    torch.cuda.synchronize()
+    ref = oracle.spec_accept(p, drafts, rnd, q)
+    assert binding.device_error() == 0
+    np.testing.assert_array_equal(num.cpu().numpy(), ref[1])
+    np.testing.assert_array_equal(out.cpu().numpy(), ref[0])
 
 
 def test_edges():
