@@ -312,6 +312,175 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_run_kernel(const Sp
   }
 }
 
+// ------------------------------------------------------------------------------------
+// Rejection rule with rows as 16-byte words: the runs and sums of spec_run_kernel, but the
+// rows reach shared memory by bulk copies, so the bytes in flight do not depend on
+// registers. A stage holds 16 KB: 16 runs of p and 16 of q, or 32 runs of p.
+// ------------------------------------------------------------------------------------
+constexpr int kStreamStages = 4;
+constexpr int kStageFloats = 4096;
+constexpr int kStreamThreads = (kWarps + 1) * 32;  // eight consumer warps, one producer
+constexpr int kStreamCtasPerSm = 3;
+
+struct StreamSmem {
+  float buf[kStreamStages][kStageFloats];
+  uint64_t full[kStreamStages];   // the stage's copies landed (one arrival with the bytes)
+  uint64_t empty[kStreamStages];  // the stage was read (one arrival per consumer warp)
+  int has_q[kStreamStages];       // q copied into the stage's second half
+  int draft[kStreamStages];       // one-hot draft token relative to the stage, -1 for none
+};
+
+// One run of sequence rows after another within [u, u_hi): at most `cap` runs, never past
+// the end of a row.
+struct Chunk {
+  int64_t u;
+  int b, m, n;
+  __device__ __forceinline__ void fit(int64_t u_hi, int runs, int cap) {
+    const int64_t left = u_hi - u;
+    int k = runs - m < cap ? runs - m : cap;
+    n = left <= 0 ? 0 : (left < k ? static_cast<int>(left) : k);
+  }
+  __device__ __forceinline__ void next(int64_t u_hi, int runs, int cap) {
+    u += n;
+    m += n;
+    if (m == runs) {
+      m = 0;
+      ++b;
+    }
+    fit(u_hi, runs, cap);
+  }
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// grid G (one wave of resident CTAs), the same share of runs per CTA as spec_run_kernel.
+// The producer warp decides each sequence's acceptance when it meets its first run, then
+// copies each chunk of a row (p, and q where the row has one) into the next free stage;
+// consumer warp w sums runs w, w + 8, ... of every stage and releases it.
+template <bool kQ>
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
+    spec_stream_kernel(const SpecParams a) {
+  constexpr int kCap = kQ ? 16 : 32;  // runs per stage
+  constexpr int kPer = kCap / kWarps;  // runs per consumer warp and stage
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  StreamSmem& sm = *reinterpret_cast<StreamSmem*>(smem_raw);
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t U = static_cast<int64_t>(a.B) * a.runs;
+  const int64_t u_lo = U * blockIdx.x / gridDim.x;
+  const int64_t u_hi = U * (blockIdx.x + 1) / gridDim.x;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStreamStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  Chunk c0;
+  c0.u = u_lo;
+  c0.b = static_cast<int>(u_lo / a.runs);
+  c0.m = static_cast<int>(u_lo - static_cast<int64_t>(c0.b) * a.runs);
+  c0.fit(u_hi, a.runs, kCap);
+  if (warp == kWarps) {
+    // producer
+    const uint64_t pol = l2_policy_evict_first();
+    int cur_b = -1, r = 0, draft = -1;
+    bool plain = true;
+    int issued = 0;
+    for (Chunk c = c0; c.n > 0; c.next(u_hi, a.runs, kCap)) {
+      if (c.b != cur_b) {
+        bool invalid;
+        r = accepted_warp(a, c.b, &plain, &invalid);
+        if (c.m == 0 && lane == 0)
+          a.acc[c.b] = r | (plain ? 1 << 8 : 0) | (invalid ? 1 << 9 : 0);
+        cur_b = c.b;
+        draft = (!kQ && !plain) ? a.drafts[c.b * a.k + r] : -1;
+      }
+      const int s = issued % kStreamStages, use = issued / kStreamStages;
+      bool ok = true;
+      if (lane == 0) {
+        ok = use == 0 || mbar_wait(&sm.empty[s], (use - 1) & 1);
+        if (ok) {
+          const int t0 = c.m * kRun;
+          const int t1 = (c.m + c.n) * kRun < a.V ? (c.m + c.n) * kRun : a.V;
+          const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * 4;  // a multiple of 16
+          const bool hq = kQ && !plain;
+          sm.has_q[s] = hq ? 1 : 0;
+          sm.draft[s] = draft >= t0 && draft < t1 ? draft - t0 : -1;
+          mbar_arrive_expect_tx(&sm.full[s], hq ? 2 * bytes : bytes);
+          bulk_load(sm.buf[s], a.p + (static_cast<int64_t>(c.b) * (a.k + 1) + r) * a.V + t0,
+                    bytes, &sm.full[s], pol);
+          if (hq)
+            bulk_load(sm.buf[s] + kStageFloats / 2,
+                      a.q + (static_cast<int64_t>(c.b) * a.k + r) * a.V + t0, bytes,
+                      &sm.full[s], pol);
+        } else {
+          record_error(a.err, kDevWaitTimeout);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      ++issued;
+    }
+    // no copy may still be writing this CTA's shared memory when it exits
+    if (lane == 0) {
+      const int first = issued > kStreamStages ? issued - kStreamStages : 0;
+      for (int i = first; i < issued; ++i)
+        mbar_wait(&sm.full[i % kStreamStages], (i / kStreamStages) & 1);
+    }
+    return;
+  }
+  // consumers
+  int idx = 0;
+  for (Chunk c = c0; c.n > 0; c.next(u_hi, a.runs, kCap), ++idx) {
+    const int s = idx % kStreamStages;
+    if (!mbar_wait(&sm.full[s], (idx / kStreamStages) & 1)) {
+      if (lane == 0) record_error(a.err, kDevWaitTimeout);
+      break;
+    }
+    const bool hq = kQ && sm.has_q[s] != 0;
+    const int dd = kQ ? -1 : sm.draft[s];
+    long long sums[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int run = warp + kWarps * j;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f), g = f;
+      if (run < c.n && (c.m + run) * kRun + 4 * lane < a.V) {
+        f = *reinterpret_cast<const float4*>(&sm.buf[s][run * kRun + 4 * lane]);
+        if (hq) g = *reinterpret_cast<const float4*>(&sm.buf[s][kStageFloats / 2 + run * kRun + 4 * lane]);
+      }
+      const float pv[4] = {f.x, f.y, f.z, f.w};
+      float qv[4] = {g.x, g.y, g.z, g.w};
+      if (dd >= 0 && (dd >> 7) == run && ((dd & (kRun - 1)) >> 2) == lane) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          if (x == (dd & 3)) qv[x] = 1.f;
+      }
+      float hs = 0.f, ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float hi, lo;
+        weight_parts(fmaxf(__fsub_rn(pv[e], qv[e]), 0.f), hi, lo);
+        hs += hi;
+        ls += lo;
+      }
+      sums[j] = (static_cast<long long>(small_int(hs)) << 20) + small_int(ls);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    const long long tot = warp_sum_n<kPer>(sums);
+    const int j = lane / (32 / kPer);
+    if (lane % (32 / kPer) == 0 && warp + kWarps * j < c.n) a.wsum[c.u + warp + kWarps * j] = tot;
+  }
+}
+
 // Exclusive scan of one value per thread over the block; *total gets the block's sum.
 __device__ long long block_exscan_ll(long long v, long long* sh, long long* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -519,8 +688,29 @@ cudaError_t launch_spec_accept(const SpecParams& a0, cudaStream_t stream) {
   cudaError_t e;
   if (a.greedy) {
     e = launch_kernel(spec_chunk_kernel, dim3(a.chunks, a.B), dim3(kThreads), 0, stream, false, a);
+  } else if (a.vec) {
+    // one wave of resident CTAs, each at least one stage of runs
+    const int cap_runs = a.q ? 16 : 32;
+    const int64_t units = static_cast<int64_t>(a.B) * a.runs;
+    const int64_t by_work = (units + cap_runs - 1) / cap_runs;
+    const int64_t cap = kStreamCtasPerSm * static_cast<int64_t>(a.num_sms > 0 ? a.num_sms : 1);
+    const int grid = static_cast<int>(by_work < cap ? by_work : cap);
+    constexpr int smem = sizeof(StreamSmem);
+    if (a.q) {
+      static std::atomic<uint64_t> done{0};
+      e = ensure_smem_limit(spec_stream_kernel<true>, smem, done);
+      if (e == cudaSuccess)
+        e = launch_kernel(spec_stream_kernel<true>, dim3(grid), dim3(kStreamThreads), smem,
+                          stream, false, a);
+    } else {
+      static std::atomic<uint64_t> done{0};
+      e = ensure_smem_limit(spec_stream_kernel<false>, smem, done);
+      if (e == cudaSuccess)
+        e = launch_kernel(spec_stream_kernel<false>, dim3(grid), dim3(kStreamThreads), smem,
+                          stream, false, a);
+    }
   } else {
-    // one wave of resident CTAs, each at least one load group per warp
+    // rows as 4-byte words: one wave of resident CTAs, each at least one load group per warp
     const int n = a.q ? 4 : 8;
     const int64_t units = static_cast<int64_t>(a.B) * a.runs;
     const int64_t by_work = (units + kWarps * n - 1) / (kWarps * n);
