@@ -463,8 +463,9 @@ int ps_rope_reshape_and_cache(void* q, const void* k, const void* v, const int32
 
 size_t ps_spec_accept_workspace_size(int B, int k, int V) {
   if (B < 0 || k < 0 || V <= 0) return 0;
-  const size_t c = static_cast<size_t>(ps::spec_chunks(V));
-  const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
+  // greedy entries per row: one per run (16-byte rows) or per chunk, whichever is more
+  const int per_row = ps::spec_runs(V) > ps::spec_chunks(V) ? ps::spec_runs(V) : ps::spec_chunks(V);
+  const size_t rows = static_cast<size_t>(B) * (k + 1) * per_row;
   const size_t runs = static_cast<size_t>(B) * ps::spec_runs(V);
   return ps::up256(runs * 8) + 2 * ps::up256(rows * 4) + ps::up256(static_cast<size_t>(B) * 4);
 }
@@ -486,8 +487,8 @@ int ps_spec_accept(const float* target_probs, const float* draft_probs,
   DeviceState* ds;
   int rc = current_device_state(&ds);
   if (rc) return rc;
-  const size_t c = static_cast<size_t>(ps::spec_chunks(V));
-  const size_t rows = static_cast<size_t>(B) * (k + 1) * c;
+  const int per_row = ps::spec_runs(V) > ps::spec_chunks(V) ? ps::spec_runs(V) : ps::spec_chunks(V);
+  const size_t rows = static_cast<size_t>(B) * (k + 1) * per_row;
   const size_t runs = ps::up256(static_cast<size_t>(B) * ps::spec_runs(V) * 8);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   ps::SpecParams a = {};

@@ -149,15 +149,16 @@ struct SpecParams {
   const int32_t* drafts;   // [B, k]
   const uint32_t* rnd;     // [B, k + 1] random words (rejection rule only)
   int B, k, V, greedy;
-  int chunks, chunk;       // vocabulary chunks, greedy rule (set by the launcher)
-  int runs;                // 128-token runs per row, rejection rule (set by the launcher)
+  int chunks, chunk;       // vocabulary chunks, greedy rule with 4-byte rows (set by the launcher)
+  int runs;                // 128-token runs per row (set by the launcher)
+  int gent;                // greedy (max, token) entries per row (set by the launcher)
   int num_sms;
   int vec;                 // rows as float4 loads: V % 4 == 0, p and q 16-byte aligned
   int32_t* out;            // [B, k + 1] accepted drafts, the final token, then -1
   int32_t* num;            // [B] accepted drafts
   long long* wsum;         // [B, runs] workspace: fixed-point residual sums of the runs
-  float* amax_v;           // [B, k + 1, chunks] workspace: chunk maxima (greedy)
-  int* amax_i;             // [B, k + 1, chunks] workspace: their tokens
+  float* amax_v;           // [B, k + 1, gent] workspace: run or chunk maxima (greedy)
+  int* amax_i;             // [B, k + 1, gent] workspace: their tokens
   int* acc;                // [B] workspace: accepted drafts | plain << 8 | invalid << 9
   int* err;
 };

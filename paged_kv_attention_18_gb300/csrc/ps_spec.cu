@@ -46,32 +46,57 @@ __device__ __forceinline__ long long token_weight(float pv, float qe) {
   return fixed_weight(fmaxf(__fsub_rn(pv, qe), 0.f));
 }
 
-// Acceptance of sequence b's drafts under the rejection rule, by the calling warp (one
-// lane per draft, k <= 31): the number accepted; *plain when the final draw is from p
-// itself (every draft survived, or the stopping draft id lies outside the vocabulary,
-// then also *invalid).
-__device__ int accepted_warp(const SpecParams& a, int b, bool* plain, bool* invalid) {
+// Acceptance of a sequence's drafts under the rejection rule, decided by a warp (one
+// lane per draft, k <= 31).
+struct Accept {
+  int r;         // drafts accepted
+  bool plain;    // the final draw is from p itself: every draft survived, or the stopping
+  bool invalid;  //   draft id lies outside the vocabulary (then also `invalid`)
+  int draft;     // the stopping draft's token (the one-hot row's 1), -1 when plain
+};
+
+// One lane's part for sequence b: its draft's token and test. Branch-free, so the loads of
+// two sequences can be in flight together; an id outside the vocabulary reads token 0.
+struct AcceptLane {
+  int d;
+  bool ok, bad;
+};
+
+__device__ __forceinline__ AcceptLane accept_lane(const SpecParams& a, int b) {
   const int lane = threadIdx.x & 31;
-  bool ok = true, bad = false;
+  AcceptLane x = {-1, true, false};
   if (lane < a.k) {
-    const int d = a.drafts[b * a.k + lane];
-    if (d < 0 || d >= a.V) {
-      bad = true;
-      ok = false;
-    } else {
-      const float pv = a.p[(static_cast<int64_t>(b) * (a.k + 1) + lane) * a.V + d];
-      const float qv = a.q ? a.q[(static_cast<int64_t>(b) * a.k + lane) * a.V + d] : 1.f;
-      const double lhs = __dmul_rn(static_cast<double>(a.rnd[b * (a.k + 1) + lane]), qv);
-      const double rhs = __dmul_rn(static_cast<double>(pv), 4294967296.0);
-      ok = lhs < rhs;
-    }
+    x.d = a.drafts[b * a.k + lane];
+    x.bad = x.d < 0 || x.d >= a.V;
+    const int dc = x.bad ? 0 : x.d;
+    const float pv = a.p[(static_cast<int64_t>(b) * (a.k + 1) + lane) * a.V + dc];
+    const float qv = a.q ? a.q[(static_cast<int64_t>(b) * a.k + lane) * a.V + dc] : 1.f;
+    const double lhs = __dmul_rn(static_cast<double>(a.rnd[b * (a.k + 1) + lane]), qv);
+    const double rhs = __dmul_rn(static_cast<double>(pv), 4294967296.0);
+    x.ok = !x.bad && lhs < rhs;
   }
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < a.k && !ok);
-  const int r = rej ? __ffs(rej) - 1 : a.k;
-  const bool inv = __shfl_sync(0xffffffffu, bad ? 1 : 0, r & 31) != 0;
-  *invalid = rej != 0 && inv;
-  *plain = rej == 0 || *invalid;
-  return r;
+  return x;
+}
+
+__device__ __forceinline__ Accept accept_finish(const SpecParams& a, const AcceptLane& x) {
+  const int lane = threadIdx.x & 31;
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < a.k && !x.ok);
+  Accept y;
+  y.r = rej ? __ffs(rej) - 1 : a.k;
+  const bool inv = __shfl_sync(0xffffffffu, x.bad ? 1 : 0, y.r & 31) != 0;
+  const int d = __shfl_sync(0xffffffffu, x.d, y.r & 31);
+  y.invalid = rej != 0 && inv;
+  y.plain = rej == 0 || y.invalid;
+  y.draft = y.plain ? -1 : d;
+  return y;
+}
+
+__device__ __forceinline__ Accept accepted_warp(const SpecParams& a, int b) {
+  return accept_finish(a, accept_lane(a, b));
+}
+
+__device__ __forceinline__ int accept_word(const Accept& y) {
+  return y.r | (y.plain ? 1 << 8 : 0) | (y.invalid ? 1 << 9 : 0);
 }
 
 template <typename T>
@@ -155,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) spec_chunk_kernel(const SpecParams a
     }
     block_argmax(v, t, shv, shi);
     if (threadIdx.x == 0) {
-      const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.chunks + c;
+      const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.gent + c;
       a.amax_v[o] = v;
       a.amax_i[o] = t;
     }
@@ -193,6 +218,41 @@ __device__ __forceinline__ void weight_parts(float w, float& hi, float& lo) {
   hi = __fsub_rn(__fadd_rz(y, 8388608.0f), 8388608.0f);
   const float z = __fsub_rn(y, hi) * 1048576.0f;
   lo = __fsub_rn(__fadd_rz(z, 8388608.0f), 8388608.0f);
+}
+
+// weight_parts on two tokens at once (packed fp32 pairs, each lane rounded as the scalar
+// form), added into hs and ls: hs += hi, ls += lo per token.
+__device__ __forceinline__ void weight_parts2_add(float w0, float w1, float2& hs, float2& ls) {
+  asm("{\n\t.reg .b64 w, y, hb, hi, z, lb, lo, c20, c23, hs, ls;\n\t"
+      "mov.b64 w, {%4, %5};\n\t"
+      "mov.b64 c20, {%6, %6};\n\t"
+      "mov.b64 c23, {%7, %7};\n\t"
+      "mul.rn.f32x2 y, w, c20;\n\t"
+      "add.rz.f32x2 hb, y, c23;\n\t"
+      "sub.rn.f32x2 hi, hb, c23;\n\t"
+      "sub.rn.f32x2 z, y, hi;\n\t"
+      "mul.rn.f32x2 z, z, c20;\n\t"
+      "add.rz.f32x2 lb, z, c23;\n\t"
+      "sub.rn.f32x2 lo, lb, c23;\n\t"
+      "mov.b64 hs, {%0, %1};\n\t"
+      "mov.b64 ls, {%2, %3};\n\t"
+      "add.rn.f32x2 hs, hs, hi;\n\t"
+      "add.rn.f32x2 ls, ls, lo;\n\t"
+      "mov.b64 {%0, %1}, hs;\n\t"
+      "mov.b64 {%2, %3}, ls;\n\t}"
+      : "+f"(hs.x), "+f"(hs.y), "+f"(ls.x), "+f"(ls.y)
+      : "f"(w0), "f"(w1), "f"(1048576.0f), "f"(8388608.0f));
+}
+
+// p - q on two tokens at once.
+__device__ __forceinline__ float2 sub2(float2 p, float2 q) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(p.x), "f"(p.y), "f"(q.x), "f"(q.y));
+  return d;
 }
 
 // An integer-valued float in [0, 2^23) as an integer: its bits after adding 2^23.
@@ -239,14 +299,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_run_kernel(const Sp
       }
       if (u0 + t >= u_hi) continue;  // warp-uniform
       if (b != cur_b) {
-        bool plain, invalid;
-        const int r = accepted_warp(a, b, &plain, &invalid);
-        if (m == 0 && lane == 0)
-          a.acc[b] = r | (plain ? 1 << 8 : 0) | (invalid ? 1 << 9 : 0);
+        const Accept y = accepted_warp(a, b);
+        if (m == 0 && lane == 0) a.acc[b] = accept_word(y);
         cur_b = b;
-        row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + r) * a.V;
-        qrow = (kQ && !plain) ? a.q + (static_cast<int64_t>(b) * a.k + r) * a.V : nullptr;
-        draft = (!kQ && !plain) ? a.drafts[b * a.k + r] : -1;
+        row = a.p + (static_cast<int64_t>(b) * (a.k + 1) + y.r) * a.V;
+        qrow = (kQ && !y.plain) ? a.q + (static_cast<int64_t>(b) * a.k + y.r) * a.V : nullptr;
+        draft = kQ ? -1 : y.draft;
       }
       const int t0 = m * kRun;
       dl[t] = draft >= t0 && draft < t0 + kRun ? draft - t0 : -1;
@@ -351,6 +409,25 @@ struct Chunk {
   }
 };
 
+// Wait for the phase with the given parity, the thread suspended in between (it resumes
+// when the phase completes, or after at most 20 us per poll), so waiting warps leave the
+// issue slots to the others; gives up after `limit` polls (about 1.3 s) and returns false.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity,
+                                               uint32_t limit = (1u << 16)) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -360,20 +437,27 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// grid G (one wave of resident CTAs), the same share of runs per CTA as spec_run_kernel.
-// The producer warp decides each sequence's acceptance when it meets its first run, then
-// copies each chunk of a row (p, and q where the row has one) into the next free stage;
-// consumer warp w sums runs w, w + 8, ... of every stage and releases it.
-template <bool kQ>
+// What a stream kernel computes per run: the residual sum with draft rows q, the residual
+// sum with one-hot drafts (or none), or the argmax of every row (greedy rule).
+enum StreamMode { kResidualQ = 0, kResidualOneHot = 1, kArgmax = 2 };
+
+// grid G (one wave of resident CTAs), the same share of runs per CTA as spec_run_kernel
+// (greedy: the runs of all k + 1 rows of every sequence). The producer warp decides each
+// sequence's acceptance when it meets its first run (rejection rule), then copies each
+// chunk of a row (p, and q where the row has one) into the next free stage; consumer warp
+// w handles runs w, w + 8, ... of every stage and releases it.
+template <int kMode>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     spec_stream_kernel(const SpecParams a) {
+  constexpr bool kQ = kMode == kResidualQ, kGreedy = kMode == kArgmax;
   constexpr int kCap = kQ ? 16 : 32;  // runs per stage
   constexpr int kPer = kCap / kWarps;  // runs per consumer warp and stage
   extern __shared__ __align__(128) unsigned char smem_raw[];
   StreamSmem& sm = *reinterpret_cast<StreamSmem*>(smem_raw);
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t U = static_cast<int64_t>(a.B) * a.runs;
+  const int rows = kGreedy ? a.B * (a.k + 1) : a.B;
+  const int64_t U = static_cast<int64_t>(rows) * a.runs;
   const int64_t u_lo = U * blockIdx.x / gridDim.x;
   const int64_t u_hi = U * (blockIdx.x + 1) / gridDim.x;
   if (threadIdx.x == 0) {
@@ -384,7 +468,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     fence_barrier_init();
   }
   __syncthreads();
-  Chunk c0;
+  Chunk c0;  // c.b: the sequence (rejection rule) or the row b * (k + 1) + i (greedy)
   c0.u = u_lo;
   c0.b = static_cast<int>(u_lo / a.runs);
   c0.m = static_cast<int>(u_lo - static_cast<int64_t>(c0.b) * a.runs);
@@ -392,22 +476,40 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
   if (warp == kWarps) {
     // producer
     const uint64_t pol = l2_policy_evict_first();
-    int cur_b = -1, r = 0, draft = -1;
-    bool plain = true;
+    Accept cur = {0, true, false, -1}, nxt = cur;
+    int cur_b = -1, nxt_b = -1;
+    if (!kGreedy && c0.n > 0) {
+      // the share's first sequence, and the next one when the share reaches it: their
+      // loads in flight together
+      const bool two = static_cast<int64_t>(c0.b + 1) * a.runs < u_hi;
+      const AcceptLane x0 = accept_lane(a, c0.b);
+      const AcceptLane x1 = two ? accept_lane(a, c0.b + 1) : x0;
+      nxt = accept_finish(a, x0);
+      nxt_b = c0.b;
+      if (two) {
+        cur = nxt;
+        cur_b = c0.b;
+        if (c0.m == 0 && lane == 0) a.acc[c0.b] = accept_word(cur);
+        nxt = accept_finish(a, x1);
+        nxt_b = c0.b + 1;
+      }
+    }
+    int r = cur.r, draft = kQ ? -1 : cur.draft;
+    bool plain = cur.plain;
     int issued = 0;
     for (Chunk c = c0; c.n > 0; c.next(u_hi, a.runs, kCap)) {
-      if (c.b != cur_b) {
-        bool invalid;
-        r = accepted_warp(a, c.b, &plain, &invalid);
-        if (c.m == 0 && lane == 0)
-          a.acc[c.b] = r | (plain ? 1 << 8 : 0) | (invalid ? 1 << 9 : 0);
+      if (!kGreedy && c.b != cur_b) {
+        cur = c.b == nxt_b ? nxt : accepted_warp(a, c.b);
         cur_b = c.b;
-        draft = (!kQ && !plain) ? a.drafts[c.b * a.k + r] : -1;
+        if (c.m == 0 && lane == 0) a.acc[c.b] = accept_word(cur);
+        r = cur.r;
+        plain = cur.plain;
+        draft = kQ ? -1 : cur.draft;
       }
       const int s = issued % kStreamStages, use = issued / kStreamStages;
       bool ok = true;
       if (lane == 0) {
-        ok = use == 0 || mbar_wait(&sm.empty[s], (use - 1) & 1);
+        ok = use == 0 || mbar_wait_idle(&sm.empty[s], (use - 1) & 1);
         if (ok) {
           const int t0 = c.m * kRun;
           const int t1 = (c.m + c.n) * kRun < a.V ? (c.m + c.n) * kRun : a.V;
@@ -416,8 +518,8 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
           sm.has_q[s] = hq ? 1 : 0;
           sm.draft[s] = draft >= t0 && draft < t1 ? draft - t0 : -1;
           mbar_arrive_expect_tx(&sm.full[s], hq ? 2 * bytes : bytes);
-          bulk_load(sm.buf[s], a.p + (static_cast<int64_t>(c.b) * (a.k + 1) + r) * a.V + t0,
-                    bytes, &sm.full[s], pol);
+          const int64_t prow = kGreedy ? c.b : static_cast<int64_t>(c.b) * (a.k + 1) + r;
+          bulk_load(sm.buf[s], a.p + prow * a.V + t0, bytes, &sm.full[s], pol);
           if (hq)
             bulk_load(sm.buf[s] + kStageFloats / 2,
                       a.q + (static_cast<int64_t>(c.b) * a.k + r) * a.V + t0, bytes,
@@ -433,7 +535,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     if (lane == 0) {
       const int first = issued > kStreamStages ? issued - kStreamStages : 0;
       for (int i = first; i < issued; ++i)
-        mbar_wait(&sm.full[i % kStreamStages], (i / kStreamStages) & 1);
+        mbar_wait_idle(&sm.full[i % kStreamStages], (i / kStreamStages) & 1);
     }
     return;
   }
@@ -441,43 +543,92 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
   int idx = 0;
   for (Chunk c = c0; c.n > 0; c.next(u_hi, a.runs, kCap), ++idx) {
     const int s = idx % kStreamStages;
-    if (!mbar_wait(&sm.full[s], (idx / kStreamStages) & 1)) {
+    if (!mbar_wait_idle(&sm.full[s], (idx / kStreamStages) & 1)) {
       if (lane == 0) record_error(a.err, kDevWaitTimeout);
       break;
     }
-    const bool hq = kQ && sm.has_q[s] != 0;
-    const int dd = kQ ? -1 : sm.draft[s];
-    long long sums[kPer];
+    if (kGreedy) {
+      // (largest value, lowest token holding it) over the warp's runs of the stage: each
+      // lane meets its tokens in increasing order, so a strict comparison keeps the lowest
+      // of equal values; then one exchange over the warp, written as the entry of the
+      // warp's first run and (-inf, none) for its other runs
+      float4 f[kPer];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int run = warp + kWarps * j;
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f), g = f;
-      if (run < c.n && (c.m + run) * kRun + 4 * lane < a.V) {
-        f = *reinterpret_cast<const float4*>(&sm.buf[s][run * kRun + 4 * lane]);
-        if (hq) g = *reinterpret_cast<const float4*>(&sm.buf[s][kStageFloats / 2 + run * kRun + 4 * lane]);
+      for (int j = 0; j < kPer; ++j) {
+        const int run = warp + kWarps * j;
+        f[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (run < c.n && (c.m + run) * kRun + 4 * lane < a.V)
+          f[j] = *reinterpret_cast<const float4*>(&sm.buf[s][run * kRun + 4 * lane]);
       }
-      const float pv[4] = {f.x, f.y, f.z, f.w};
-      float qv[4] = {g.x, g.y, g.z, g.w};
-      if (dd >= 0 && (dd >> 7) == run && ((dd & (kRun - 1)) >> 2) == lane) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      float v = -INFINITY;
+      int t = INT32_MAX;
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
-          if (x == (dd & 3)) qv[x] = 1.f;
-      }
-      float hs = 0.f, ls = 0.f;
+      for (int j = 0; j < kPer; ++j) {
+        const int run = warp + kWarps * j;
+        const int base = (c.m + run) * kRun + 4 * lane;
+        if (run < c.n && base < a.V) {
+          const float x[4] = {f[j].x, f[j].y, f[j].z, f[j].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float hi, lo;
-        weight_parts(fmaxf(__fsub_rn(pv[e], qv[e]), 0.f), hi, lo);
-        hs += hi;
-        ls += lo;
+          for (int e = 0; e < 4; ++e) {
+            if (x[e] > v) {
+              v = x[e];
+              t = base + e;
+            }
+          }
+        }
       }
-      sums[j] = (static_cast<long long>(small_int(hs)) << 20) + small_int(ls);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
+        amax_merge(v, t, v2, t2);
+      }
+      if (lane < kPer && warp + kWarps * lane < c.n) {
+        a.amax_v[c.u + warp + kWarps * lane] = lane == 0 ? v : -INFINITY;
+        a.amax_i[c.u + warp + kWarps * lane] = lane == 0 ? t : INT32_MAX;
+      }
+    } else {
+      // each run's fixed-point residual sum
+      const bool hq = kQ && sm.has_q[s] != 0;
+      const int dd = kMode == kResidualOneHot ? sm.draft[s] : -1;
+      long long sums[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int run = warp + kWarps * j;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f), g = f;
+        if (run < c.n && (c.m + run) * kRun + 4 * lane < a.V) {
+          f = *reinterpret_cast<const float4*>(&sm.buf[s][run * kRun + 4 * lane]);
+          if (hq)
+            g = *reinterpret_cast<const float4*>(
+                &sm.buf[s][kStageFloats / 2 + run * kRun + 4 * lane]);
+        }
+        // residual weights max(p - q, 0): q from the stage, or 1 at a one-hot row's
+        // draft token and 0 elsewhere
+        float2 w01 = make_float2(f.x, f.y), w23 = make_float2(f.z, f.w);
+        if (kQ) {
+          w01 = sub2(w01, make_float2(g.x, g.y));
+          w23 = sub2(w23, make_float2(g.z, g.w));
+        } else if (dd >= 0 && (dd >> 7) == run && ((dd & (kRun - 1)) >> 2) == lane) {
+          const int e = dd & 3;
+          if (e == 0) w01.x = __fsub_rn(w01.x, 1.f);
+          if (e == 1) w01.y = __fsub_rn(w01.y, 1.f);
+          if (e == 2) w23.x = __fsub_rn(w23.x, 1.f);
+          if (e == 3) w23.y = __fsub_rn(w23.y, 1.f);
+        }
+        float2 hs = make_float2(0.f, 0.f), ls = hs;
+        weight_parts2_add(fmaxf(w01.x, 0.f), fmaxf(w01.y, 0.f), hs, ls);
+        weight_parts2_add(fmaxf(w23.x, 0.f), fmaxf(w23.y, 0.f), hs, ls);
+        sums[j] = (static_cast<long long>(small_int(hs.x + hs.y)) << 20) + small_int(ls.x + ls.y);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      const long long tot = warp_sum_n<kPer>(sums);
+      const int j = lane / (32 / kPer);
+      if (lane % (32 / kPer) == 0 && warp + kWarps * j < c.n)
+        a.wsum[c.u + warp + kWarps * j] = tot;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[s]);
-    const long long tot = warp_sum_n<kPer>(sums);
-    const int j = lane / (32 / kPer);
-    if (lane % (32 / kPer) == 0 && warp + kWarps * j < c.n) a.wsum[c.u + warp + kWarps * j] = tot;
   }
 }
 
@@ -595,8 +746,8 @@ __global__ void __launch_bounds__(kThreads) spec_final_kernel(const SpecParams a
     for (int i = 0; i <= a.k; ++i) {
       float v = -INFINITY;
       int t = INT32_MAX;
-      for (int c = threadIdx.x; c < a.chunks; c += kThreads) {
-        const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.chunks + c;
+      for (int c = threadIdx.x; c < a.gent; c += kThreads) {
+        const int64_t o = (static_cast<int64_t>(b) * (a.k + 1) + i) * a.gent + c;
         amax_merge(v, t, a.amax_v[o], a.amax_i[o]);
       }
       block_argmax(v, t, shv, shi);
@@ -676,6 +827,23 @@ int spec_chunks(int V) {
 
 int spec_runs(int V) { return (V + kRun - 1) / kRun; }
 
+template <int kMode>
+static cudaError_t launch_stream(const SpecParams& a, cudaStream_t stream) {
+  // one wave of resident CTAs, each at least one stage of runs
+  const int cap_runs = kMode == kResidualQ ? 16 : 32;
+  const int rows = kMode == kArgmax ? a.B * (a.k + 1) : a.B;
+  const int64_t units = static_cast<int64_t>(rows) * a.runs;
+  const int64_t by_work = (units + cap_runs - 1) / cap_runs;
+  const int64_t cap = kStreamCtasPerSm * static_cast<int64_t>(a.num_sms > 0 ? a.num_sms : 1);
+  const int grid = static_cast<int>(by_work < cap ? by_work : cap);
+  constexpr int smem = sizeof(StreamSmem);
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t e = ensure_smem_limit(spec_stream_kernel<kMode>, smem, done);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(spec_stream_kernel<kMode>, dim3(grid), dim3(kStreamThreads), smem, stream,
+                       false, a);
+}
+
 cudaError_t launch_spec_accept(const SpecParams& a0, cudaStream_t stream) {
   if (a0.B == 0) return cudaSuccess;
   SpecParams a = a0;
@@ -685,30 +853,15 @@ cudaError_t launch_spec_accept(const SpecParams& a0, cudaStream_t stream) {
   a.runs = spec_runs(a.V);
   a.vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
           (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+  // greedy: one (max, token) entry per run with 16-byte rows, per chunk otherwise
+  a.gent = a.vec ? a.runs : a.chunks;
   cudaError_t e;
   if (a.greedy) {
-    e = launch_kernel(spec_chunk_kernel, dim3(a.chunks, a.B), dim3(kThreads), 0, stream, false, a);
+    e = a.vec ? launch_stream<kArgmax>(a, stream)
+              : launch_kernel(spec_chunk_kernel, dim3(a.chunks, a.B), dim3(kThreads), 0, stream,
+                              false, a);
   } else if (a.vec) {
-    // one wave of resident CTAs, each at least one stage of runs
-    const int cap_runs = a.q ? 16 : 32;
-    const int64_t units = static_cast<int64_t>(a.B) * a.runs;
-    const int64_t by_work = (units + cap_runs - 1) / cap_runs;
-    const int64_t cap = kStreamCtasPerSm * static_cast<int64_t>(a.num_sms > 0 ? a.num_sms : 1);
-    const int grid = static_cast<int>(by_work < cap ? by_work : cap);
-    constexpr int smem = sizeof(StreamSmem);
-    if (a.q) {
-      static std::atomic<uint64_t> done{0};
-      e = ensure_smem_limit(spec_stream_kernel<true>, smem, done);
-      if (e == cudaSuccess)
-        e = launch_kernel(spec_stream_kernel<true>, dim3(grid), dim3(kStreamThreads), smem,
-                          stream, false, a);
-    } else {
-      static std::atomic<uint64_t> done{0};
-      e = ensure_smem_limit(spec_stream_kernel<false>, smem, done);
-      if (e == cudaSuccess)
-        e = launch_kernel(spec_stream_kernel<false>, dim3(grid), dim3(kStreamThreads), smem,
-                          stream, false, a);
-    }
+    e = a.q ? launch_stream<kResidualQ>(a, stream) : launch_stream<kResidualOneHot>(a, stream);
   } else {
     // rows as 4-byte words: one wave of resident CTAs, each at least one load group per warp
     const int n = a.q ? 4 : 8;

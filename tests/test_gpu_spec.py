@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import spec_oracle
 from paged_kv_attention_18_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -74,6 +75,75 @@ def test_full_vocabulary_batch():
     got = run(p, drafts, rnd, q)
     ref = oracle.spec_accept(p, drafts, rnd, q)
     assert binding.device_error() == 0
+    np.testing.assert_array_equal(got[1], ref[1])
+    np.testing.assert_array_equal(got[0], ref[0])
+    # greedy over the same rows, a third of the drafts on the target's argmax
+    am = p.argmax(axis=-1)[:, :k]
+    gd = np.where(np.arange(B)[:, None] % 3 == 0, am, drafts).astype(np.int32)
+    got = run(p, gd, None, greedy=True)
+    ref = oracle.spec_accept(p, gd, greedy=True)
+    assert binding.device_error() == 0
+    np.testing.assert_array_equal(got[1], ref[1])
+    np.testing.assert_array_equal(got[0], ref[0])
+
+
+@pytest.mark.parametrize("V", [4096, 3001])
+@pytest.mark.parametrize("mode", ["draft_model", "ngram", "bonus"])
+def test_draw_on_exact_boundaries(V, mode):
+    """The fixed-point sums are exact. Residual mass below 2^-8 gives Z < 2^32, so the final
+    word can put the target on any integer. Targets at C_v - 1 and at C_v (C the oracle's
+    running sums) must pick token v and the next weighted token. An error of one unit in
+    any weight before v would change the token. V = 4096 takes 16-byte rows, V = 3001
+    4-byte ones."""
+    B, k = 16, 2
+    rng = np.random.default_rng(V + 7 * len(mode))
+    p = _softmax(rng.standard_normal((B, k + 1, V)).astype(np.float32))
+    drafts = rng.integers(0, V, (B, k)).astype(np.int32)
+    rnd = np.zeros((B, k + 1), np.uint64)
+    q = None
+    if mode == "draft_model":
+        # q a hair below p: residual mass about 2^-11; draft 0 rejected (q above p there)
+        q = (p[:, :k] * np.float32(1 - 2.0 ** -11)).astype(np.float32)
+        for b in range(B):
+            q[b, 0, drafts[b, 0]] = p[b, 0, drafts[b, 0]] * np.float32(1.5)
+        rnd[:, 0] = U32 - 1
+        rows = [np.maximum(p[b, 0] - q[b, 0], np.float32(0)) for b in range(B)]
+    elif mode == "ngram":
+        # one-hot drafts on rows of mass 2^-10: draft 0 rejected, residual = p but 0 at it
+        p = (p * np.float32(2.0 ** -10)).astype(np.float32)
+        rnd[:, 0] = U32 - 1
+        rows = []
+        for b in range(B):
+            w = p[b, 0].copy()
+            w[drafts[b, 0]] = max(w[drafts[b, 0]] - np.float32(1), np.float32(0))
+            rows.append(w)
+    else:
+        # every draft accepted (R = 0): the bonus draw from p_k, mass 2^-10
+        p = (p * np.float32(2.0 ** -10)).astype(np.float32)
+        rows = [p[b, k] for b in range(B)]
+    expect = np.zeros(B, np.int64)
+    for b in range(B):
+        W = spec_oracle.weights(rows[b])
+        C = np.cumsum(W)
+        Z = int(C[-1])
+        assert 0 < Z < 2 ** 32
+        v = V // 3 + 37 * b
+        while W[v] == 0:
+            v += 1
+        T = int(C[v]) - (1 if b % 2 == 0 else 0)
+        R = (T * 2 ** 32 + Z - 1) // Z
+        assert R < 2 ** 32 and (R * Z) >> 32 == T
+        rnd[b, k] = R
+        nxt = v + 1
+        while W[nxt] == 0:
+            nxt += 1
+        expect[b] = v if b % 2 == 0 else nxt
+    rnd = rnd.astype(np.uint32)
+    got = run(p, drafts, rnd, q)
+    ref = oracle.spec_accept(p, drafts, rnd, q)
+    assert binding.device_error() == 0
+    last = ref[0][np.arange(B), ref[1]]
+    np.testing.assert_array_equal(last, expect)  # the case is set up as described
     np.testing.assert_array_equal(got[1], ref[1])
     np.testing.assert_array_equal(got[0], ref[0])
 
