@@ -48,58 +48,81 @@ constexpr double kInvTwoPi = 0.1591549430918953357688837633725143620344596457404
 constexpr double kTwoTo64 = 18446744073709551616.0;
 constexpr float kTurnToRad = 1.46291807926715968e-09f;  // 2 pi / 2^32
 constexpr int kTokensPerPass = 8;
+constexpr int kRopeCtasPerSm = 3;
+constexpr int kUnits = 4;  // q/k units per thread per round
 
-// Each pass of a CTA takes 8 tokens. A thread first issues the loads of its units (a unit
-// is one (token, head) pair of 16-byte chunks i..i+7 and i+D/2..i+D/2+7 of q or k), then
-// computes the tokens' cosines and sines into shared memory while those loads are in
-// flight, and after the barrier rotates and stores; the V rows are copied last.
+// One CTA takes a contiguous range of passes of 8 tokens. A pass's q and k rows are
+// 8 * (H_q + H_kv) rows of D elements; thread t takes chunk pair t % (D/16) (16-byte chunks
+// i..i+7 and i+D/2..i+D/2+7) of rows t / (D/16), + 256 / (D/16), ... A round first issues
+// every load of its units and of the V rows, then computes the pass's cosines and sines
+// into one of two shared tables while the loads are in flight; after one barrier it
+// rotates and stores. The two tables let the next pass start without a second barrier.
 template <bool kBF16, int D>
-__global__ void __launch_bounds__(kRopeThreads)
+__global__ void __launch_bounds__(kRopeThreads, kRopeCtasPerSm)
     rope_reshape_and_cache_kernel(uint4* __restrict__ q, const uint4* __restrict__ k,
                                   const uint4* __restrict__ v, const int32_t* __restrict__ pos,
                                   const int32_t* __restrict__ slots, uint4* __restrict__ k_pool,
                                   uint4* __restrict__ v_pool, int T, int H_q, int H_kv,
                                   int64_t num_slots, double log2_theta, int* err) {
   constexpr int kHalf = D / 2, kChunks = kHalf / 8;  // 16-byte chunks per half row
-  constexpr int kUnits = 4;                          // q/k units per thread per round
+  constexpr int kRowsPerRound = kRopeThreads / kChunks;
   __shared__ unsigned long long turns[kHalf];  // f_i / (2 pi) in units of 2^-64 turn
-  __shared__ float cs[kTokensPerPass][kHalf], sn[kTokensPerPass][kHalf];
+  __shared__ float cs[2][kTokensPerPass][kHalf], sn[2][kTokensPerPass][kHalf];
   for (int i = threadIdx.x; i < kHalf; i += blockDim.x)
     turns[i] = __double2ull_rn(exp2(-(2.0 * i / D) * log2_theta) * kInvTwoPi * kTwoTo64);
+  const int heads = H_q + H_kv;
+  const int rows = kTokensPerPass * heads;  // q and k rows of a pass
+  const int vecs = H_kv * D / 8;            // 16-byte words of a token's V row
+  const int ch = threadIdx.x % kChunks, row0 = threadIdx.x / kChunks;
+  const int passes = (T + kTokensPerPass - 1) / kTokensPerPass;
+  const int p_lo = static_cast<int>(static_cast<int64_t>(passes) * blockIdx.x / gridDim.x);
+  const int p_hi = static_cast<int>(static_cast<int64_t>(passes) * (blockIdx.x + 1) / gridDim.x);
   __syncthreads();
-  const int units_tok = (H_q + H_kv) * kChunks;
-  const int units = kTokensPerPass * units_tok;
-  const int vecs = H_kv * D / 8;
-  for (int t0 = blockIdx.x * kTokensPerPass; t0 < T; t0 += gridDim.x * kTokensPerPass) {
-    for (int r0 = 0; r0 < units; r0 += kUnits * kRopeThreads) {
-      // 1. loads of this round's units
+  int buf = 0;
+  for (int pass = p_lo; pass < p_hi; ++pass, buf ^= 1) {
+    const int t0 = pass * kTokensPerPass;
+    for (int r0 = 0; r0 < rows; r0 += kUnits * kRowsPerRound) {
+      // 1. loads of this round's units, and (first round) of the pass's V rows
       uint4 lo[kUnits], hi[kUnits];
-      int tok[kUnits], head[kUnits], ch[kUnits], slot[kUnits];
+      int slot[kUnits];
 #pragma unroll
       for (int j = 0; j < kUnits; ++j) {
-        const int x = r0 + j * kRopeThreads + threadIdx.x;
-        const int u = x / units_tok, w = x - u * units_tok;
-        tok[j] = (x < units && t0 + u < T) ? t0 + u : -1;
-        head[j] = w / kChunks;
-        ch[j] = w - head[j] * kChunks;
-        slot[j] = -1;
-        if (tok[j] < 0) continue;
-        const uint4* row;
-        if (head[j] < H_q) {
-          row = q + (static_cast<int64_t>(tok[j]) * H_q + head[j]) * (D / 8);
+        const int row = r0 + row0 + j * kRowsPerRound;
+        const int u = row / heads, head = row - u * heads, t = t0 + u;
+        slot[j] = -2;  // -2: no unit; -1: a k row with nothing to cache
+        if (row >= rows || t >= T) continue;
+        const uint4* src;
+        if (head < H_q) {
+          slot[j] = -3;  // a q row
+          src = q + (static_cast<int64_t>(t) * H_q + head) * (D / 8);
         } else {
-          slot[j] = slots[tok[j]];
-          row = k + (static_cast<int64_t>(tok[j]) * H_kv + head[j] - H_q) * (D / 8);
-          if (slot[j] < 0 || slot[j] >= num_slots) {
-            tok[j] = -1;  // nothing to cache for this token
+          const int sl = slots[t];
+          slot[j] = sl >= 0 && sl < num_slots ? sl : -1;
+          src = k + (static_cast<int64_t>(t) * H_kv + head - H_q) * (D / 8);
+          if (slot[j] < 0) continue;
+        }
+        lo[j] = src[ch];
+        hi[j] = src[ch + kChunks];
+      }
+      constexpr int kV = 1;  // V words per thread per pass held in registers
+      uint4 vv[kV];
+      int vslot[kV];
+      if (r0 == 0) {
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+          const int x = threadIdx.x + j * kRopeThreads;
+          const int u = x / vecs, w = x - u * vecs, t = t0 + u;
+          vslot[j] = -1;
+          if (u >= kTokensPerPass || t >= T) continue;
+          const int vs = slots[t];
+          if (vs >= num_slots) {
+            if (w == 0) record_error(err, kDevBadSlot);
             continue;
           }
+          vslot[j] = vs;
+          if (vs >= 0) vv[j] = v[static_cast<int64_t>(t) * vecs + w];
         }
-        lo[j] = row[ch[j]];
-        hi[j] = row[ch[j] + kChunks];
-      }
-      // 2. the tokens' cosines and sines (first round of the pass)
-      if (r0 == 0) {
+        // 2. the pass's cosines and sines
         for (int x = threadIdx.x; x < kTokensPerPass * kHalf; x += blockDim.x) {
           const int u = x / kHalf, i = x - u * kHalf;
           const int t = t0 + u;
@@ -109,39 +132,47 @@ __global__ void __launch_bounds__(kRopeThreads)
           const float r = static_cast<float>(static_cast<int32_t>(ph >> 32)) * kTurnToRad;
           float sf, cf;
           sincosf(r, &sf, &cf);
-          cs[u][i] = cf;
-          sn[u][i] = sf;
+          cs[buf][u][i] = cf;
+          sn[buf][u][i] = sf;
         }
         __syncthreads();
       }
       // 3. rotate and store
 #pragma unroll
       for (int j = 0; j < kUnits; ++j) {
-        if (tok[j] < 0) continue;
-        const int u = tok[j] - t0, i0 = ch[j] * 8;
-        rotate8<kBF16>(lo[j], hi[j], cs[u] + i0, sn[u] + i0);
-        uint4* dst;
-        if (head[j] < H_q)
-          dst = q + (static_cast<int64_t>(tok[j]) * H_q + head[j]) * (D / 8);
-        else
-          dst = k_pool + (static_cast<int64_t>(slot[j]) * H_kv + head[j] - H_q) * (D / 8);
-        dst[ch[j]] = lo[j];
-        dst[ch[j] + kChunks] = hi[j];
+        if (slot[j] < -2 || slot[j] >= 0) {
+          const int row = r0 + row0 + j * kRowsPerRound;
+          const int u = row / heads, head = row - u * heads, t = t0 + u;
+          const int i0 = ch * 8;
+          rotate8<kBF16>(lo[j], hi[j], cs[buf][u] + i0, sn[buf][u] + i0);
+          uint4* dst = head < H_q
+                           ? q + (static_cast<int64_t>(t) * H_q + head) * (D / 8)
+                           : k_pool + (static_cast<int64_t>(slot[j]) * H_kv + head - H_q) * (D / 8);
+          dst[ch] = lo[j];
+          dst[ch + kChunks] = hi[j];
+        }
+      }
+      if (r0 == 0) {
+        // the V rows as they are
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+          const int x = threadIdx.x + j * kRopeThreads;
+          if (vslot[j] >= 0) v_pool[static_cast<int64_t>(vslot[j]) * vecs + x % vecs] = vv[j];
+        }
+        // V words beyond what the registers held (more than 256 in a pass)
+        for (int x = threadIdx.x + kV * kRopeThreads; x < kTokensPerPass * vecs;
+             x += kRopeThreads) {
+          const int u = x / vecs, w = x - u * vecs, t = t0 + u;
+          if (t >= T) continue;
+          const int vs = slots[t];
+          if (vs >= num_slots) {
+            if (w == 0) record_error(err, kDevBadSlot);
+            continue;
+          }
+          if (vs >= 0) v_pool[static_cast<int64_t>(vs) * vecs + w] = v[static_cast<int64_t>(t) * vecs + w];
+        }
       }
     }
-    // the V rows as they are
-    for (int x = threadIdx.x; x < kTokensPerPass * vecs; x += blockDim.x) {
-      const int u = x / vecs, w = x - u * vecs;
-      const int t = t0 + u;
-      if (t >= T) continue;
-      const int vs = slots[t];
-      if (vs >= num_slots) {
-        if (w == 0) record_error(err, kDevBadSlot);
-        continue;
-      }
-      if (vs >= 0) v_pool[static_cast<int64_t>(vs) * vecs + w] = v[static_cast<int64_t>(t) * vecs + w];
-    }
-    __syncthreads();  // the pass's cosines are read before the next pass writes them
   }
 }
 
@@ -150,8 +181,9 @@ cudaError_t launch_rope_t(void* q, const void* k, const void* v, const int32_t* 
                           const int32_t* slots, void* k_pool, void* v_pool, int T, int H_q,
                           int H_kv, int num_blocks, float theta, int* err, int num_sms,
                           cudaStream_t stream) {
+  // one wave of resident CTAs, each a contiguous range of passes
   const int passes = (T + kTokensPerPass - 1) / kTokensPerPass;
-  const int grid = passes < num_sms * 8 ? passes : num_sms * 8;
+  const int grid = passes < num_sms * kRopeCtasPerSm ? passes : num_sms * kRopeCtasPerSm;
   rope_reshape_and_cache_kernel<kBF16, D><<<grid, kRopeThreads, 0, stream>>>(
       static_cast<uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v), pos,
       slots, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), T, H_q, H_kv,
