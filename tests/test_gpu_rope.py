@@ -34,9 +34,11 @@ def within_bound(got_bits, exact, x_bits, dtype):
     return np.abs(got - exact) <= ulp(exact, dtype) + 2.0 ** -20 * mag
 
 
+# the last case has 136 heads per token: nine rounds of 128 rows in each 8-token pass
 @pytest.mark.parametrize("dtype,H_q,H_kv,D,theta", [("bf16", 12, 2, 128, 1e6),
                                                     ("f16", 14, 2, 64, 1e6),
-                                                    ("bf16", 8, 8, 128, 1e4)])
+                                                    ("bf16", 8, 8, 128, 1e4),
+                                                    ("f16", 128, 8, 128, 1e6)])
 def test_rope_scatter_matches_oracle(dtype, H_q, H_kv, D, theta):
     rng = np.random.default_rng(110 + D + H_q)
     T, nb = 700, 96
