@@ -1006,12 +1006,20 @@ def run_spec_accept(args, rank, world, local_rank) -> dict | None:
         "greedy": (cycled(lambda p, q, d, r: binding.spec_accept(p, d, None, None, greedy=True,
                                                                   workspace=ws)), k + 1),
     }
+    # rows each call reads: with draft rows q, the stopping row of p and of q, or p alone
+    # for a sequence whose every draft survived (the bonus draw); averaged over the sets
+    q_rows = []
+    for p, q, drafts, rnd in sets:
+        _, num = binding.spec_accept(p, drafts, rnd, q, workspace=ws)
+        q_rows.append(float((num < k).float().mean().item()))
+    runs["draft_model"] = (runs["draft_model"][0], 1 + sum(q_rows) / len(q_rows))
     res = {}
     for name, (fn, rows) in runs.items():
         ms = reduce_max(time_events(fn, args.steps, args.warmup, per_graph=10), world)
         nbytes = B * rows * V * 4  # probability rows the rule needs per call
         res[name] = {"ms": ms, "gbs": world * nbytes / (ms / 1e3) / 1e9,
-                     "seq_per_s": world * B / (ms / 1e3), "rows_read_per_sequence": rows}
+                     "seq_per_s": world * B / (ms / 1e3),
+                     "rows_read_per_sequence": round(rows, 4)}
     p, q, drafts, rnd = sets[0]
     _, num = binding.spec_accept(p, drafts, rnd, q, workspace=ws)
     torch.cuda.synchronize()
