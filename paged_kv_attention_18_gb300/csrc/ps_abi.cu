@@ -674,7 +674,8 @@ const void* device_view(const void* h) {
 // The host step. dev[i] is the device's view of host buffer i (q, k, v, block tables,
 // lengths, offsets, out) or null: inputs with a view are gathered by one kernel that reads
 // them across the host link, the others copied one by one; an output with a view is
-// written by a kernel, otherwise copied.
+// written by the step's kernels themselves (up to 4 MB) or by a kernel after them,
+// otherwise copied.
 int host_step(const void* q, const void* k, const void* v, const int32_t* block_tables,
               const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
               void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
@@ -744,16 +745,22 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
     if ((rc = ps::current_device(&num_sms, &err))) return rc;
     if (ps::launch_gather_in(segs, num_sms, s, false) != cudaSuccess) return PS_ERR_CUDA;
   }
+  // A small output (up to kDirectOutBytes) goes straight from the step's kernels into the
+  // page-locked host buffer, so it crosses the host link while the last kernels run. A
+  // larger one is written to the staging buffer and then moved by a kernel that follows the
+  // step's last kernel (or copied): written directly, its stores would hold the attention
+  // kernels back at the link's rate.
+  constexpr size_t kDirectOutBytes = size_t(4) << 20;
+  const size_t out_bytes = static_cast<size_t>(T) * H_q * D * 2;
+  const bool direct_out = dev[6] && aligned16(dev[6]) && out_bytes <= kDirectOutBytes;
   rc = ps_attention_step(st + l.q, st + l.k, st + l.v, k_pool, v_pool,
                          reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
                          reinterpret_cast<const int32_t*>(st + l.sl),
                          reinterpret_cast<const int32_t*>(st + l.qsl), B, T, H_q, H_kv, D,
-                         num_blocks, scale, st + l.out, reinterpret_cast<int32_t*>(st + l.slots),
-                         st + l.ws, ws_bytes, dtype, stream);
-  if (rc) return rc;
-  // the output: written straight into the page-locked host buffer by a kernel that follows
-  // the step's last kernel, or copied
-  const size_t out_bytes = static_cast<size_t>(T) * H_q * D * 2;
+                         num_blocks, scale, direct_out ? const_cast<void*>(dev[6]) : st + l.out,
+                         reinterpret_cast<int32_t*>(st + l.slots), st + l.ws, ws_bytes, dtype,
+                         stream);
+  if (rc || direct_out) return rc;
   if (dev[6] && out_bytes % 4 == 0) {
     ps::CopySegments o{};
     o.seg[0] = ps::CopySegment{const_cast<void*>(dev[6]), st + l.out,

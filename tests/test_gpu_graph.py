@@ -158,6 +158,28 @@ def test_host_step_graph_empty_batch():
     assert np.array_equal(host_bits(pools.k), wl.k_pool)
 
 
+def test_host_step_large_output_matches_device_step():
+    # a 25 MB output (the chunked-prefill step) is written to the staging buffer and then
+    # moved to the page-locked host buffer by a kernel after the step (small outputs are
+    # written there by the step's own kernels): bit-identical to the device entry point's
+    # output on the same inputs, in a fresh pool each
+    wl = W.named("prefix_chunked_prefill")
+    st = wl.steps[0]
+    assert st.T * wl.H_q * wl.D * 2 > 4 << 20
+    dt = wl.dtype
+    pools_d = DevicePools(wl)
+    q, k, v = dev(st.q, dt), dev(st.k, dt), dev(st.v, dt)
+    bt, sl, qs = dev(st.block_tables), dev(st.seq_lens), dev(st.query_start_loc)
+    ref = binding.attention_step(q, k, v, pools_d.k, pools_d.v, bt, sl, qs, wl.scale)
+    pools_h = DevicePools(wl)
+    args = _host_step_tensors(wl, st, pinned=True)
+    binding.attention_step_host(*args[:7], pools_h.k, pools_h.v, wl.scale, args[7])
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert torch.equal(args[6].view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(pools_h.k, pools_d.k) and torch.equal(pools_h.v, pools_d.v)
+
+
 def test_host_step_graph_rejects_pageable_buffers():
     # the graph copies from and to page-locked host memory only: pageable buffers are
     # rejected before anything is recorded, and a graph over pinned buffers still works
