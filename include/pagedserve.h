@@ -297,7 +297,8 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
  *                  the attention workspace are placed in it).
  * Host memory must stay valid and unmodified until the stream completes. Page-locked host
  * arrays that the device can address (pinned and mapped, 4-byte aligned) are read by one
- * kernel that gathers all such inputs across the host link. Such an `out` (16-byte aligned)
+ * kernel that gathers all such inputs across the host link; such k and v (16-byte aligned)
+ * are instead read by the step's KV scatter directly. Such an `out` (16-byte aligned)
  * is written by the step's kernels themselves when it is at most 4 MB, and otherwise by a
  * kernel after the step's last one; any other array is copied with one cudaMemcpyAsync.
  */

@@ -672,10 +672,10 @@ const void* device_view(const void* h) {
 }
 
 // The host step. dev[i] is the device's view of host buffer i (q, k, v, block tables,
-// lengths, offsets, out) or null: inputs with a view are gathered by one kernel that reads
-// them across the host link, the others copied one by one; an output with a view is
-// written by the step's kernels themselves (up to 4 MB) or by a kernel after them,
-// otherwise copied.
+// lengths, offsets, out) or null: the new K and V rows with a view are read by the step's
+// scatter itself, other inputs with a view are gathered by one kernel that reads them
+// across the host link, the rest copied one by one; an output with a view is written by
+// the step's kernels themselves (up to 4 MB) or by a kernel after them, otherwise copied.
 int host_step(const void* q, const void* k, const void* v, const int32_t* block_tables,
               const int32_t* seq_lens, const int32_t* query_start_loc, void* out, void* k_pool,
               void* v_pool, int max_blocks_per_seq, int B, int T, int H_q, int H_kv, int D,
@@ -730,10 +730,13 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
       {st + l.sl, seq_lens, static_cast<size_t>(B) * 4},
       {st + l.qsl, query_start_loc, static_cast<size_t>(B + 1) * 4},
   };
+  // The new tokens' K and V rows are read once, by the step's KV scatter: with a 16-byte
+  // aligned device view, the scatter reads them across the host link itself.
+  const bool kv_direct = dev[1] && dev[2] && aligned16(dev[1]) && aligned16(dev[2]);
   ps::CopySegments segs{};
   for (int i = 0; i < 6; ++i) {
     const Copy& c = in[i];
-    if (c.bytes == 0) continue;
+    if (c.bytes == 0 || (kv_direct && (i == 1 || i == 2))) continue;
     if (dev[i] && c.bytes % 4 == 0) {
       segs.seg[segs.n++] = ps::CopySegment{c.dst, dev[i], static_cast<int64_t>(c.bytes)};
     } else if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
@@ -753,7 +756,8 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
   constexpr size_t kDirectOutBytes = size_t(4) << 20;
   const size_t out_bytes = static_cast<size_t>(T) * H_q * D * 2;
   const bool direct_out = dev[6] && aligned16(dev[6]) && out_bytes <= kDirectOutBytes;
-  rc = ps_attention_step(st + l.q, st + l.k, st + l.v, k_pool, v_pool,
+  rc = ps_attention_step(st + l.q, kv_direct ? dev[1] : st + l.k, kv_direct ? dev[2] : st + l.v,
+                         k_pool, v_pool,
                          reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
                          reinterpret_cast<const int32_t*>(st + l.sl),
                          reinterpret_cast<const int32_t*>(st + l.qsl), B, T, H_q, H_kv, D,
