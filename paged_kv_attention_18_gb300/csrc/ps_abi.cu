@@ -267,7 +267,12 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   if ((rc = make_pool_map(&vmap, v_pool, p.num_blocks, p.H_kv, p.D, bf16))) return rc;
   if (tiles && (rc = make_q_map(&qmap, p.q, p.T, p.H_q, p.D, p.G, p.tpt, bf16))) return rc;
   cudaError_t e;
-  if (direct_fits(p, num_sms)) {
+  const CopySegments* pre = scatter != nullptr ? scatter->pre : nullptr;
+  const bool direct = direct_fits(p, num_sms), direct_tile = tiles && direct_tile_fits(p, num_sms);
+  if (pre != nullptr && pre->n > 0 && (direct || direct_tile) &&
+      (e = launch_gather_in(*pre, num_sms, s, false)) != cudaSuccess)
+    return cuda_fail(e, "input gather kernel");
+  if (direct) {
     // a small batch: the whole step (scatter included) in one launch, without a plan
     p.direct = 1;
     if (scatter) {
@@ -284,7 +289,7 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
   // A few sequences with query tiles and short contexts: the tile kernel alone, right after
   // the step's scatter, each CTA deriving its items (every sequence unsplit) from seq_lens
   // and qsl. No plan, nothing to combine.
-  if (tiles && direct_tile_fits(p, num_sms)) {
+  if (direct_tile) {
     if (scatter) {
       Timed tm(1, s);
       if ((e = launch_step_scatter(scatter->k, scatter->v, p.block_tables, p.max_blocks,
@@ -316,7 +321,7 @@ int run_attention(const AttnParams& p0, void* k_pool, void* v_pool, bool bf16, c
       pp.v_pool = v_pool;
     }
     Timed tm(2, s);
-    if ((e = launch_plan(pp, concurrency, num_sms, num_sms, s)) != cudaSuccess)
+    if ((e = launch_plan(pp, concurrency, num_sms, num_sms, s, pre)) != cudaSuccess)
       return cuda_fail(e, "plan kernel");
   }
   // One stream, every launch chained with programmatic dependent launch. With both
@@ -582,11 +587,34 @@ int ps_paged_attention(const void* q, const void* k_pool, const void* v_pool,
                            dtype == PS_BF16, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// The step, with copies still to make before the attention kernels read their
+// destinations (`pre`, the host step's queries) or none.
+int attention_step_impl(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* seq_lens, const int32_t* query_start_loc, int B, int T,
+                        int H_q, int H_kv, int D, int num_blocks, float scale, void* out,
+                        int32_t* slot_mapping, void* workspace, size_t workspace_bytes, int dtype,
+                        void* stream, const ps::CopySegments* pre);
+}  // namespace
+
 int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
                       const int32_t* query_start_loc, int B, int T, int H_q, int H_kv, int D,
                       int num_blocks, float scale, void* out, int32_t* slot_mapping,
                       void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  return attention_step_impl(q, k, v, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
+                             query_start_loc, B, T, H_q, H_kv, D, num_blocks, scale, out,
+                             slot_mapping, workspace, workspace_bytes, dtype, stream, nullptr);
+}
+
+namespace {
+int attention_step_impl(const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* seq_lens, const int32_t* query_start_loc, int B, int T,
+                        int H_q, int H_kv, int D, int num_blocks, float scale, void* out,
+                        int32_t* slot_mapping, void* workspace, size_t workspace_bytes, int dtype,
+                        void* stream, const ps::CopySegments* pre) {
   // validate everything before enqueuing anything
   int rc = check_attention(q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
                            query_start_loc, B, T, H_q, H_kv, D, num_blocks, out, workspace,
@@ -614,10 +642,11 @@ int ps_attention_step(const void* q, const void* k, const void* v, void* k_pool,
   p.slots = slot_mapping;
   if (!ps::layout_workspace(p, static_cast<uint8_t*>(workspace), workspace_bytes, false))
     return PS_ERR_WORKSPACE;
-  const ps::ScatterArgs sc{k, v};
+  const ps::ScatterArgs sc{k, v, pre};
   return ps::run_attention(p, k_pool, v_pool, dtype == PS_BF16, static_cast<cudaStream_t>(stream),
                            &sc);
 }
+}  // namespace
 
 namespace {
 struct StagingLayout {
@@ -733,12 +762,16 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
   // The new tokens' K and V rows are read once, by the step's KV scatter: with a 16-byte
   // aligned device view, the scatter reads them across the host link itself.
   const bool kv_direct = dev[1] && dev[2] && aligned16(dev[1]) && aligned16(dev[2]);
-  ps::CopySegments segs{};
+  // The queries are read only by the attention kernels: their copy goes to the step, which
+  // makes it on extra CTAs of the planner's launch (beside the planning), or first when the
+  // step has no planner. The other inputs are gathered before the step.
+  ps::CopySegments segs{}, pre{};
   for (int i = 0; i < 6; ++i) {
     const Copy& c = in[i];
     if (c.bytes == 0 || (kv_direct && (i == 1 || i == 2))) continue;
     if (dev[i] && c.bytes % 4 == 0) {
-      segs.seg[segs.n++] = ps::CopySegment{c.dst, dev[i], static_cast<int64_t>(c.bytes)};
+      ps::CopySegments& to = i == 0 ? pre : segs;
+      to.seg[to.n++] = ps::CopySegment{c.dst, dev[i], static_cast<int64_t>(c.bytes)};
     } else if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
       return PS_ERR_CUDA;
     }
@@ -756,14 +789,14 @@ int host_step(const void* q, const void* k, const void* v, const int32_t* block_
   constexpr size_t kDirectOutBytes = size_t(4) << 20;
   const size_t out_bytes = static_cast<size_t>(T) * H_q * D * 2;
   const bool direct_out = dev[6] && aligned16(dev[6]) && out_bytes <= kDirectOutBytes;
-  rc = ps_attention_step(st + l.q, kv_direct ? dev[1] : st + l.k, kv_direct ? dev[2] : st + l.v,
-                         k_pool, v_pool,
-                         reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
-                         reinterpret_cast<const int32_t*>(st + l.sl),
-                         reinterpret_cast<const int32_t*>(st + l.qsl), B, T, H_q, H_kv, D,
-                         num_blocks, scale, direct_out ? const_cast<void*>(dev[6]) : st + l.out,
-                         reinterpret_cast<int32_t*>(st + l.slots), st + l.ws, ws_bytes, dtype,
-                         stream);
+  rc = attention_step_impl(st + l.q, kv_direct ? dev[1] : st + l.k,
+                           kv_direct ? dev[2] : st + l.v, k_pool, v_pool,
+                           reinterpret_cast<const int32_t*>(st + l.bt), max_blocks_per_seq,
+                           reinterpret_cast<const int32_t*>(st + l.sl),
+                           reinterpret_cast<const int32_t*>(st + l.qsl), B, T, H_q, H_kv, D,
+                           num_blocks, scale, direct_out ? const_cast<void*>(dev[6]) : st + l.out,
+                           reinterpret_cast<int32_t*>(st + l.slots), st + l.ws, ws_bytes, dtype,
+                           stream, pre.n > 0 ? &pre : nullptr);
   if (rc || direct_out) return rc;
   if (dev[6] && out_bytes % 4 == 0) {
     ps::CopySegments o{};

@@ -248,7 +248,8 @@ constexpr int kPlanRankSeqs = 512;  // tile sequences up to which every rank goe
 constexpr int kPlanMaxCtas = 64;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int concurrency,
-                                                    int tile_ctas, int plan_ctas) {
+                                                    int tile_ctas, int plan_ctas,
+                                                    const CopySegments pre, int copy_ctas) {
   __shared__ int4 sh4[32];
   __shared__ Sum3 shl[32];
   extern __shared__ int plan_smem[];
@@ -260,13 +261,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnParams p, int conc
   // only once their lists are written: those CTAs, resident early and waiting, slowed the
   // planner's own passes.
   pdl_wait();
+  // The last copy_ctas CTAs copy inputs that only the later kernels read (the queries,
+  // from page-locked host memory), beside the planning and the scatter.
+  const int first_copy = static_cast<int>(gridDim.x) - copy_ctas;
+  if (static_cast<int>(blockIdx.x) >= first_copy) {
+    copy_segments(pre, static_cast<int64_t>(static_cast<int>(blockIdx.x) - first_copy) * nth + tid,
+                  static_cast<int64_t>(copy_ctas) * nth);
+    return;
+  }
   if (static_cast<int>(blockIdx.x) >= plan_ctas) {
     scatter_step_tokens(static_cast<const uint4*>(p.new_k), static_cast<const uint4*>(p.new_v),
                         p.block_tables, p.max_blocks, p.seq_lens, p.qsl, p.B, p.T,
                         p.H_kv * p.D / 8, p.num_blocks, p.slots, static_cast<uint4*>(p.k_pool),
                         static_cast<uint4*>(p.v_pool), p.err,
                         (static_cast<int>(blockIdx.x) - plan_ctas) * (nth >> 5) + (tid >> 5),
-                        (static_cast<int>(gridDim.x) - plan_ctas) * (nth >> 5));
+                        (first_copy - plan_ctas) * (nth >> 5));
     return;
   }
   const bool in_smem = p.B <= kPlanSmemSeqs;
@@ -1128,7 +1137,7 @@ static int plan_threads(int B) {
 }
 
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int num_sms,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const CopySegments* pre) {
   const int smem =
       p.B <= kPlanSmemSeqs ? kPlanSmemArrays * (p.B + 1) * static_cast<int>(sizeof(int)) : 0;
   if (smem > 48 * 1024) {
@@ -1150,10 +1159,22 @@ cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int
     const int64_t cap = static_cast<int64_t>(num_sms) * 64 / warps;
     if (scatter > cap) scatter = cap;
   }
+  // the copy CTAs: one 16-byte word per thread and round, at most two CTAs per SM
+  CopySegments segs{};
+  int64_t copies = 0;
+  if (pre != nullptr && pre->n > 0) {
+    segs = *pre;
+    int64_t words = 0;
+    for (int k = 0; k < segs.n; ++k) words += segs.seg[k].bytes / 16 + 1;
+    copies = (words + threads - 1) / threads;
+    const int64_t cap = 2 * static_cast<int64_t>(num_sms);
+    if (copies > cap) copies = cap;
+  }
   // programmatic dependent launch: the CTAs may start while the kernel before them on the
   // stream finishes (see plan_kernel for what they wait for, and when)
-  return launch_kernel(plan_kernel, dim3(static_cast<unsigned>(ctas + scatter)), dim3(threads),
-                       static_cast<size_t>(smem), stream, true, p, concurrency, tile_ctas, ctas);
+  return launch_kernel(plan_kernel, dim3(static_cast<unsigned>(ctas + scatter + copies)),
+                       dim3(threads), static_cast<size_t>(smem), stream, true, p, concurrency,
+                       tile_ctas, ctas, segs, static_cast<int>(copies));
 }
 
 template <bool kBF16, int D, bool kDirect, int kS = 0>

@@ -172,9 +172,10 @@ int attention_warps(int D);
 
 // concurrency: split-kernel warps; tile_ctas: tile-kernel CTAs (work is sized for both).
 // With p.new_k set, the same launch also carries the step's KV scatter (p.new_k, p.new_v
-// into p.k_pool, p.v_pool, slots to p.slots) on extra CTAs beside the planning ones.
+// into p.k_pool, p.v_pool, slots to p.slots) on extra CTAs beside the planning ones; with
+// `pre`, further CTAs make those copies (inputs that only the later kernels read).
 cudaError_t launch_plan(const AttnParams& p, int concurrency, int tile_ctas, int num_sms,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const CopySegments* pre = nullptr);
 
 // Query tokens per 128-row tile for G query heads per KV head (0 = use the split kernel).
 int tile_tokens(int G);
@@ -237,10 +238,13 @@ size_t partial_bytes(int64_t cap_part, int D);
 bool layout_workspace(AttnParams& p, uint8_t* ws, size_t bytes, bool shrink);
 
 // The new tokens' K/V to scatter into the pools (the scatter writes their slots into
-// AttnParams::slots).
+// AttnParams::slots), and copies still to make before the attention kernels read their
+// destinations (the host step's queries): on extra CTAs of the planner's launch, or by a
+// gather kernel first when the step has no planner.
 struct ScatterArgs {
   const void* k;
   const void* v;
+  const CopySegments* pre = nullptr;
 };
 
 // Plan, [KV scatter], split kernel, tile kernel, combine on `s` (p's problem and workspace

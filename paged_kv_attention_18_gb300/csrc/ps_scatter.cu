@@ -115,22 +115,8 @@ cudaError_t launch_step_scatter(const void* k, const void* v, const int32_t* blo
 __global__ void __launch_bounds__(256) gather_in_kernel(const CopySegments segs) {
   pdl_wait();
   pdl_launch_dependents();
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int k = 0; k < segs.n; ++k) {
-    const CopySegment& c = segs.seg[k];
-    const bool wide = ((reinterpret_cast<uintptr_t>(c.dst) | reinterpret_cast<uintptr_t>(c.src) |
-                        static_cast<uintptr_t>(c.bytes)) & 15u) == 0;
-    if (wide) {
-      const uint4* src = static_cast<const uint4*>(c.src);
-      uint4* dst = static_cast<uint4*>(c.dst);
-      for (int64_t i = tid; i < c.bytes / 16; i += nth) dst[i] = src[i];
-    } else {
-      const uint32_t* src = static_cast<const uint32_t*>(c.src);
-      uint32_t* dst = static_cast<uint32_t*>(c.dst);
-      for (int64_t i = tid; i < c.bytes / 4; i += nth) dst[i] = src[i];
-    }
-  }
+  copy_segments(segs, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                static_cast<int64_t>(gridDim.x) * blockDim.x);
 }
 
 cudaError_t launch_gather_in(const CopySegments& segs, int num_sms, cudaStream_t stream,

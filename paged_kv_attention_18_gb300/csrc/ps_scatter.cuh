@@ -6,8 +6,30 @@
 // context (PageServe, section 01 "Scheduler loop"; section 03 "Paged KV cache").
 #pragma once
 #include "ps_common.cuh"
+#include "ps_launch.h"
 
 namespace ps {
+
+// Copies of whole buffers by a set of threads (thread index tid of nth): 16-byte words
+// where both addresses and the size allow, 4-byte words otherwise. Used by the gather
+// kernel and by the planner's copy CTAs; either side may be page-locked host memory seen
+// through its device address.
+__device__ __forceinline__ void copy_segments(const CopySegments& segs, int64_t tid, int64_t nth) {
+  for (int k = 0; k < segs.n; ++k) {
+    const CopySegment& c = segs.seg[k];
+    const bool wide = ((reinterpret_cast<uintptr_t>(c.dst) | reinterpret_cast<uintptr_t>(c.src) |
+                        static_cast<uintptr_t>(c.bytes)) & 15u) == 0;
+    if (wide) {
+      const uint4* src = static_cast<const uint4*>(c.src);
+      uint4* dst = static_cast<uint4*>(c.dst);
+      for (int64_t i = tid; i < c.bytes / 16; i += nth) dst[i] = src[i];
+    } else {
+      const uint32_t* src = static_cast<const uint32_t*>(c.src);
+      uint32_t* dst = static_cast<uint32_t*>(c.dst);
+      for (int64_t i = tid; i < c.bytes / 4; i += nth) dst[i] = src[i];
+    }
+  }
+}
 
 // Sequence of packed token t: the largest b in [0, B) with qsl[b] <= t (empty sequences
 // share their start with the next one), found by the whole warp in 32-way rounds, so a
