@@ -158,14 +158,19 @@ def test_host_step_graph_empty_batch():
     assert np.array_equal(host_bits(pools.k), wl.k_pool)
 
 
-def test_host_step_large_output_matches_device_step():
-    # a 25 MB output (the chunked-prefill step) is written to the staging buffer and then
-    # moved to the page-locked host buffer by a kernel after the step (small outputs are
-    # written there by the step's own kernels): bit-identical to the device entry point's
-    # output on the same inputs, in a fresh pool each
-    wl = W.named("prefix_chunked_prefill")
+@pytest.mark.parametrize("name,batch", [("tiny_decode", None), ("qwen05b_mixed", None),
+                                        ("qwen15b_decode", 64), ("prefix_chunked_prefill", None)])
+def test_host_step_matches_device_step(name, batch):
+    # Each path of the host step with page-locked buffers:
+    #   - tiny decode: direct split mode, the query copy a gather kernel first;
+    #   - mixed: the tile kernel's direct mode, likewise;
+    #   - 64 decodes: the planner, with the query copy on its extra CTAs and the output
+    #     written into the host buffer by the step's kernels;
+    #   - chunked prefill: the planner, with a 25 MB output moved by a kernel after the step.
+    # Each must be bit-identical to the device entry point's output on the same inputs, in
+    # a fresh pool each, and leave the same pools.
+    wl = W.named(name, batch=batch) if batch else W.named(name)
     st = wl.steps[0]
-    assert st.T * wl.H_q * wl.D * 2 > 4 << 20
     dt = wl.dtype
     pools_d = DevicePools(wl)
     q, k, v = dev(st.q, dt), dev(st.k, dt), dev(st.v, dt)
