@@ -1050,14 +1050,35 @@ template <bool kBF16, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  const int n = *reinterpret_cast<volatile const int*>(p.hdr + 7) * p.H_q;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wid < n; wid += nwarps) {
+  int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // The warp's list entry is read beside the count (the list has room for T entries, so
+  // the read stays in bounds; the entry is used only below the count).
+  int tok_next = wid / p.H_q < p.T ? p.tok_list[wid / p.H_q] : 0;
+  const int n = *reinterpret_cast<volatile const int*>(p.hdr + 7) * p.H_q;
+  constexpr int kPer = D / 32;  // elements per lane
+  for (; wid < n; wid += nwarps) {
     const int li = wid / p.H_q, h = wid - li * p.H_q;
-    const int tok = p.tok_list[li];
+    const int tok = tok_next;
+    const int li_next = (wid + nwarps) / p.H_q;
+    tok_next = li_next < p.T ? p.tok_list[li_next] : 0;
     const int ns = p.tok_ns[tok];
     const int base = p.tok_base[tok];
+    // the first round's partials are loaded beside the log-sum-exps (they do not need them)
+    auto load = [&](int s) -> float4 {
+      const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        return *reinterpret_cast<const float4*>(src);
+      } else {
+        const float2 v2 = *reinterpret_cast<const float2*>(src);
+        return make_float4(v2.x, v2.y, 0.f, 0.f);
+      }
+    };
+    float4 v[kCombineUnroll];
+#pragma unroll
+    for (int u = 0; u < kCombineUnroll; ++u)
+      v[u] = u < ns ? load(u) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float lse = lane < ns ? p.part_lse[base + lane * p.H_q + h] : -INFINITY;
     float M = lse;
 #pragma unroll
@@ -1066,38 +1087,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     float Wsum = w;
 #pragma unroll
     for (int o = 16; o; o >>= 1) Wsum += __shfl_xor_sync(0xffffffffu, Wsum, o);
-    constexpr int kPer = D / 32;  // elements per lane
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     // kCombineUnroll partials' loads in flight per round
     for (int s0 = 0; s0 < ns; s0 += kCombineUnroll) {
-      float ws[kCombineUnroll];
-      float4 v[kCombineUnroll];
+      if (s0 > 0) {
 #pragma unroll
-      for (int u = 0; u < kCombineUnroll; ++u) {
-        const int s = s0 + u;
-        ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s < ns) {
-          const float* src = p.part_o + static_cast<int64_t>(base + s * p.H_q + h) * D + lane * kPer;
-          if constexpr (kPer == 4) {
-            v[u] = *reinterpret_cast<const float4*>(src);
-          } else {
-            const float2 v2 = *reinterpret_cast<const float2*>(src);
-            v[u] = make_float4(v2.x, v2.y, 0.f, 0.f);
-          }
-        } else {
-          ws[u] = 0.f;
-        }
+        for (int u = 0; u < kCombineUnroll; ++u)
+          v[u] = s0 + u < ns ? load(s0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kCombineUnroll; ++u) {
-        acc[0] += ws[u] * v[u].x;
-        acc[1] += ws[u] * v[u].y;
+        const float ws = s0 + u < ns ? __shfl_sync(0xffffffffu, w, (s0 + u) & 31) : 0.f;
+        acc[0] += ws * v[u].x;
+        acc[1] += ws * v[u].y;
         if constexpr (kPer == 4) {
-          acc[2] += ws[u] * v[u].z;
-          acc[3] += ws[u] * v[u].w;
+          acc[2] += ws * v[u].z;
+          acc[3] += ws * v[u].w;
         }
       }
     }
@@ -1105,10 +1112,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(tok) * p.H_q + h) * D +
                     lane * kPer;
     if constexpr (kPer == 4) {
-      uint2 v;
-      v.x = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
-      v.y = pack2<kBF16>(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2*>(dst) = v;
+      uint2 o;
+      o.x = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
+      o.y = pack2<kBF16>(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = o;
     } else {
       *reinterpret_cast<uint32_t*>(dst) = pack2<kBF16>(acc[0] * inv, acc[1] * inv);
     }
