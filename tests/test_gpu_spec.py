@@ -68,6 +68,34 @@ def test_matches_oracle(B, k, V, mode):
         assert 0 < ref[1].mean() < k  # both accepting and rejecting paths ran
 
 
+def test_modes_in_turn_share_one_workspace():
+    # greedy, draft-model and one-hot calls in turn through one workspace: each call writes
+    # every entry it later reads, so no mode sees another's stale sums or maxima
+    B, k, V = 40, 3, 20000
+    p, q, drafts, rnd = make_case(B, k, V, seed=321)
+    am = p.argmax(axis=-1)[:, :k]
+    gd = np.where(np.arange(B)[:, None] % 2 == 0, am, drafts).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    ws = torch.empty(max(int(binding.lib().ps_spec_accept_workspace_size(B, k, V)), 256),
+                     dtype=torch.uint8, device="cuda")
+    pd, qd, rd = dev(p), dev(q), dev(rnd.view(np.int32))
+    cases = [
+        (lambda: binding.spec_accept(pd, dev(gd), None, None, greedy=True, workspace=ws),
+         oracle.spec_accept(p, gd, greedy=True)),
+        (lambda: binding.spec_accept(pd, dev(drafts), rd, qd, workspace=ws),
+         oracle.spec_accept(p, drafts, rnd, q)),
+        (lambda: binding.spec_accept(pd, dev(drafts), rd, None, workspace=ws),
+         oracle.spec_accept(p, drafts, rnd, None)),
+    ]
+    for _ in range(2):
+        for call, ref in cases:
+            out, num = call()
+            torch.cuda.synchronize()
+            assert binding.device_error() == 0
+            np.testing.assert_array_equal(num.cpu().numpy(), ref[1])
+            np.testing.assert_array_equal(out.cpu().numpy(), ref[0])
+
+
 def test_full_vocabulary_batch():
     # 132 sequences x (4 drafts + bonus) over a 151936-token vocabulary
     B, k, V = 132, 4, 151936
