@@ -769,8 +769,11 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
                "api": ("ps_attention_step_host (pinned host buffers, stream sync per step)"
                        if args.e2e_eager else
                        "ps_attention_step_host_graph_create once per engine step, then "
-                       "ps_graph_launch each step: the copies in from pinned host buffers, the "
-                       "step and the copy out, stream sync per step")}
+                       "ps_graph_launch each step: the inputs read from the pinned host "
+                       "buffers (block tables, lengths and offsets by a gather kernel, the "
+                       "queries by the planner's copy CTAs, the new K/V by the scatter), the "
+                       "step, the output written into the pinned buffer by the step's "
+                       "kernels; stream sync per step")}
         del wl
     del head_dw
     torch.cuda.empty_cache()
